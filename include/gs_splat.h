@@ -1,0 +1,233 @@
+/*
+ * gs_splat.h -- C ABI of the GB300 (sm_103a) tile-binned Gaussian-splat
+ * raster library (libgs_splat_gb300.so).
+ *
+ * The path has four calls, in order:
+ *   gs_isect_tiles    tile rect of every splat, 64-bit intersection keys
+ *                     (camera | tile | depth bits) with flatten ids, sorted
+ *   gs_tile_offsets   first list position of every tile
+ *   gs_rasterize_fwd  front-to-back compositing of each tile's sorted list
+ *   gs_rasterize_bwd  reverse walk giving per-splat gradients
+ *
+ * Sources (page title, file, function):
+ *   gsplat 1.0.0, data/ext/gsplat_native/intersections.c:
+ *       gs_tile_bits, gs_bounds, gs_isect_tiles, gs_radix_sort_without_gvl,
+ *       gs_offset_encode
+ *   gsplat 1.0.0, data/ext/gsplat_native/raster_backward.c and
+ *       raster_backward_bridge.c: gs_raster_backward_pixel,
+ *       gs_raster_backward_without_gvl, gs_raster_backward
+ *   rlx-metal 0.2.9, src/splat_training.rs: training_forward_metal_traced
+ *       (alpha_cutoff, transmittance_threshold)
+ *
+ * Conventions for every call:
+ *   - Array arguments are DEVICE pointers owned by the caller, C-contiguous,
+ *     row-major, in the dtype named.  Host pointers are marked "host".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it; no call synchronises it except the
+ *     size query of gs_isect_tiles (documented there).
+ *   - The library never allocates device memory.  Scratch space is the
+ *     caller's `workspace` (size from the matching *_workspace_size call).
+ *   - Every call returns a gs_status.  Argument errors are found on the host
+ *     before anything is enqueued, and nothing is written then.  Errors only
+ *     the GPU can see (a key outside the grid, a total that differs from the
+ *     caller's, a wait that ran out) are written to `d_status`, an optional
+ *     device int32 that the caller zeroes beforehand; the library only ever
+ *     stores a nonzero code there (the first error wins).  NULL = not reported.
+ *   - No call traps, asserts or aborts.
+ */
+#ifndef GS_SPLAT_H
+#define GS_SPLAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gs_status {
+    GS_OK = 0,
+    GS_ERR_INVALID_ARG = 1,    /* bad pointer, size, shape or option          */
+    GS_ERR_CAPACITY = 2,       /* more intersections than the buffers hold   */
+    GS_ERR_KEY_OUT_OF_GRID = 3,/* key names camera >= C or tile >= TW*TH     */
+    GS_ERR_WORKSPACE = 4,      /* workspace missing or smaller than needed   */
+    GS_ERR_TIMEOUT = 5,        /* a bounded inter-block wait ran out         */
+    GS_ERR_CUDA = 6,           /* a CUDA runtime call failed                 */
+    GS_ERR_UNSORTED = 7,       /* gs_tile_offsets was given unsorted keys    */
+    GS_ERR_COUNT_MISMATCH = 8  /* n_isects differs from the emitted total    */
+} gs_status;
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gs_version(void);
+
+/* Static English text for a status code. */
+const char* gs_status_string(int status);
+
+/* gsplat 1.0.0, intersections.c, gs_tile_bits: the fewest bits b with
+ * 2^b >= tile_width * tile_height (0 for a single tile). */
+int gs_tile_bits(int tile_width, int tile_height);
+
+/* Bytes of workspace gs_isect_tiles needs.  n_isects = 0 gives the size of
+ * the size-query call; the emitting call needs the size for its n_isects. */
+size_t gs_isect_workspace_size(int C, int N, int tile_width, int tile_height,
+                               int64_t n_isects, int sort);
+
+/*
+ * gs_isect_tiles -- gsplat 1.0.0, intersections.c, gs_bounds and
+ * gs_isect_tiles (+ gs_radix_sort_without_gvl when sort != 0).
+ *
+ * Inputs (device):
+ *   means2d  float32 (C, N, 2)   splat centres in pixels
+ *   radii    float32 (C, N) if elliptical == 0 (isotropic, ry = rx),
+ *            float32 (C, N, 2) if elliptical != 0 (rx, ry)
+ *   depths   float32 (C, N)
+ * Per splat i = c*N + n the tile rect is
+ *   x0 = clamp(floor((mx - rx) / tile_size), 0, tile_width)
+ *   x1 = clamp(ceil ((mx + rx) / tile_size), 0, tile_width)   (y likewise)
+ * in IEEE single precision; rx <= 0 or ry <= 0, or a non-finite mean or
+ * radius, gives an empty rect; a finite value beyond the grid clamps to
+ * its edge.  tiles_per_gauss[i] = (x1 - x0) * (y1 - y0).
+ * For every covered tile (ty, tx) one intersection is emitted:
+ *   key = ((c << tile_bits | (ty * tile_width + tx)) << 32) | bits(depth_i)
+ *   flatten_id = c*N + n
+ * With sort == 0 they are in emission order (camera, splat, ty, tx); with
+ * sort != 0 they are sorted ascending by key, equal keys in emission order
+ * (a stable sort).  Both orders match the CPU listing bit for bit.
+ *
+ * Two calls:
+ *   1. Size query: keys == NULL.  Writes tiles_per_gauss (if not NULL) and
+ *      the total count I to *h_n_isects (host).  This call synchronises
+ *      `stream`, because the caller must size keys/flatten_ids from I.
+ *      workspace needs gs_isect_workspace_size(C, N, TW, TH, 0, sort).
+ *   2. Emit: keys != NULL, n_isects = I from the query.  Writes keys
+ *      uint64 (I), flatten_ids int32 (I) and, if not NULL, tiles_per_gauss
+ *      int32 (C, N).  Asynchronous.  If the emitted total differs from
+ *      n_isects, GS_ERR_COUNT_MISMATCH goes to d_status and at most
+ *      n_isects entries are written.
+ * Limits: C >= 1, N >= 0, C*N < 2^31, tile_size >= 1, tile dims >= 1,
+ * tile_bits + bitlen(C-1) <= 32, I < 2^31.
+ */
+int gs_isect_tiles(const float* means2d, const float* radii, int elliptical,
+                   const float* depths, int C, int N, int tile_size,
+                   int tile_width, int tile_height, int sort,
+                   int32_t* tiles_per_gauss, int64_t* h_n_isects,
+                   uint64_t* keys, int32_t* flatten_ids, int64_t n_isects,
+                   void* workspace, size_t workspace_bytes,
+                   int32_t* d_status, void* stream);
+
+/*
+ * gs_tile_offsets -- gsplat 1.0.0, intersections.c, gs_offset_encode.
+ * offsets int32 (C, tile_height, tile_width): offsets[t] = number of keys
+ * whose tile (camera * tile_width * tile_height + tile) is below t, i.e. the
+ * first list position of tile t; an empty tile gets the next tile's start.
+ * A tile's list ends at offsets[t + 1], or at n_isects for the last tile.
+ * keys must be sorted ascending (as gs_isect_tiles with sort != 0 leaves
+ * them): the start of each tile is found where the tile id changes.
+ * Out-of-grid keys (camera >= C or tile >= TW*TH) report
+ * GS_ERR_KEY_OUT_OF_GRID and unsorted keys GS_ERR_UNSORTED in d_status;
+ * offsets are then unspecified.
+ */
+int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
+                    int tile_width, int tile_height, int32_t* offsets,
+                    int32_t* d_status, void* stream);
+
+/*
+ * gs_rasterize_fwd -- front-to-back compositing (the recurrence whose
+ * reverse walk is gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel;
+ * parameters of rlx-metal 0.2.9, splat_training.rs).
+ * For pixel (x, y) of camera c in tile t, over list positions
+ * j = offsets[t] .. end(t)-1, g = flatten_ids[j]:
+ *   d = means2d[g] - (x + 0.5, y + 0.5)
+ *   s = 0.5 (a dx^2 + c dy^2) + b dx dy      conics[g] = (a, b, c)
+ *   skip unless s >= 0;  alpha = min(0.99, opacities[g] exp(-s))
+ *   skip if alpha < alpha_cutoff
+ *   rgb += T alpha colors[g];  T *= 1 - alpha;  last = j
+ *   stop once T < transmittance_threshold (after compositing that splat)
+ * render_colors = rgb + T * backgrounds[c] (0 if backgrounds == NULL),
+ * render_alphas = 1 - T, last_ids = last (-1 if none).  A tile with
+ * masks[t] == 0 composites nothing.
+ * Inputs: means2d (C,N,2), conics (C,N,3), colors (C,N,channels),
+ *   opacities (C,N), backgrounds (C,channels) or NULL, masks int32
+ *   (C,TH,TW) or NULL, offsets int32 (C,TH,TW), flatten_ids int32
+ *   (n_isects) -- flatten ids index the (C*N) splat arrays.
+ * Outputs: render_colors float32 (C,H,W,channels), render_alphas float32
+ *   (C,H,W,1), last_ids int32 (C,H,W); pair_counts int32 (C,H,W,2) or NULL:
+ *   per pixel the list entries visited before it stopped and the entries it
+ *   composited (a work measure, e.g. for throughput accounting).
+ * Supported: channels == 3, tile_size == 16; TH = ceil(H/16), TW = ceil(W/16).
+ */
+int gs_rasterize_fwd(const float* means2d, const float* conics,
+                     const float* colors, const float* opacities,
+                     const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height,
+                     int tile_size, const int32_t* offsets,
+                     const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, float transmittance_threshold,
+                     float* render_colors, float* render_alphas,
+                     int32_t* last_ids, int32_t* pair_counts,
+                     int32_t* d_status, void* stream);
+
+/*
+ * gs_rasterize_bwd -- gsplat 1.0.0, raster_backward.c,
+ * gs_raster_backward_pixel / gs_raster_backward_without_gvl, and
+ * raster_backward_bridge.c, gs_raster_backward (argument and output sets).
+ * Per pixel the list is walked from its end to its start.  With
+ * T = 1 - render_alpha, T_after = 1, rem = background (or 0), a pair j is
+ * valid when render_alpha > 0, s >= 0, alpha >= alpha_cutoff,
+ * last_ids >= j, T < 1 and alpha < 1; then
+ *   T_before = T / (1 - alpha), vis = T_before alpha
+ *   dL/dcolors += g_rgb vis
+ *   g_alpha = T_before (sum_ch g_rgb (color - rem) + g_a T_after)
+ *   g_raw = raw < 0.99 ? g_alpha : 0;  dL/dopacities += g_raw exp(-s)
+ *   g_s = -g_raw raw
+ *   dL/dmeans2d += g_s (a dx + b dy, c dy + b dx)
+ *   dL/dconics  += g_s (dx^2 / 2, dx dy, dy^2 / 2)
+ *   rem = alpha color + (1 - alpha) rem; T_after *= 1 - alpha; T = T_before
+ * dL/dbackgrounds += g_rgb (1 - render_alpha) per pixel.
+ * grad_means2d_abs (absgrad, optional) sums |dL/dmeans2d| per pixel term.
+ * Inputs: the forward's inputs (means2d ... n_isects, alpha_cutoff),
+ *   render_alphas float32 (C,H,W,1), last_ids int32 (C,H,W),
+ *   grad_render_colors float32 (C,H,W,channels),
+ *   grad_render_alphas float32 (C,H,W,1).
+ * Outputs (zeroed by this call, then accumulated with atomics, so the sum
+ * order and the last bits vary from run to run):
+ *   grad_means2d (C,N,2), grad_conics (C,N,3), grad_colors (C,N,channels),
+ *   grad_opacities (C,N); grad_backgrounds (C,channels) or NULL;
+ *   grad_means2d_abs (C,N,2) or NULL.
+ * Supported: channels == 3, tile_size == 16.
+ */
+int gs_rasterize_bwd(const float* means2d, const float* conics,
+                     const float* colors, const float* opacities,
+                     const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height,
+                     int tile_size, const int32_t* offsets,
+                     const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, const float* render_alphas,
+                     const int32_t* last_ids, const float* grad_render_colors,
+                     const float* grad_render_alphas, float* grad_means2d,
+                     float* grad_conics, float* grad_colors,
+                     float* grad_opacities, float* grad_backgrounds,
+                     float* grad_means2d_abs, int32_t* d_status,
+                     void* stream);
+
+/* Bytes of workspace gs_sort_pairs needs for n pairs. */
+size_t gs_sort_workspace_size(int64_t n);
+
+/*
+ * gs_sort_pairs -- the stable LSD radix sort of gsplat 1.0.0,
+ * intersections.c, gs_radix_sort_without_gvl, restricted to the bits that
+ * can differ: sorts (keys uint64 (n), values int32 (n)) in place, ascending
+ * by bits [begin_bit, end_bit) of the key, equal digits keeping their input
+ * order.  With begin_bit = 0, end_bit = 64 this is the listing's sort; when
+ * the key bits outside the range are equal across all keys the result is
+ * the full stable sort.  0 <= begin_bit <= end_bit <= 64, n < 2^31.
+ */
+int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit,
+                  int end_bit, void* workspace, size_t workspace_bytes,
+                  int32_t* d_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_SPLAT_H */

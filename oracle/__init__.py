@@ -52,7 +52,7 @@ def lib():
         L.orc_rasterize_fwd_f64.restype = I32
         L.orc_rasterize_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                         P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
-                                        F32]
+                                        F32, P]
         L.orc_rasterize_bwd.restype = I32
         _lib = L
     return _lib
@@ -195,10 +195,11 @@ def rasterize_fwd_f64(means2d, conics, colors, opacities, backgrounds, width, he
 def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, render_alphas, last_ids,
                   grad_render_colors, grad_render_alphas, want_grad_backgrounds=None,
-                  absgrad=False, pixels=None, tie_rel=0.0):
+                  absgrad=False, pixels=None, tie_rel=0.0, magnitudes=False):
     """Backward.  Returns dict(grad_means2d, grad_conics, grad_colors,
     grad_opacities, grad_backgrounds (or None), grad_means2d_abs (or None),
-    near_tie (C,H,W) uint8)."""
+    near_tie (C,H,W) uint8, and with magnitudes=True mag_* arrays: per
+    gradient element the sum of |per-pair term|)."""
     means2d = _c(means2d, np.float32)
     conics = _c(conics, np.float32)
     colors = _c(colors, np.float32)
@@ -224,6 +225,7 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                grad_means2d_abs=np.empty((C, N, 2), np.float32) if absgrad else None,
                near_tie=np.zeros((C, height, width), np.uint8))
     px = None if pixels is None else _c(pixels, np.int64)
+    mags = np.zeros((6 + ch) * C * N, np.float64) if magnitudes else None
     rc = lib().orc_rasterize_bwd(
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
         _ptr(masks), C, N, ch, width, height, tile_size, TW, TH, _ptr(offsets),
@@ -231,9 +233,15 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         _ptr(last_ids), _ptr(grad_render_colors), _ptr(grad_render_alphas), _ptr(px),
         0 if px is None else px.size, _ptr(out["grad_means2d"]), _ptr(out["grad_conics"]),
         _ptr(out["grad_colors"]), _ptr(out["grad_opacities"]), _ptr(out["grad_backgrounds"]),
-        _ptr(out["grad_means2d_abs"]), _ptr(out["near_tie"]), float(tie_rel))
+        _ptr(out["grad_means2d_abs"]), _ptr(out["near_tie"]), float(tie_rel), _ptr(mags))
     if rc != 0:
         raise ValueError("oracle backward: bad arguments")
+    if magnitudes:
+        CN = C * N
+        out["mag_means2d"] = mags[:2 * CN].reshape(C, N, 2)
+        out["mag_conics"] = mags[2 * CN:5 * CN].reshape(C, N, 3)
+        out["mag_colors"] = mags[5 * CN:(5 + ch) * CN].reshape(C, N, ch)
+        out["mag_opacities"] = mags[(5 + ch) * CN:].reshape(C, N)
     return out
 
 

@@ -448,6 +448,10 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
 // to float once.  pixels/n_pixels restricts the walk to listed pixels.
 // near_tie (optional, per pixel) marks pixels where alpha was within tie_rel
 // of the cutoff or raw alpha within tie_rel of the clamp.
+// magnitudes (optional, double) receives, per gradient element, the sum of
+// the absolute values of its per-pair terms, laid out as grad_means2d (2CN),
+// grad_conics (3CN), grad_colors (channels*CN), grad_opacities (CN): the
+// scale of the rounding error any other summation order makes.
 int orc_rasterize_bwd(const float* means2d, const float* conics, const float* colors,
                       const float* opacities, const float* backgrounds, const int32_t* masks,
                       int64_t C, int64_t N, int channels, int width, int height, int tile_size,
@@ -458,11 +462,17 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                       const int64_t* pixels, int64_t n_pixels, float* grad_means2d,
                       float* grad_conics, float* grad_colors, float* grad_opacities,
                       float* grad_backgrounds, float* grad_means2d_abs, uint8_t* near_tie,
-                      float tie_rel) {
+                      float tie_rel, double* magnitudes) {
     if (channels < 1 || channels > 64) return 1;
     int64_t CN = C * N;
     std::vector<double> gm(2 * CN, 0.0), gq(3 * CN, 0.0), gc((size_t)channels * CN, 0.0),
         go(CN, 0.0), gb((size_t)channels * C, 0.0), gma(2 * CN, 0.0);
+    double* mag_m = magnitudes;
+    double* mag_q = magnitudes ? magnitudes + 2 * CN : nullptr;
+    double* mag_c = magnitudes ? magnitudes + 5 * CN : nullptr;
+    double* mag_o = magnitudes ? magnitudes + (5 + channels) * CN : nullptr;
+    if (magnitudes)
+        for (int64_t i = 0; i < (6 + (int64_t)channels) * CN; ++i) magnitudes[i] = 0.0;
     int64_t tiles = C * tile_height * tile_width;
     int64_t HW = (int64_t)width * height;
     int64_t count = pixels ? n_pixels : C * HW;
@@ -509,6 +519,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             float dot = 0.0f;
             for (int ch = 0; ch < channels; ++ch) {
                 gc[(int64_t)channels * g + ch] += (double)(g_rgb[ch] * vis);
+                if (mag_c) mag_c[(int64_t)channels * g + ch] += std::fabs((double)(g_rgb[ch] * vis));
                 dot += g_rgb[ch] * (col[ch] - rem[ch]);
             }
             float g_alpha = Tb * (dot + g_a * Ta);
@@ -524,6 +535,14 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             gq[3 * g] += (double)(g_s * 0.5f * dx * dx);
             gq[3 * g + 1] += (double)(g_s * dx * dy);
             gq[3 * g + 2] += (double)(g_s * 0.5f * dy * dy);
+            if (magnitudes) {
+                mag_m[2 * g] += std::fabs((double)gmx);
+                mag_m[2 * g + 1] += std::fabs((double)gmy);
+                mag_q[3 * g] += std::fabs((double)(g_s * 0.5f * dx * dx));
+                mag_q[3 * g + 1] += std::fabs((double)(g_s * dx * dy));
+                mag_q[3 * g + 2] += std::fabs((double)(g_s * 0.5f * dy * dy));
+                mag_o[g] += std::fabs((double)(g_raw * resp));
+            }
             for (int ch = 0; ch < channels; ++ch)
                 rem[ch] = alpha * col[ch] + (1.0f - alpha) * rem[ch];
             Ta *= 1.0f - alpha;

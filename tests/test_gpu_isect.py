@@ -1,0 +1,183 @@
+"""GPU parity of intersection, sort and tile ranges (gs_isect_tiles,
+gs_tile_offsets, gs_sort_pairs) against the oracle: bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import DEV, gpu_isect, scene_to_dev, to_dev, u64
+from tile_gaussian_splat_gb300 import binding as gs
+from tile_gaussian_splat_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_isect(s, sort=True):
+    d = scene_to_dev(s)
+    st = gs.new_status(DEV)
+    tpg, keys, ids = gpu_isect(s, d, sort=sort, status=st)
+    gs.check_status(st)
+    r_tpg, r_keys, r_ids = oracle.isect_tiles(s.means2d, s.radii, s.depths, s.tile_size,
+                                              s.tile_width, s.tile_height, sort=sort)
+    np.testing.assert_array_equal(tpg.cpu().numpy(), r_tpg)
+    assert keys.numel() == r_keys.size
+    np.testing.assert_array_equal(u64(keys), r_keys)
+    np.testing.assert_array_equal(ids.cpu().numpy(), r_ids)
+    if keys.numel():
+        off = gs.gs_tile_offsets(keys, s.C, s.tile_width, s.tile_height, d_status=st) \
+            if sort else None
+        if sort:
+            gs.check_status(st)
+            np.testing.assert_array_equal(
+                off.cpu().numpy(), oracle.tile_offsets(r_keys, s.C, s.tile_width, s.tile_height))
+    return r_keys.size
+
+
+@pytest.mark.parametrize("k", [1, 2, 5])
+@pytest.mark.parametrize("sort", [True, False])
+def test_workloads_small(k, sort):
+    assert _check_isect(scenes.workload(k), sort=sort) > 0
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_multi_camera_ragged(seed):
+    # 3 cameras, ragged 200x120 image (13x8 tiles), big radii: many tiles per splat,
+    # I spans several sort tiles with a ragged tail
+    s = scenes.random_small(seed, C=3, N=4000, W=200, H=120, sigma=(0.5, 12.0),
+                            elliptical=seed % 2 == 0)
+    n = _check_isect(s)
+    assert n > 3 * 3072
+
+
+def test_equal_depths_keep_splat_order():
+    # many equal depths and equal keys: the sort must be stable
+    s = scenes.random_small(7, C=2, N=20000, W=256, H=256, sigma=(0.5, 6.0))
+    s.depths[:] = np.round(s.depths * 2) / 2  # 19 distinct depths
+    _check_isect(s)
+
+
+def test_negative_and_special_depths():
+    s = scenes.random_small(8, C=1, N=5000, W=128, H=96)
+    s.depths[0, ::3] *= -1.0
+    s.depths[0, 1::7] = 0.0
+    s.depths[0, 2::11] = -0.0
+    _check_isect(s)
+
+
+def test_degenerate_splats():
+    s = scenes.random_small(9, C=1, N=3000, W=64, H=64)
+    s.radii[0, ::5] = 0.0
+    s.radii[0, 1::9] = -3.0
+    s.means2d[0, 2::13] = np.nan
+    s.radii[0, 3::17] = np.inf
+    s.means2d[0, 4::19] = 1e30
+    s.means2d[0, 5::23] = -1e30
+    _check_isect(s)
+
+
+def test_empty_and_invisible():
+    s = scenes.random_small(1, C=2, N=0, W=64, H=64)
+    assert _check_isect(s) == 0
+    s = scenes.random_small(1, C=2, N=100, W=64, H=64)
+    s.means2d[:] = -1000.0
+    assert _check_isect(s) == 0
+
+
+def test_single_tile_grid():
+    s = scenes.random_small(2, C=1, N=500, W=16, H=16)
+    assert _check_isect(s) > 0
+
+
+def test_max_camera_bits():
+    # tile_bits + camera bits == 32: 2^16 tiles (256x256 grid), 2^16 cameras
+    C = 65536
+    rng = np.random.default_rng(3)
+    s = scenes.random_small(3, C=1, N=1, W=16, H=16)
+    s.C, s.N, s.width, s.height = C, 1, 4096, 4096
+    s.means2d = rng.uniform(0, 4096, (C, 1, 2)).astype(np.float32)
+    s.radii = rng.uniform(1, 40, (C, 1, 2)).astype(np.float32)
+    s.depths = rng.uniform(1, 5, (C, 1)).astype(np.float32)
+    assert gs.gs_tile_bits(256, 256) == 16
+    _check_isect(s)
+
+
+def test_too_many_key_bits_rejected():
+    s = scenes.random_small(3, C=65537, N=1, W=16, H=16)
+    d = scene_to_dev(s)
+    with pytest.raises(gs.GsError) as e:
+        gs.gs_isect_tiles(d["means2d"], d["radii"], d["depths"], 16, 256, 256)
+    assert e.value.code == 1
+
+
+def test_count_mismatch_reported():
+    s = scenes.random_small(4, C=1, N=300, W=64, H=64)
+    d = scene_to_dev(s)
+    tpg, keys, ids = gpu_isect(s, d)
+    I = keys.numel()
+    ws = torch.empty(gs.gs_isect_workspace_size(1, 300, 4, 4, I - 1, True), dtype=torch.uint8,
+                     device=DEV)
+    st = gs.new_status(DEV)
+    k2 = torch.empty(I - 1, dtype=torch.int64, device=DEV)
+    i2 = torch.empty(I - 1, dtype=torch.int32, device=DEV)
+    rc = gs.lib().gs_isect_tiles(gs._ptr(d["means2d"]), gs._ptr(d["radii"]), 1,
+                                 gs._ptr(d["depths"]), 1, 300, 16, 4, 4, 1, None, None,
+                                 gs._ptr(k2), gs._ptr(i2), I - 1, gs._ptr(ws), ws.numel(),
+                                 gs._ptr(st), gs._stream())
+    assert rc == 0
+    assert int(st.item()) == 8
+
+
+def test_tile_offsets_errors():
+    tb = gs.gs_tile_bits(3, 3)
+    good = (np.uint64(4) << np.uint64(32)) | np.uint64(7)
+    bad_tile = np.uint64(12) << np.uint64(32)
+    bad_cam = np.uint64(2 << tb) << np.uint64(32)
+    for keys, code in [([good, bad_tile], 3), ([bad_cam], 3),
+                       ([good, np.uint64(1) << np.uint64(32)], 7)]:
+        k = torch.from_numpy(np.array(keys, np.uint64).view(np.int64)).to(DEV)
+        st = gs.new_status(DEV)
+        gs.gs_tile_offsets(k, 2, 3, 3, d_status=st)
+        assert int(st.item()) == code
+    st = gs.new_status(DEV)
+    off = gs.gs_tile_offsets(torch.empty(0, dtype=torch.int64, device=DEV), 2, 3, 3, d_status=st)
+    assert (off == 0).all() and int(st.item()) == 0
+
+
+@pytest.mark.parametrize("n,distinct,begin,end", [
+    (0, 1, 0, 64), (1, 1, 0, 64), (2, 2, 0, 64), (3071, 50, 0, 64), (3072, 3072, 0, 64),
+    (3073, 3, 0, 64), (100_000, 1000, 0, 64), (250_007, 250_007, 0, 64), (100_000, 77, 32, 47),
+    (65_536, 9, 5, 13)])
+def test_sort_pairs(n, distinct, begin, end):
+    rng = np.random.default_rng(n + distinct + begin)
+    pool = rng.integers(0, 2**63, distinct, dtype=np.uint64) * np.uint64(2) + \
+        rng.integers(0, 2, distinct, dtype=np.uint64)
+    keys = rng.choice(pool, n).astype(np.uint64) if n else np.zeros(0, np.uint64)
+    vals = np.arange(n, dtype=np.int32)
+    k = torch.from_numpy(keys.view(np.int64).copy()).to(DEV)
+    v = torch.from_numpy(vals.copy()).to(DEV)
+    st = gs.new_status(DEV)
+    gs.gs_sort_pairs(k, v, begin, end, d_status=st)
+    gs.check_status(st)
+    width = end - begin
+    mask = np.uint64((1 << width) - 1) if width < 64 else np.uint64(2**64 - 1)
+    digits = (keys >> np.uint64(begin)) & mask
+    perm = np.argsort(digits, kind="stable")
+    np.testing.assert_array_equal(u64(k), keys[perm])
+    np.testing.assert_array_equal(v.cpu().numpy(), vals[perm])
+    if begin == 0 and end == 64:
+        rk, rv = keys.copy(), vals.copy()
+        oracle.sort_pairs(rk, rv)
+        np.testing.assert_array_equal(u64(k), rk)
+        np.testing.assert_array_equal(v.cpu().numpy(), rv)
+
+
+def test_repeat_runs_bit_identical():
+    # races in the scan/sort would show up as run-to-run differences
+    s = scenes.workload2()
+    d = scene_to_dev(s)
+    a = gpu_isect(s, d)
+    for _ in range(3):
+        b = gpu_isect(s, d)
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)

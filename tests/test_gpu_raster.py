@@ -1,0 +1,182 @@
+"""GPU parity of forward compositing and the backward (gs_rasterize_fwd,
+gs_rasterize_bwd) against the oracle: last_ids exact and RGBA within 1e-5
+max-abs away from near-tie pixels; gradients within 1e-3 relative with a
+1e-6 absolute floor."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (DEV, RGBA_ATOL, TIE_REL, compare_forward, gpu_forward, scene_to_dev,
+                      to_dev)
+from tile_gaussian_splat_gb300 import binding as gs
+from tile_gaussian_splat_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_forward(s, masks=None):
+    iso, _ = oracle.render(s, tie_rel=TIE_REL)
+    fwd = oracle.rasterize_fwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, masks,
+                               s.width, s.height, s.tile_size, iso["offsets"],
+                               iso["flatten_ids"], s.alpha_cutoff, s.transmittance_threshold,
+                               tie_rel=TIE_REL)
+    return iso, fwd
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_forward_workloads(k):
+    s = scenes.workload(k)
+    iso, ref = _oracle_forward(s)
+    got = gpu_forward(s, scene_to_dev(s))
+    ties = compare_forward(ref, got)
+    assert ties <= 1e-3 * s.C * s.width * s.height
+
+
+@pytest.mark.parametrize("seed,W,H,C", [(0, 100, 70, 2), (1, 33, 17, 1), (2, 257, 129, 3)])
+def test_forward_ragged_with_background(seed, W, H, C):
+    s = scenes.random_small(seed, C=C, N=3000, W=W, H=H, sigma=(0.5, 10.0))
+    iso, ref = _oracle_forward(s)
+    compare_forward(ref, gpu_forward(s, scene_to_dev(s)))
+
+
+def test_forward_masks():
+    s = scenes.random_small(5, C=2, N=2000, W=96, H=64)
+    rng = np.random.default_rng(0)
+    masks = rng.integers(0, 2, (2, 4, 6)).astype(np.int32)
+    iso, ref = _oracle_forward(s, masks=masks)
+    got = gpu_forward(s, scene_to_dev(s), masks=masks)
+    compare_forward(ref, got)
+
+
+def test_forward_dense_stack_terminates():
+    # heavy overlap: most pixels stop on the transmittance threshold
+    s = scenes.random_small(6, C=1, N=6000, W=64, H=64, sigma=(3.0, 12.0), opacity=(0.5, 0.99))
+    iso, ref = _oracle_forward(s)
+    got = gpu_forward(s, scene_to_dev(s))
+    compare_forward(ref, got)
+    T = 1 - ref["render_alphas"]
+    assert (T < s.transmittance_threshold).mean() > 0.5
+
+
+def test_forward_empty_lists():
+    s = scenes.random_small(7, C=1, N=10, W=64, H=48)
+    s.means2d[:] = -500.0
+    iso, ref = _oracle_forward(s)
+    got = gpu_forward(s, scene_to_dev(s))
+    compare_forward(ref, got)
+    assert (got["last_ids"] == -1).all()
+
+
+def _bwd_case(s, masks=None, absgrad=True, seed=1):
+    iso, ref = _oracle_forward(s, masks=masks)
+    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, seed=seed)
+    rb = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, masks,
+                              s.width, s.height, s.tile_size, iso["offsets"], iso["flatten_ids"],
+                              s.alpha_cutoff, ref["render_alphas"], ref["last_ids"], g_rgb, g_a,
+                              absgrad=absgrad, tie_rel=TIE_REL, magnitudes=True)
+    d = scene_to_dev(s)
+    # the GPU backward gets the oracle's forward state, so it is compared alone
+    got = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"],
+                              d["backgrounds"], to_dev(masks), s.width, s.height, s.tile_size,
+                              to_dev(iso["offsets"]), to_dev(iso["flatten_ids"]), s.alpha_cutoff,
+                              to_dev(ref["render_alphas"]), to_dev(ref["last_ids"]),
+                              to_dev(g_rgb), to_dev(g_a), absgrad=absgrad)
+    torch.cuda.synchronize()
+    # splats touched by a near-tie pixel (either pass) are left out
+    tie_pix = (ref["near_tie"] | rb["near_tie"]).reshape(-1).astype(bool)
+    excluded = np.zeros(s.C * s.N, bool)
+    if tie_pix.any():
+        offs = iso["offsets"].reshape(-1)
+        ends = np.append(offs[1:], iso["flatten_ids"].size)
+        p = np.nonzero(tie_pix)[0]
+        c, rem = p // (s.width * s.height), p % (s.width * s.height)
+        t = (c * s.tile_height + (rem // s.width) // 16) * s.tile_width + (rem % s.width) // 16
+        for tt in np.unique(t):
+            excluded[iso["flatten_ids"][offs[tt]:ends[tt]]] = True
+    return rb, got, excluded.reshape(s.C, s.N)
+
+
+def _compare_grads(rb, got, excluded, rtol=1e-3, atol=1e-6):
+    """Strict bound |g - r| <= rtol |r| + atol on every element whose sum is
+    not dominated by cancellation; elements whose |r| is below 1e-4 of the sum
+    of |terms| (the float-summation error scale of any order) are held to
+    4e-6 of that sum instead.  Returns (checked, cancellation-bound) counts."""
+    stats = [0, 0]
+    for name, mag, w in [("grad_means2d", "mag_means2d", 2), ("grad_conics", "mag_conics", 3),
+                         ("grad_colors", "mag_colors", 3), ("grad_opacities", "mag_opacities", 1)]:
+        g = got[name].cpu().numpy().astype(np.float64)
+        r = rb[name].astype(np.float64)
+        m = rb[mag]
+        keep = ~excluded if w == 1 else np.repeat(~excluded[..., None], w, axis=-1)
+        g, r, m = g[keep], r[keep], m[keep]
+        err = np.abs(g - r)
+        cancel = np.abs(r) < 1e-4 * m
+        strict_bad = (err > rtol * np.abs(r) + atol) & ~cancel
+        assert not strict_bad.any(), (
+            f"{name}: {strict_bad.sum()} of {g.size} off; worst err "
+            f"{err[strict_bad].max()} (ref {r[strict_bad][np.argmax(err[strict_bad])]})")
+        loose_bad = (err > 4e-6 * m + atol) & cancel
+        assert not loose_bad.any(), f"{name}: {loose_bad.sum()} cancellation-bound elements off"
+        stats[0] += g.size
+        stats[1] += int(cancel.sum())
+    return stats
+
+
+def test_backward_workload5():
+    s = scenes.workload(5)
+    rb, got, excluded = _bwd_case(s, absgrad=True)
+    assert excluded.mean() < 0.02
+    checked, cancel = _compare_grads(rb, got, excluded)
+    assert cancel < 1e-3 * checked
+    np.testing.assert_allclose(got["grad_means2d_abs"].cpu().numpy()[~excluded],
+                               rb["grad_means2d_abs"][~excluded], rtol=1e-3, atol=1e-5)
+
+
+@pytest.mark.parametrize("seed,W,H,C", [(0, 100, 70, 2), (2, 257, 129, 1)])
+def test_backward_ragged_with_background(seed, W, H, C):
+    s = scenes.random_small(seed, C=C, N=3000, W=W, H=H, sigma=(0.5, 10.0))
+    rb, got, excluded = _bwd_case(s)
+    _compare_grads(rb, got, excluded)
+    np.testing.assert_allclose(got["grad_backgrounds"].cpu().numpy(), rb["grad_backgrounds"],
+                               rtol=1e-4, atol=1e-3)
+
+
+def test_backward_masks_and_dense_stack():
+    s = scenes.random_small(6, C=1, N=6000, W=64, H=64, sigma=(3.0, 12.0), opacity=(0.5, 0.99))
+    masks = np.array([[[1, 0, 1, 1], [1, 1, 0, 1], [1, 1, 1, 1], [0, 1, 1, 1]]], np.int32)
+    rb, got, excluded = _bwd_case(s, masks=masks)
+    _compare_grads(rb, got, excluded)
+
+
+def test_forward_then_backward_on_gpu_state():
+    # end to end on the GPU: the backward consumes the GPU forward's outputs
+    s = scenes.random_small(11, C=1, N=3000, W=128, H=128, sigma=(0.5, 8.0))
+    d = scene_to_dev(s)
+    f = gpu_forward(s, d)
+    g_rgb, g_a = scenes.upstream_grads(1, 128, 128, seed=1)
+    got = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"],
+                              d["backgrounds"], None, 128, 128, 16, f["offsets"],
+                              f["flatten_ids"], s.alpha_cutoff, f["render_alphas"],
+                              f["last_ids"], to_dev(g_rgb), to_dev(g_a))
+    iso, ref = _oracle_forward(s)
+    rb = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None,
+                              128, 128, 16, iso["offsets"], iso["flatten_ids"], s.alpha_cutoff,
+                              ref["render_alphas"], ref["last_ids"], g_rgb, g_a, tie_rel=TIE_REL,
+                              magnitudes=True)
+    excluded = np.zeros((1, s.N), bool)
+    if ref["near_tie"].any() or rb["near_tie"].any():
+        pytest.skip("near tie in this scene")
+    _compare_grads(rb, got, excluded)
+
+
+def test_raster_argument_errors():
+    s = scenes.random_small(1, C=1, N=10, W=32, H=32)
+    d = scene_to_dev(s)
+    off = torch.zeros((1, 2, 2), dtype=torch.int32, device=DEV)
+    ids = torch.zeros(0, dtype=torch.int32, device=DEV)
+    with pytest.raises(gs.GsError) as e:
+        gs.gs_rasterize_fwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None, None,
+                            32, 32, 8, off, ids, 1 / 255, 1e-4)
+    assert e.value.code == 1

@@ -1,0 +1,404 @@
+// C ABI of libgs_splat_gb300 (declared in include/gs_splat.h): argument
+// checks, workspace layout and the launch sequence of each call.
+//
+// gs_isect_tiles with sort != 0 produces the listing's stable sort by the
+// 64-bit key (gsplat 1.0.0, intersections.c, gs_radix_sort_without_gvl) in
+// fewer bytes moved:
+//   1. the splats are sorted by the bits of their depth (four 8-bit passes
+//      over C*N 32-bit keys, stable, so equal depths stay in index order);
+//   2. the intersections are emitted splat by splat in that order, so in
+//      every tile they already appear by (depth bits, splat index);
+//   3. a stable LSD sort on the camera|tile digits of the key's upper word
+//      (ceil((tile_bits + camera bits) / 8) passes over the I keys) then
+//      yields exactly the order of a stable sort of the full keys.
+// Every key of a splat carries the same depth bits, so its low 32 bits are
+// sorted once per splat instead of once per intersection.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/gs_splat.h"
+#include "gs_internal.h"
+
+namespace {
+
+using namespace gs;
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+int bitlen(uint64_t v) {
+    int b = 0;
+    while (v) {
+        ++b;
+        v >>= 1;
+    }
+    return b;
+}
+
+// Bump allocator over a caller buffer (or a null base when only sizing).
+struct Carver {
+    char* base;
+    size_t used = 0;
+    template <typename T>
+    T* take(size_t count) {
+        size_t at = used;
+        used = align_up(used + count * sizeof(T));
+        return base ? reinterpret_cast<T*>(base + at) : nullptr;
+    }
+};
+
+constexpr int kMaxPasses = 8;
+
+// Workspace of gs_isect_tiles.  Everything up to `zero_end` is cleared by one
+// memset per call; the sort buffers after it are fully overwritten.
+struct IsectLayout {
+    int32_t* abort_flag;
+    unsigned long long* total;
+    uint32_t* tickets;       // [2 * kMaxPasses + 1]
+    uint32_t* hist_depth;    // [4][256]
+    uint32_t* hist_up;       // [4][256]
+    uint64_t* lb_emit;       // [chunks]
+    uint64_t* lb_depth[4];   // [blocks32 * 256] each
+    uint64_t* lb_up[4];      // [blocks64 * 256] each
+    size_t zero_end;
+    uint32_t* dkeys[2];      // [C*N]
+    int32_t* dvals[2];       // [C*N]
+    uint64_t* alt_keys;      // [I]
+    int32_t* alt_ids;        // [I]
+    size_t bytes;
+};
+
+struct IsectPlan {
+    int64_t CN;
+    int tile_bits, cam_bits, up_passes;
+    bool presort;
+};
+
+IsectPlan make_plan(int C, int N, int tw, int th, int64_t n_isects, int sort) {
+    IsectPlan p;
+    p.CN = (int64_t)C * N;
+    p.tile_bits = gs_tile_bits(tw, th);
+    p.cam_bits = bitlen((uint64_t)(C > 0 ? C - 1 : 0));
+    p.up_passes = sort ? (p.tile_bits + p.cam_bits + 7) / 8 : 0;
+    p.presort = sort && n_isects > 1 && p.CN > 1;
+    if (n_isects <= 1) p.up_passes = 0;
+    return p;
+}
+
+IsectLayout carve_isect(void* ws, const IsectPlan& p, int64_t n_isects, bool query) {
+    Carver cv{static_cast<char*>(ws)};
+    IsectLayout L{};
+    L.abort_flag = cv.take<int32_t>(1);
+    L.total = cv.take<unsigned long long>(1);
+    L.tickets = cv.take<uint32_t>(2 * kMaxPasses + 1);
+    L.hist_depth = cv.take<uint32_t>(4 * 256);
+    L.hist_up = cv.take<uint32_t>(4 * 256);
+    if (!query) {
+        L.lb_emit = cv.take<uint64_t>((size_t)((p.CN + kIsectThreads - 1) / kIsectThreads));
+        if (p.presort)
+            for (int i = 0; i < 4; ++i)
+                L.lb_depth[i] = cv.take<uint64_t>((size_t)sort_blocks(p.CN, kTile32) * 256);
+        for (int i = 0; i < p.up_passes; ++i)
+            L.lb_up[i] = cv.take<uint64_t>((size_t)sort_blocks(n_isects, kTile64) * 256);
+    }
+    L.zero_end = cv.used;
+    if (!query) {
+        if (p.presort) {
+            for (int i = 0; i < 2; ++i) {
+                L.dkeys[i] = cv.take<uint32_t>((size_t)p.CN);
+                L.dvals[i] = cv.take<int32_t>((size_t)p.CN);
+            }
+        }
+        if (p.up_passes > 0) {
+            L.alt_keys = cv.take<uint64_t>((size_t)n_isects);
+            L.alt_ids = cv.take<int32_t>((size_t)n_isects);
+        }
+    }
+    L.bytes = cv.used;
+    return L;
+}
+
+int check_launch() {
+    return cudaGetLastError() == cudaSuccess ? GS_OK : GS_ERR_CUDA;
+}
+
+int isect_args_ok(const float* means2d, const float* radii, int C, int N, int tile_size,
+                  int tile_width, int tile_height) {
+    if (C < 1 || N < 0 || tile_size < 1 || tile_width < 1 || tile_height < 1) return 0;
+    if ((int64_t)C * N >= ((int64_t)1 << 31)) return 0;
+    if ((int64_t)tile_width * tile_height > ((int64_t)1 << 23)) return 0;
+    if (gs_tile_bits(tile_width, tile_height) + bitlen((uint64_t)(C - 1)) > 32) return 0;
+    if ((int64_t)C * N > 0 && (!means2d || !radii)) return 0;
+    return 1;
+}
+
+int raster_args_ok(const float* means2d, const float* conics, const float* colors,
+                   const float* opacities, int C, int N, int channels, int width, int height,
+                   int tile_size, const int32_t* offsets, const int32_t* flatten_ids,
+                   int64_t n_isects) {
+    if (C < 1 || N < 0 || width < 1 || height < 1) return 0;
+    if (channels != 3 || tile_size != 16) return 0;
+    if ((int64_t)C * N >= ((int64_t)1 << 31) || n_isects < 0 || n_isects >= ((int64_t)1 << 31))
+        return 0;
+    if (!offsets) return 0;
+    if (n_isects > 0 && (!flatten_ids || !means2d || !conics || !colors || !opacities)) return 0;
+    return 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gs_version(void) { return kVersion; }
+
+const char* gs_status_string(int status) {
+    switch (status) {
+        case GS_OK: return "ok";
+        case GS_ERR_INVALID_ARG: return "invalid argument";
+        case GS_ERR_CAPACITY: return "more intersections than the buffers hold";
+        case GS_ERR_KEY_OUT_OF_GRID: return "intersection key is outside the tile grid";
+        case GS_ERR_WORKSPACE: return "workspace missing or too small";
+        case GS_ERR_TIMEOUT: return "a bounded inter-block wait ran out";
+        case GS_ERR_CUDA: return "CUDA runtime error";
+        case GS_ERR_UNSORTED: return "keys are not sorted";
+        case GS_ERR_COUNT_MISMATCH: return "n_isects differs from the emitted total";
+        default: return "unknown status";
+    }
+}
+
+int gs_tile_bits(int tile_width, int tile_height) {
+    if (tile_width < 1 || tile_height < 1) return 0;
+    const uint64_t tiles = (uint64_t)tile_width * (uint64_t)tile_height;
+    int b = 0;
+    while (((uint64_t)1 << b) < tiles) ++b;
+    return b;
+}
+
+size_t gs_isect_workspace_size(int C, int N, int tile_width, int tile_height, int64_t n_isects,
+                               int sort) {
+    if (C < 1 || N < 0 || n_isects < 0) return 0;
+    // the emitting layout for n_isects also covers the size query's needs
+    IsectPlan p = make_plan(C, N, tile_width, tile_height, n_isects, sort);
+    return carve_isect(nullptr, p, n_isects, false).bytes;
+}
+
+int gs_isect_tiles(const float* means2d, const float* radii, int elliptical, const float* depths,
+                   int C, int N, int tile_size, int tile_width, int tile_height, int sort,
+                   int32_t* tiles_per_gauss, int64_t* h_n_isects, uint64_t* keys,
+                   int32_t* flatten_ids, int64_t n_isects, void* workspace,
+                   size_t workspace_bytes, int32_t* d_status, void* stream) {
+    if (!isect_args_ok(means2d, radii, C, N, tile_size, tile_width, tile_height))
+        return GS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool query = keys == nullptr;
+    if (query) {
+        if (!h_n_isects) return GS_ERR_INVALID_ARG;
+        IsectPlan p = make_plan(C, N, tile_width, tile_height, 0, sort);
+        IsectLayout L = carve_isect(workspace, p, 0, true);
+        if (!workspace || workspace_bytes < L.bytes) return GS_ERR_WORKSPACE;
+        if (cudaMemsetAsync(workspace, 0, L.zero_end, s) != cudaSuccess) return GS_ERR_CUDA;
+        launch_isect_count(means2d, radii, elliptical, p.CN, tile_size, tile_width, tile_height,
+                           tiles_per_gauss, L.total, s);
+        if (check_launch() != GS_OK) return GS_ERR_CUDA;
+        unsigned long long total = 0;
+        if (cudaMemcpyAsync(&total, L.total, sizeof(total), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+            return GS_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+        *h_n_isects = (int64_t)total;
+        return total >= ((unsigned long long)1 << 31) ? GS_ERR_CAPACITY : GS_OK;
+    }
+    if (n_isects < 0 || n_isects >= ((int64_t)1 << 31)) return GS_ERR_INVALID_ARG;
+    if (n_isects > 0 && (!flatten_ids || !depths)) return GS_ERR_INVALID_ARG;
+    IsectPlan p = make_plan(C, N, tile_width, tile_height, n_isects, sort);
+    IsectLayout L = carve_isect(workspace, p, n_isects, false);
+    if (!workspace || workspace_bytes < L.bytes) return GS_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, L.zero_end, s) != cudaSuccess) return GS_ERR_CUDA;
+    if (p.CN == 0) {
+        if (n_isects != 0 && d_status) {
+            const int32_t code = GS_ERR_COUNT_MISMATCH;
+            if (cudaMemcpyAsync(d_status, &code, 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return GS_ERR_CUDA;
+            if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+        }
+        return GS_OK;
+    }
+    const int32_t* order = nullptr;
+    if (p.presort) {
+        // 1. splats by depth bits, four stable passes (values start as indices)
+        const uint32_t* dbits = reinterpret_cast<const uint32_t*>(depths);
+        launch_digit_hist_u32(dbits, p.CN, 0, 32, L.hist_depth, s);
+        const uint32_t* kin = dbits;
+        const int32_t* vin = nullptr;
+        for (int pass = 0; pass < 4; ++pass) {
+            uint32_t* kout = L.dkeys[pass & 1];
+            int32_t* vout = L.dvals[pass & 1];
+            launch_onesweep_u32(kin, vin, kout, vout, p.CN, 8 * pass, 32,
+                                L.hist_depth + 256 * pass,
+                                LookbackScratch{L.lb_depth[pass], L.tickets + pass},
+                                L.abort_flag, d_status, s);
+            kin = kout;
+            vin = vout;
+        }
+        order = vin;
+    }
+    // 2. emission (into the buffer that makes the last radix pass land in keys)
+    const bool odd = (p.up_passes & 1) != 0;
+    uint64_t* ek = odd ? L.alt_keys : keys;
+    int32_t* ei = odd ? L.alt_ids : flatten_ids;
+    launch_isect_emit(means2d, radii, elliptical, depths, order, p.CN, tile_size, tile_width,
+                      tile_height, N, p.tile_bits, ek, ei, n_isects, tiles_per_gauss,
+                      LookbackScratch{L.lb_emit, L.tickets + 2 * kMaxPasses},
+                      p.up_passes ? L.hist_up : nullptr, p.up_passes, L.abort_flag, d_status, s);
+    // 3. stable passes over the camera|tile digits of the upper word
+    const int end_bit = 32 + p.tile_bits + p.cam_bits;
+    uint64_t* src_k = ek;
+    int32_t* src_i = ei;
+    for (int pass = 0; pass < p.up_passes; ++pass) {
+        uint64_t* dst_k = src_k == keys ? L.alt_keys : keys;
+        int32_t* dst_i = src_i == flatten_ids ? L.alt_ids : flatten_ids;
+        launch_onesweep_u64(src_k, src_i, dst_k, dst_i, n_isects, 32 + 8 * pass, end_bit,
+                            L.hist_up + 256 * pass,
+                            LookbackScratch{L.lb_up[pass], L.tickets + 4 + pass}, L.abort_flag,
+                            d_status, s);
+        src_k = dst_k;
+        src_i = dst_i;
+    }
+    return check_launch();
+}
+
+int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C, int tile_width,
+                    int tile_height, int32_t* offsets, int32_t* d_status, void* stream) {
+    if (C < 1 || tile_width < 1 || tile_height < 1 || !offsets) return GS_ERR_INVALID_ARG;
+    if (n_isects < 0 || n_isects >= ((int64_t)1 << 31) || (n_isects > 0 && !keys))
+        return GS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t ntiles = (int64_t)C * tile_width * tile_height;
+    if (n_isects == 0) {
+        if (cudaMemsetAsync(offsets, 0, (size_t)ntiles * sizeof(int32_t), s) != cudaSuccess)
+            return GS_ERR_CUDA;
+        return GS_OK;
+    }
+    launch_tile_ranges(keys, n_isects, C, tile_width, tile_height,
+                       gs_tile_bits(tile_width, tile_height), offsets, d_status, s);
+    return check_launch();
+}
+
+int gs_rasterize_fwd(const float* means2d, const float* conics, const float* colors,
+                     const float* opacities, const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height, int tile_size,
+                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, float transmittance_threshold, float* render_colors,
+                     float* render_alphas, int32_t* last_ids, int32_t* pair_counts,
+                     int32_t* d_status, void* stream) {
+    (void)d_status;
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects))
+        return GS_ERR_INVALID_ARG;
+    if (!render_colors || !render_alphas || !last_ids) return GS_ERR_INVALID_ARG;
+    RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
+                 C, N, width, height, (width + 15) / 16, (height + 15) / 16,
+                 offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold};
+    launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts,
+                      static_cast<cudaStream_t>(stream));
+    return check_launch();
+}
+
+int gs_rasterize_bwd(const float* means2d, const float* conics, const float* colors,
+                     const float* opacities, const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height, int tile_size,
+                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, const float* render_alphas, const int32_t* last_ids,
+                     const float* grad_render_colors, const float* grad_render_alphas,
+                     float* grad_means2d, float* grad_conics, float* grad_colors,
+                     float* grad_opacities, float* grad_backgrounds, float* grad_means2d_abs,
+                     int32_t* d_status, void* stream) {
+    (void)d_status;
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects))
+        return GS_ERR_INVALID_ARG;
+    if (!render_alphas || !last_ids || !grad_render_colors || !grad_render_alphas)
+        return GS_ERR_INVALID_ARG;
+    const int64_t CN = (int64_t)C * N;
+    if (CN > 0 && (!grad_means2d || !grad_conics || !grad_colors || !grad_opacities))
+        return GS_ERR_INVALID_ARG;
+    if (grad_backgrounds && !backgrounds) return GS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t f = sizeof(float);
+    if (CN > 0) {
+        if (cudaMemsetAsync(grad_means2d, 0, CN * 2 * f, s) != cudaSuccess ||
+            cudaMemsetAsync(grad_conics, 0, CN * 3 * f, s) != cudaSuccess ||
+            cudaMemsetAsync(grad_colors, 0, CN * 3 * f, s) != cudaSuccess ||
+            cudaMemsetAsync(grad_opacities, 0, CN * f, s) != cudaSuccess)
+            return GS_ERR_CUDA;
+        if (grad_means2d_abs && cudaMemsetAsync(grad_means2d_abs, 0, CN * 2 * f, s) != cudaSuccess)
+            return GS_ERR_CUDA;
+    }
+    if (grad_backgrounds && cudaMemsetAsync(grad_backgrounds, 0, (size_t)C * 3 * f, s) != cudaSuccess)
+        return GS_ERR_CUDA;
+    RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
+                 C, N, width, height, (width + 15) / 16, (height + 15) / 16,
+                 offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f};
+    RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
+                  grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
+                  grad_means2d_abs};
+    launch_raster_bwd(a, g, s);
+    return check_launch();
+}
+
+size_t gs_sort_workspace_size(int64_t n) {
+    if (n < 0) return 0;
+    Carver cv{nullptr};
+    cv.take<int32_t>(1);
+    cv.take<uint32_t>(kMaxPasses);
+    cv.take<uint32_t>(kMaxPasses * 256);
+    for (int i = 0; i < kMaxPasses; ++i) cv.take<uint64_t>((size_t)sort_blocks(n, kTile64) * 256);
+    cv.take<uint64_t>((size_t)n);
+    cv.take<int32_t>((size_t)n);
+    return cv.used;
+}
+
+int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit, int end_bit,
+                  void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+    if (n < 0 || n >= ((int64_t)1 << 31) || begin_bit < 0 || end_bit > 64 ||
+        begin_bit > end_bit || (n > 0 && (!keys || !values)))
+        return GS_ERR_INVALID_ARG;
+    if (n <= 1 || begin_bit == end_bit) return GS_OK;
+    if (!workspace || workspace_bytes < gs_sort_workspace_size(n)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int passes = (end_bit - begin_bit + 7) / 8;
+    Carver cv{static_cast<char*>(workspace)};
+    int32_t* abort_flag = cv.take<int32_t>(1);
+    uint32_t* tickets = cv.take<uint32_t>(kMaxPasses);
+    uint32_t* hist = cv.take<uint32_t>(kMaxPasses * 256);
+    uint64_t* lb[kMaxPasses];
+    for (int i = 0; i < kMaxPasses; ++i)
+        lb[i] = cv.take<uint64_t>((size_t)sort_blocks(n, kTile64) * 256);
+    const size_t zero_end = cv.used;
+    uint64_t* alt_k = cv.take<uint64_t>((size_t)n);
+    int32_t* alt_v = cv.take<int32_t>((size_t)n);
+    if (cudaMemsetAsync(workspace, 0, zero_end, s) != cudaSuccess) return GS_ERR_CUDA;
+    launch_digit_hist_u64(keys, n, begin_bit, end_bit, hist, s);
+    uint64_t* sk = keys;
+    int32_t* sv = values;
+    for (int pass = 0; pass < passes; ++pass) {
+        uint64_t* dk = sk == keys ? alt_k : keys;
+        int32_t* dv = sv == values ? alt_v : values;
+        launch_onesweep_u64(sk, sv, dk, dv, n, begin_bit + 8 * pass, end_bit, hist + 256 * pass,
+                            LookbackScratch{lb[pass], tickets + pass}, abort_flag, d_status, s);
+        sk = dk;
+        sv = dv;
+    }
+    if (sk != keys) {
+        if (cudaMemcpyAsync(keys, sk, (size_t)n * 8, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(values, sv, (size_t)n * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return GS_ERR_CUDA;
+    }
+    return check_launch();
+}
+
+}  // extern "C"

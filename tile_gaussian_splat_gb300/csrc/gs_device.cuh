@@ -1,0 +1,138 @@
+// Device helpers shared by the kernels of libgs_splat_gb300 (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gs_splat.h"
+
+namespace gs {
+
+constexpr int kWarp = 32;
+
+// Flags in the low two bits of a decoupled look-back word; the value sits in
+// the upper 62 bits.  0 = not yet published.
+constexpr uint64_t kFlagAggregate = 1;  // this block's own count
+constexpr uint64_t kFlagPrefix = 2;     // inclusive prefix up to this block
+constexpr uint64_t kFlagMask = 3;
+
+// Upper bound on polls of one look-back word.  A predecessor publishes within
+// microseconds; the bound only matters when something has already gone wrong,
+// and turns that into GS_ERR_TIMEOUT instead of a hang.
+constexpr int kSpinLimit = 1 << 22;
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_relaxed_i32(const int32_t* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Records the first error in the caller's status word (if any).
+__device__ __forceinline__ void report(int32_t* d_status, int code) {
+    if (d_status) atomicCAS(d_status, 0, code);
+}
+
+// Errors seen by a look-back wait: the internal abort flag (workspace) stops
+// every other waiter at once, the caller's word gets the code.
+struct ErrorSink {
+    int32_t* abort_flag;  // workspace word, zeroed per call
+    int32_t* d_status;    // caller's word or null
+    __device__ __forceinline__ void raise(int code) const {
+        atomicCAS(abort_flag, 0, code);
+        report(d_status, code);
+    }
+    __device__ __forceinline__ bool aborted() const { return ld_relaxed_i32(abort_flag) != 0; }
+};
+
+// Polls *p until a flag is set.  Returns the word, or a word flagged PREFIX
+// with value 0 after the bound (the error is raised, results are garbage but
+// nothing hangs).
+__device__ __forceinline__ uint64_t wait_published(const uint64_t* p, const ErrorSink& err) {
+    uint64_t v = ld_relaxed_u64(p);
+    int it = 0;
+    while ((v & kFlagMask) == 0) {
+        if (++it >= kSpinLimit) {
+            err.raise(GS_ERR_TIMEOUT);
+            return kFlagPrefix;
+        }
+        if ((it & 255) == 0 && err.aborted()) return kFlagPrefix;
+        __nanosleep(32);
+        v = ld_relaxed_u64(p);
+    }
+    return v;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Block-wide exclusive scan of one int64 per thread (blockDim.x == 32*W).
+// `scratch` holds >= 32 int64.  Returns the exclusive prefix; *total gets the
+// block sum.  Contains __syncthreads.
+template <int THREADS>
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* scratch,
+                                                        int64_t* total) {
+    constexpr int W = THREADS / kWarp;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t s = lane < W ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < W) scratch[lane] = s;  // inclusive warp totals
+    }
+    __syncthreads();
+    int64_t warp_prefix = warp == 0 ? 0 : scratch[warp - 1];
+    *total = scratch[W - 1];
+    return warp_prefix + x - v;
+}
+
+// Tile rect of one splat (gsplat 1.0.0, intersections.c, gs_bounds) in IEEE
+// single precision: sub and div round once each, floor/ceil are exact.  A
+// non-finite mean or radius gives the empty rect; values beyond the grid
+// clamp to its edge before conversion, so no conversion is out of range.
+struct Rect {
+    int x0, y0, x1, y1;
+};
+
+__device__ __forceinline__ int clamp_to_grid(float v, int maximum) {
+    if (!(v > 0.0f)) return 0;
+    if (v >= (float)maximum) return maximum;
+    return (int)v;
+}
+
+__device__ __forceinline__ Rect splat_rect(float mx, float my, float rx, float ry, float ts,
+                                           int tile_width, int tile_height) {
+    Rect r = {0, 0, 0, 0};
+    if (!(isfinite(mx) && isfinite(my) && isfinite(rx) && isfinite(ry))) return r;
+    if (rx <= 0.0f || ry <= 0.0f) return r;
+    r.x0 = clamp_to_grid(floorf(__fdiv_rn(__fsub_rn(mx, rx), ts)), tile_width);
+    r.y0 = clamp_to_grid(floorf(__fdiv_rn(__fsub_rn(my, ry), ts)), tile_height);
+    r.x1 = clamp_to_grid(ceilf(__fdiv_rn(__fadd_rn(mx, rx), ts)), tile_width);
+    r.y1 = clamp_to_grid(ceilf(__fdiv_rn(__fadd_rn(my, ry), ts)), tile_height);
+    return r;
+}
+
+}  // namespace gs

@@ -1,0 +1,101 @@
+// Host-side launchers shared between the translation units of
+// libgs_splat_gb300.  Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gs {
+
+// Scratch carved from the caller's workspace (all pointers device).
+struct LookbackScratch {
+    uint64_t* words;   // per-block (per-digit) look-back words, zeroed per call
+    uint32_t* ticket;  // virtual block counter, zeroed per call
+};
+
+// ---- sort.cu
+constexpr int kSortThreads = 256;
+constexpr int kItems64 = 12;  // keys per thread, 64-bit keys
+constexpr int kItems32 = 16;  // keys per thread, 32-bit keys
+constexpr int kTile64 = kSortThreads * kItems64;
+constexpr int kTile32 = kSortThreads * kItems32;
+
+inline int64_t sort_blocks(int64_t n, int tile) { return (n + tile - 1) / tile; }
+
+// Digit histograms of the 8-bit digits covering bits [shift0, end_bit),
+// accumulated into hist[pass][256] (zeroed by the caller).
+void launch_digit_hist_u64(const uint64_t* keys, int64_t n, int shift0, int end_bit,
+                           uint32_t* hist, cudaStream_t s);
+void launch_digit_hist_u32(const uint32_t* keys, int64_t n, int shift0, int end_bit,
+                           uint32_t* hist, cudaStream_t s);
+
+// One stable onesweep pass over digit bits [shift, min(shift+8, end_bit)).
+// vals_in ==
+// nullptr means values are the element indices.  lookback needs
+// sort_blocks(n, tile) * 256 words, ticket one word, both zeroed.
+void launch_onesweep_u64(const uint64_t* keys_in, const int32_t* vals_in, uint64_t* keys_out,
+                         int32_t* vals_out, int64_t n, int shift, int end_bit,
+                         const uint32_t* hist,
+                         LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                         cudaStream_t s);
+void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32_t* keys_out,
+                         int32_t* vals_out, int64_t n, int shift, int end_bit,
+                         const uint32_t* hist,
+                         LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                         cudaStream_t s);
+
+// ---- isect.cu
+constexpr int kIsectThreads = 256;
+
+void launch_isect_count(const float* means2d, const float* radii, int elliptical, int64_t CN,
+                        int tile_size, int tile_width, int tile_height, int32_t* tiles_per_gauss,
+                        unsigned long long* total, cudaStream_t s);
+
+// Emits keys/ids for splats in `order` (nullptr = index order) with a
+// decoupled look-back scan of their counts.  up_hist (may be null) receives
+// histograms of the up_passes 8-bit digits of the key's upper word.
+void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
+                       const float* depths, const int32_t* order, int64_t CN, int tile_size,
+                       int tile_width, int tile_height, int N, int tile_bits, uint64_t* keys,
+                       int32_t* ids, int64_t capacity, int32_t* tiles_per_gauss,
+                       LookbackScratch lb, uint32_t* up_hist, int up_passes,
+                       int32_t* abort_flag, int32_t* d_status, cudaStream_t s);
+
+void launch_tile_ranges(const uint64_t* keys, int64_t n, int C, int tile_width, int tile_height,
+                        int tile_bits, int32_t* offsets, int32_t* d_status, cudaStream_t s);
+
+// ---- raster.cu
+struct RasterArgs {
+    const float* means2d;
+    const float* conics;
+    const float* colors;
+    const float* opacities;
+    const float* backgrounds;
+    const int32_t* masks;
+    int C, N, width, height, tile_width, tile_height;
+    const int32_t* offsets;
+    const int32_t* flatten_ids;
+    int64_t n_isects;
+    float alpha_cutoff, transmittance_threshold;
+};
+
+void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_alphas,
+                       int32_t* last_ids, int32_t* pair_counts, cudaStream_t s);
+
+struct RasterGrads {
+    const float* render_alphas;
+    const int32_t* last_ids;
+    const float* grad_render_colors;
+    const float* grad_render_alphas;
+    float* grad_means2d;
+    float* grad_conics;
+    float* grad_colors;
+    float* grad_opacities;
+    float* grad_backgrounds;
+    float* grad_means2d_abs;
+};
+
+void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, cudaStream_t s);
+
+}  // namespace gs

@@ -1,0 +1,252 @@
+// Tile intersection (gsplat 1.0.0, intersections.c: gs_bounds,
+// gs_isect_tiles) and tile ranges (gs_offset_encode) on sm_103a.
+//
+//   k_isect_count  one thread per splat: rect, tiles_per_gauss, block sum
+//                  added to the total (size query).
+//   k_isect_emit   one thread per splat of a 256-splat chunk taken in ticket
+//                  order; a block scan of the counts plus a decoupled
+//                  look-back over earlier chunks gives each splat's first
+//                  output slot; then the block's whole run of keys is written
+//                  cooperatively (every thread finds the key's splat by a
+//                  binary search over the block's prefix sums), so stores are
+//                  coalesced whatever the per-splat counts are.  Optionally
+//                  also histograms the 8-bit digits of the key's upper word
+//                  for the radix passes that follow.
+//   k_tile_ranges  one thread per sorted key: where the tile id changes, the
+//                  tiles in between get this key's position.
+#include <cstdint>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+namespace {
+
+constexpr int kThreads = kIsectThreads;
+
+__global__ void __launch_bounds__(kThreads)
+    k_isect_count(const float* __restrict__ means2d, const float* __restrict__ radii,
+                  int elliptical, int64_t CN, float ts, int tile_width, int tile_height,
+                  int32_t* __restrict__ tiles_per_gauss, unsigned long long* __restrict__ total) {
+    __shared__ int64_t scratch[32];
+    int64_t local = 0;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < CN; i += stride) {
+        const float2 m = reinterpret_cast<const float2*>(means2d)[i];
+        float rx, ry;
+        if (elliptical) {
+            const float2 r = reinterpret_cast<const float2*>(radii)[i];
+            rx = r.x;
+            ry = r.y;
+        } else {
+            rx = ry = radii[i];
+        }
+        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+        const int cnt = (r.x1 - r.x0) * (r.y1 - r.y0);
+        if (tiles_per_gauss) tiles_per_gauss[i] = cnt;
+        local += cnt;
+    }
+    int64_t sum;
+    block_exclusive_scan<kThreads>(local, scratch, &sum);
+    if (threadIdx.x == 0 && sum) atomicAdd(total, (unsigned long long)sum);
+}
+
+struct EmitSmem {
+    int32_t incl[kThreads];   // inclusive prefix of counts in the chunk
+    int32_t x0[kThreads];
+    int32_t y0[kThreads];
+    int32_t w[kThreads];      // rect width in tiles
+    uint32_t upper[kThreads];  // camera << tile_bits
+    uint32_t dbits[kThreads];
+    int32_t sid[kThreads];
+    uint32_t hist[4][256];
+    int64_t scratch[32];
+    int64_t base;
+    uint32_t blk;
+};
+
+__device__ __forceinline__ void hist_inc(uint32_t* bins, uint32_t d, bool valid) {
+    unsigned act = __ballot_sync(0xffffffffu, valid);
+    if (!valid) return;
+    unsigned peers = __match_any_sync(act, d);
+    if ((peers & lanemask_lt()) == 0) atomicAdd(&bins[d], (uint32_t)__popc(peers));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_isect_emit(const float* __restrict__ means2d, const float* __restrict__ radii, int elliptical,
+                 const float* __restrict__ depths, const int32_t* __restrict__ order, int64_t CN,
+                 float ts, int tile_width, int tile_height, int N, int tile_bits,
+                 uint64_t* __restrict__ keys, int32_t* __restrict__ ids, int64_t capacity,
+                 int32_t* __restrict__ tiles_per_gauss, uint64_t* __restrict__ lookback,
+                 uint32_t* __restrict__ ticket, uint32_t* __restrict__ up_hist, int up_passes,
+                 ErrorSink err) {
+    __shared__ EmitSmem sm;
+    const int tid = threadIdx.x;
+    if (tid == 0) sm.blk = atomicAdd(ticket, 1u);
+    if (up_hist)
+        for (int i = tid; i < 4 * 256; i += kThreads) (&sm.hist[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t blk = sm.blk;
+    const int64_t k = blk * kThreads + tid;
+    int cnt = 0;
+    if (k < CN) {
+        const int64_t s = order ? (int64_t)order[k] : k;
+        const float2 m = reinterpret_cast<const float2*>(means2d)[s];
+        float rx, ry;
+        if (elliptical) {
+            const float2 r = reinterpret_cast<const float2*>(radii)[s];
+            rx = r.x;
+            ry = r.y;
+        } else {
+            rx = ry = radii[s];
+        }
+        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+        cnt = (r.x1 - r.x0) * (r.y1 - r.y0);
+        sm.x0[tid] = r.x0;
+        sm.y0[tid] = r.y0;
+        sm.w[tid] = r.x1 - r.x0;
+        sm.upper[tid] = (uint32_t)((uint64_t)(s / N) << tile_bits);
+        sm.dbits[tid] = __float_as_uint(depths[s]);
+        sm.sid[tid] = (int32_t)s;
+        if (tiles_per_gauss) tiles_per_gauss[s] = cnt;
+    }
+    int64_t chunk_total;
+    const int64_t excl = block_exclusive_scan<kThreads>(cnt, sm.scratch, &chunk_total);
+    sm.incl[tid] = (int32_t)(excl + cnt);
+
+    // decoupled look-back over earlier chunks (thread 0)
+    if (tid == 0) {
+        uint64_t* mine = lookback + blk;
+        int64_t prefix = 0;
+        if (blk == 0) {
+            st_relaxed_u64(mine, ((uint64_t)chunk_total << 2) | kFlagPrefix);
+        } else {
+            st_relaxed_u64(mine, ((uint64_t)chunk_total << 2) | kFlagAggregate);
+            for (int64_t p = blk - 1;; --p) {
+                const uint64_t v = wait_published(lookback + p, err);
+                prefix += (int64_t)(v >> 2);
+                if ((v & kFlagMask) == kFlagPrefix || p == 0) break;
+            }
+            st_relaxed_u64(mine, ((uint64_t)(prefix + chunk_total) << 2) | kFlagPrefix);
+        }
+        sm.base = prefix;
+        const int64_t nchunks = (CN + kThreads - 1) / kThreads;
+        if (prefix + chunk_total > capacity) err.raise(GS_ERR_COUNT_MISMATCH);
+        if (blk == nchunks - 1 && prefix + chunk_total != capacity)
+            err.raise(GS_ERR_COUNT_MISMATCH);
+    }
+    __syncthreads();
+    const int64_t base = sm.base;
+    const int total = (int)chunk_total;
+    const int rounds = (total + kThreads - 1) / kThreads;
+    for (int r = 0; r < rounds; ++r) {
+        const int q = r * kThreads + tid;
+        const bool valid = q < total;
+        uint32_t upper = 0;
+        if (valid) {
+            // owner: first o with incl[o] > q
+            int lo = 0, hi = kThreads - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (sm.incl[mid] > q) hi = mid;
+                else lo = mid + 1;
+            }
+            const int o = lo;
+            const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
+            const int w = sm.w[o];
+            const int dy = li / w;
+            const int ty = sm.y0[o] + dy;
+            const int tx = sm.x0[o] + (li - dy * w);
+            upper = sm.upper[o] | (uint32_t)(ty * tile_width + tx);
+            const int64_t pos = base + q;
+            if (pos < capacity) {
+                keys[pos] = ((uint64_t)upper << 32) | sm.dbits[o];
+                ids[pos] = sm.sid[o];
+            }
+        }
+        if (up_hist) {
+            for (int p = 0; p < up_passes; ++p) hist_inc(sm.hist[p], (upper >> (8 * p)) & 0xffu, valid);
+        }
+    }
+    if (up_hist) {
+        __syncthreads();
+        for (int i = tid; i < up_passes * 256; i += kThreads) {
+            const uint32_t v = (&sm.hist[0][0])[i];
+            if (v) atomicAdd(&up_hist[i], v);
+        }
+    }
+}
+
+__device__ __forceinline__ int64_t flat_tile(uint64_t key, int C, int64_t per_camera,
+                                             int tile_bits, bool* ok) {
+    const uint64_t upper = key >> 32;
+    const uint64_t cam = upper >> tile_bits;
+    const uint64_t tile = tile_bits == 0 ? 0 : (upper & ((1ull << tile_bits) - 1));
+    *ok = cam < (uint64_t)C && tile < (uint64_t)per_camera;
+    return (int64_t)cam * per_camera + (int64_t)tile;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_tile_ranges(const uint64_t* __restrict__ keys, int64_t n, int C, int tile_width,
+                  int tile_height, int tile_bits, int32_t* __restrict__ offsets,
+                  int32_t* d_status) {
+    const int64_t per_camera = (int64_t)tile_width * tile_height;
+    const int64_t ntiles = (int64_t)C * per_camera;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i <= n; i += stride) {
+        bool ok_cur = true, ok_prev = true;
+        int64_t cur = i < n ? flat_tile(keys[i], C, per_camera, tile_bits, &ok_cur) : ntiles;
+        int64_t prev = i > 0 ? flat_tile(keys[i - 1], C, per_camera, tile_bits, &ok_prev) : -1;
+        if (!ok_cur) {
+            report(d_status, GS_ERR_KEY_OUT_OF_GRID);
+            continue;
+        }
+        if (!ok_prev) continue;  // reported by that key's own thread
+        if (cur < prev) {
+            report(d_status, GS_ERR_UNSORTED);
+            continue;
+        }
+        for (int64_t t = prev + 1; t <= cur && t < ntiles; ++t) offsets[t] = (int32_t)i;
+    }
+}
+
+int grid_for(int64_t n, int per_thread) {
+    int64_t g = (n + (int64_t)kThreads * per_thread - 1) / ((int64_t)kThreads * per_thread);
+    if (g < 1) g = 1;
+    if (g > 152 * 16) g = 152 * 16;
+    return (int)g;
+}
+
+}  // namespace
+
+void launch_isect_count(const float* means2d, const float* radii, int elliptical, int64_t CN,
+                        int tile_size, int tile_width, int tile_height, int32_t* tiles_per_gauss,
+                        unsigned long long* total, cudaStream_t s) {
+    if (CN <= 0) return;
+    k_isect_count<<<grid_for(CN, 4), kThreads, 0, s>>>(means2d, radii, elliptical, CN,
+                                                       (float)tile_size, tile_width, tile_height,
+                                                       tiles_per_gauss, total);
+}
+
+void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
+                       const float* depths, const int32_t* order, int64_t CN, int tile_size,
+                       int tile_width, int tile_height, int N, int tile_bits, uint64_t* keys,
+                       int32_t* ids, int64_t capacity, int32_t* tiles_per_gauss,
+                       LookbackScratch lb, uint32_t* up_hist, int up_passes,
+                       int32_t* abort_flag, int32_t* d_status, cudaStream_t s) {
+    if (CN <= 0) return;
+    const int64_t chunks = (CN + kThreads - 1) / kThreads;
+    k_isect_emit<<<(unsigned)chunks, kThreads, 0, s>>>(
+        means2d, radii, elliptical, depths, order, CN, (float)tile_size, tile_width, tile_height,
+        N, tile_bits, keys, ids, capacity, tiles_per_gauss, lb.words, lb.ticket, up_hist,
+        up_passes, ErrorSink{abort_flag, d_status});
+}
+
+void launch_tile_ranges(const uint64_t* keys, int64_t n, int C, int tile_width, int tile_height,
+                        int tile_bits, int32_t* offsets, int32_t* d_status, cudaStream_t s) {
+    k_tile_ranges<<<grid_for(n + 1, 4), kThreads, 0, s>>>(keys, n, C, tile_width, tile_height,
+                                                          tile_bits, offsets, d_status);
+}
+
+}  // namespace gs

@@ -1,0 +1,253 @@
+// Stable LSD radix sort of (key, int32 value) pairs, one 8-bit digit per
+// pass, as a single-pass "onesweep" kernel per digit with decoupled
+// look-back (the CPU listing's counting pass + exclusive scan + stable
+// scatter, gsplat 1.0.0, intersections.c, gs_radix_sort_without_gvl, done
+// by every block for its own tile of keys at once).
+//
+// Per pass, each 256-thread block:
+//   1. takes a virtual block id from an atomic ticket (so a block only ever
+//      waits on blocks that are already running);
+//   2. loads its tile of keys warp-striped (coalesced) into registers;
+//   3. ranks each key among equal digits of its warp (match.any + popc),
+//      keeping input order (stability);
+//   4. publishes its 256 digit counts, then walks back over predecessors'
+//      words (bounded wait) to get its exclusive prefix per digit;
+//   5. reorders the tile by digit in shared memory and writes it out, so
+//      that consecutive threads write consecutive addresses of a bucket.
+// The global digit histogram that step 4 adds as bucket starts comes from
+// one histogram pass over all digits before the first sorting pass.
+#include <cstdint>
+
+#include "gs_device.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+namespace {
+
+constexpr int kThreads = kSortThreads;
+constexpr int kWarps = kThreads / kWarp;
+
+template <typename K>
+__device__ __forceinline__ uint32_t digit_of(K k, int shift, uint32_t mask) {
+    return (uint32_t)(k >> shift) & mask;
+}
+
+// Mask of the digit starting at bit `shift` when only bits below `end_bit`
+// take part (the last digit of a range may be narrower than 8 bits).
+__host__ __device__ __forceinline__ uint32_t digit_mask(int shift, int end_bit) {
+    const int bits = end_bit - shift >= 8 ? 8 : end_bit - shift;
+    return bits <= 0 ? 0u : ((1u << bits) - 1u);
+}
+
+// Adds one to bin d of a shared histogram, one atomic per distinct digit in
+// the warp (equal digits are common: constant high bits of keys).
+__device__ __forceinline__ void warp_aggregated_inc(uint32_t* bins, uint32_t d, bool valid) {
+    unsigned act = __ballot_sync(0xffffffffu, valid);
+    if (!valid) return;
+    unsigned peers = __match_any_sync(act, d);
+    if ((peers & lanemask_lt()) == 0) atomicAdd(&bins[d], (uint32_t)__popc(peers));
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kThreads) k_digit_hist(const K* __restrict__ keys, int64_t n,
+                                                         int shift0, int npasses, int end_bit,
+                                                         uint32_t* __restrict__ hist) {
+    __shared__ uint32_t sh[8][256];
+    for (int i = threadIdx.x; i < 8 * 256; i += kThreads) (&sh[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    // every lane of a warp runs the same trip count so the warp votes agree
+    const int64_t begin = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t rounds = (n + stride - 1) / stride;
+    for (int64_t r = 0; r < rounds; ++r) {
+        int64_t i = begin + r * stride;
+        bool valid = i < n;
+        K k = valid ? keys[i] : K(0);
+        for (int p = 0; p < npasses; ++p)
+            warp_aggregated_inc(sh[p],
+                                digit_of(k, shift0 + 8 * p, digit_mask(shift0 + 8 * p, end_bit)),
+                                valid);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < npasses * 256; i += kThreads) {
+        uint32_t v = (&sh[0][0])[i];
+        if (v) atomicAdd(&hist[i], v);
+    }
+}
+
+template <typename K, int ITEMS>
+struct OnesweepSmem {
+    K keys[kThreads * ITEMS];
+    int32_t vals[kThreads * ITEMS];
+    uint32_t warp_count[kWarps][256];  // per-warp digit counts, then warp prefixes
+    uint32_t local_start[256];         // first slot of each digit in the tile
+    int64_t out_base[256];             // output index of slot 0 of each digit
+    int64_t scratch_a[32];
+    int64_t scratch_b[32];
+    uint32_t blk;
+};
+
+template <typename K, int ITEMS, bool IOTA>
+__global__ void __launch_bounds__(kThreads)
+    k_onesweep(const K* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
+               K* __restrict__ keys_out, int32_t* __restrict__ vals_out, int64_t n, int shift,
+               uint32_t dmask, const uint32_t* __restrict__ hist, uint64_t* __restrict__ lookback,
+               uint32_t* __restrict__ ticket, ErrorSink err) {
+    __shared__ OnesweepSmem<K, ITEMS> sm;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) sm.blk = atomicAdd(ticket, 1u);
+    for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.warp_count[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t blk = sm.blk;
+    const int64_t tile_base = blk * (kThreads * ITEMS);
+    const int64_t warp_base = tile_base + (int64_t)warp * (kWarp * ITEMS);
+
+    K key[ITEMS];
+    int32_t val[ITEMS];
+    uint32_t rank[ITEMS];
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const int64_t idx = warp_base + i * kWarp + lane;
+        if (idx < n) {
+            key[i] = keys_in[idx];
+            val[i] = IOTA ? (int32_t)idx : vals_in[idx];
+        } else {
+            key[i] = K(0);
+            val[i] = 0;
+        }
+    }
+
+    // 3. rank within the warp, in element order (i, then lane)
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const bool valid = warp_base + i * kWarp + lane < n;
+        const uint32_t d = valid ? digit_of(key[i], shift, dmask) : 0x100u + lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        uint32_t before = valid ? sm.warp_count[warp][d] : 0u;
+        __syncwarp();
+        if (valid && (peers & lt) == 0) sm.warp_count[warp][d] = before + __popc(peers);
+        __syncwarp();
+        rank[i] = before + __popc(peers & lt);
+    }
+    __syncthreads();
+
+    // 4. per-digit totals, warp prefixes, publication and look-back
+    const int d = tid;  // one digit per thread
+    uint32_t total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        uint32_t c = sm.warp_count[w][d];
+        sm.warp_count[w][d] = total;
+        total += c;
+    }
+    uint64_t* mine = lookback + blk * 256 + d;
+    st_relaxed_u64(mine, ((uint64_t)total << 2) | (blk == 0 ? kFlagPrefix : kFlagAggregate));
+
+    int64_t all;
+    const int64_t bucket_start = block_exclusive_scan<kThreads>(hist[d], sm.scratch_a, &all);
+
+    int64_t excl = 0;
+    if (blk > 0) {
+        int64_t p = blk - 1;
+        for (;;) {
+            const uint64_t v = wait_published(lookback + p * 256 + d, err);
+            excl += (int64_t)(v >> 2);
+            if ((v & kFlagMask) == kFlagPrefix || p == 0) break;
+            --p;
+        }
+        st_relaxed_u64(mine, ((uint64_t)(excl + total) << 2) | kFlagPrefix);
+    }
+    int64_t tile_count;
+    const int64_t lstart = block_exclusive_scan<kThreads>(total, sm.scratch_b, &tile_count);
+    sm.local_start[d] = (uint32_t)lstart;
+    sm.out_base[d] = bucket_start + excl - lstart;
+    __syncthreads();
+
+    // 5. reorder by digit in shared memory, then write out bucket runs
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        if (warp_base + i * kWarp + lane < n) {
+            const uint32_t dd = digit_of(key[i], shift, dmask);
+            const uint32_t pos = sm.local_start[dd] + sm.warp_count[warp][dd] + rank[i];
+            sm.keys[pos] = key[i];
+            sm.vals[pos] = val[i];
+        }
+    }
+    __syncthreads();
+    const int cnt = (int)tile_count;
+    for (int j = tid; j < cnt; j += kThreads) {
+        const K k = sm.keys[j];
+        const int64_t o = sm.out_base[digit_of(k, shift, dmask)] + j;
+        // in range by construction when the histogram matches the keys; the
+        // test only matters after a timed-out wait or an inconsistent input
+        if ((uint64_t)o < (uint64_t)n) {
+            keys_out[o] = k;
+            vals_out[o] = sm.vals[j];
+        } else {
+            err.raise(GS_ERR_COUNT_MISMATCH);
+        }
+    }
+}
+
+int hist_grid(int64_t n) {
+    int64_t g = (n + kThreads * 16 - 1) / (kThreads * 16);
+    if (g < 1) g = 1;
+    if (g > 152 * 4) g = 152 * 4;
+    return (int)g;
+}
+
+}  // namespace
+
+void launch_digit_hist_u64(const uint64_t* keys, int64_t n, int shift0, int end_bit,
+                           uint32_t* hist, cudaStream_t s) {
+    const int npasses = (end_bit - shift0 + 7) / 8;
+    if (n <= 0 || npasses <= 0) return;
+    k_digit_hist<uint64_t><<<hist_grid(n), kThreads, 0, s>>>(keys, n, shift0, npasses, end_bit,
+                                                            hist);
+}
+
+void launch_digit_hist_u32(const uint32_t* keys, int64_t n, int shift0, int end_bit,
+                           uint32_t* hist, cudaStream_t s) {
+    const int npasses = (end_bit - shift0 + 7) / 8;
+    if (n <= 0 || npasses <= 0) return;
+    k_digit_hist<uint32_t><<<hist_grid(n), kThreads, 0, s>>>(keys, n, shift0, npasses, end_bit,
+                                                            hist);
+}
+
+void launch_onesweep_u64(const uint64_t* keys_in, const int32_t* vals_in, uint64_t* keys_out,
+                         int32_t* vals_out, int64_t n, int shift, int end_bit,
+                         const uint32_t* hist,
+                         LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                         cudaStream_t s) {
+    if (n <= 0) return;
+    const int64_t blocks = sort_blocks(n, kTile64);
+    ErrorSink err{abort_flag, d_status};
+    const uint32_t dm = digit_mask(shift, end_bit);
+    if (vals_in)
+        k_onesweep<uint64_t, kItems64, false><<<(unsigned)blocks, kThreads, 0, s>>>(
+            keys_in, vals_in, keys_out, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err);
+    else
+        k_onesweep<uint64_t, kItems64, true><<<(unsigned)blocks, kThreads, 0, s>>>(
+            keys_in, vals_in, keys_out, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err);
+}
+
+void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32_t* keys_out,
+                         int32_t* vals_out, int64_t n, int shift, int end_bit,
+                         const uint32_t* hist,
+                         LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                         cudaStream_t s) {
+    if (n <= 0) return;
+    const int64_t blocks = sort_blocks(n, kTile32);
+    ErrorSink err{abort_flag, d_status};
+    const uint32_t dm = digit_mask(shift, end_bit);
+    if (vals_in)
+        k_onesweep<uint32_t, kItems32, false><<<(unsigned)blocks, kThreads, 0, s>>>(
+            keys_in, vals_in, keys_out, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err);
+    else
+        k_onesweep<uint32_t, kItems32, true><<<(unsigned)blocks, kThreads, 0, s>>>(
+            keys_in, vals_in, keys_out, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err);
+}
+
+}  // namespace gs
