@@ -33,7 +33,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Msplat-isect/s + Mpixel/s fwd(+bwd) at 1 GB300; % HBM / FP32-SFU roofline"
-WORKLOAD = "w3: 4 cameras x 1,000,000 splats, 1920x1080, tile 16, elliptical radii"
+WORKLOADS = {
+    2: "w2: 1 camera x 100,000 splats, 1024x1024, tile 16, elliptical radii",
+    3: "w3: 4 cameras x 1,000,000 splats, 1920x1080, tile 16, elliptical radii",
+    4: "w4: 1 camera x 6,000,000 splats, 3840x2160, tile 16, elliptical radii",
+}
+WORKLOAD = WORKLOADS[3]
 SM_COUNT = 152
 FP32_LANES = 128
 SM_MAX_MHZ = 2070.0
@@ -352,7 +357,9 @@ def run_ours(args, rank, world, scene):
     names = ["isect_query", "isect_emit_sort", "tile_ranges", "raster_fwd", "raster_bwd"]
     CN, I = s.C * s.N, path.I
     tiles = s.C * s.tile_width * s.tile_height
-    up_passes = 2
+    from tile_gaussian_splat_gb300 import binding as gsb
+    key_bits = gsb.gs_tile_bits(s.tile_width, s.tile_height) + max(0, (s.C - 1).bit_length())
+    up_passes = (key_bits + 7) // 8
     # algorithmic bytes (stated in the design doc): what each stage must read and write
     bytes_ = {
         "isect_query": CN * (8 + 8 + 4),
@@ -410,7 +417,7 @@ def run_ours(args, rank, world, scene):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded workload 3 generator)",
-        "config": {"workload": WORKLOAD, "C": s.C, "N": s.N, "width": s.width,
+        "config": {"workload": WORKLOADS[args.workload], "C": s.C, "N": s.N, "width": s.width,
                    "height": s.height, "tile_size": 16, "n_isects": I,
                    "max_tile_list": max_list, "pixels_per_step": pixels,
                    "l2": "flushed between steps (256 MB write outside the step events)",
@@ -520,6 +527,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=3, choices=[2, 3, 4],
+                    help="3 is the measured workload; 2 and 4 serve profiling")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -531,9 +540,9 @@ def main():
         line = run_reference(args, rank, world)
     else:
         from tile_gaussian_splat_gb300 import scenes
-        sc = scenes.workload3()
+        sc = scenes.workload(args.workload)
         cpu = None
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == 3:
             # before any CUDA work: the oracle runs in this process, single thread
             est, desc = cpu_sample(sc)
             cpu = {"value": round(sc.C * sc.width * sc.height / est / 1e6, 6),

@@ -45,14 +45,15 @@ def lib():
         L.orc_tile_offsets.argtypes = [P, I64, I32, I32, I32, P]
         L.orc_tile_offsets.restype = I32
         L.orc_rasterize_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
-                                        P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32]
+                                        P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32, F32,
+                                        P]
         L.orc_rasterize_fwd.restype = I32
         L.orc_rasterize_fwd_f64.argtypes = [P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                             P, P, I64, F64, F64, P, P, P]
         L.orc_rasterize_fwd_f64.restype = I32
         L.orc_rasterize_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                         P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
-                                        F32, P]
+                                        F32, P, P]
         L.orc_rasterize_bwd.restype = I32
         _lib = L
     return _lib
@@ -132,7 +133,7 @@ def tile_offsets(keys, C, tile_width, tile_height):
 
 def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, transmittance_threshold,
-                  pixels=None, tie_rel=0.0, out=None):
+                  pixels=None, tie_rel=0.0, tie_rel_T=None, out=None):
     """Forward compositing.  Returns dict(render_colors (C,H,W,ch),
     render_alphas (C,H,W,1), last_ids (C,H,W), stats [evaluated, composited,
     near-tie pixels], near_tie (C,H,W) uint8)."""
@@ -152,6 +153,7 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                    render_alphas=np.zeros((C, height, width, 1), np.float32),
                    last_ids=np.full((C, height, width), -2, np.int32),
                    near_tie=np.zeros((C, height, width), np.uint8))
+    out["tie_splats"] = np.zeros((C, N), np.uint8)
     stats = np.zeros(3, np.int64)
     px = None if pixels is None else _c(pixels, np.int64)
     rc = lib().orc_rasterize_fwd(
@@ -160,7 +162,8 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         _ptr(flatten_ids), flatten_ids.size, float(alpha_cutoff), float(transmittance_threshold),
         _ptr(px), 0 if px is None else px.size, _ptr(out["render_colors"]),
         _ptr(out["render_alphas"]), _ptr(out["last_ids"]), _ptr(stats), _ptr(out["near_tie"]),
-        float(tie_rel))
+        float(tie_rel), float(tie_rel if tie_rel_T is None else tie_rel_T),
+        _ptr(out["tie_splats"]))
     if rc != 0:
         raise ValueError("oracle forward: bad arguments")
     out["stats"] = stats
@@ -223,7 +226,8 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                grad_opacities=np.empty((C, N), np.float32),
                grad_backgrounds=np.empty((C, ch), np.float32) if want_grad_backgrounds else None,
                grad_means2d_abs=np.empty((C, N, 2), np.float32) if absgrad else None,
-               near_tie=np.zeros((C, height, width), np.uint8))
+               near_tie=np.zeros((C, height, width), np.uint8),
+               tie_splats=np.zeros((C, N), np.uint8))
     px = None if pixels is None else _c(pixels, np.int64)
     mags = np.zeros((6 + ch) * C * N, np.float64) if magnitudes else None
     rc = lib().orc_rasterize_bwd(
@@ -233,7 +237,8 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         _ptr(last_ids), _ptr(grad_render_colors), _ptr(grad_render_alphas), _ptr(px),
         0 if px is None else px.size, _ptr(out["grad_means2d"]), _ptr(out["grad_conics"]),
         _ptr(out["grad_colors"]), _ptr(out["grad_opacities"]), _ptr(out["grad_backgrounds"]),
-        _ptr(out["grad_means2d_abs"]), _ptr(out["near_tie"]), float(tie_rel), _ptr(mags))
+        _ptr(out["grad_means2d_abs"]), _ptr(out["near_tie"]), float(tie_rel), _ptr(mags),
+        _ptr(out["tie_splats"]))
     if rc != 0:
         raise ValueError("oracle backward: bad arguments")
     if magnitudes:
@@ -245,7 +250,7 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
     return out
 
 
-def render(scene, sort=True, pixels=None, tie_rel=0.0):
+def render(scene, sort=True, pixels=None, tie_rel=0.0, tie_rel_T=None):
     """Whole forward path on a scenes.Scene-like object: isect, sort,
     offsets, forward.  Returns (isect dict, forward dict)."""
     tpg, keys, ids = isect_tiles(scene.means2d, scene.radii, scene.depths, scene.tile_size,
@@ -254,5 +259,5 @@ def render(scene, sort=True, pixels=None, tie_rel=0.0):
     fwd = rasterize_fwd(scene.means2d, scene.conics, scene.colors, scene.opacities,
                         scene.backgrounds, None, scene.width, scene.height, scene.tile_size,
                         offsets, ids, scene.alpha_cutoff, scene.transmittance_threshold,
-                        pixels=pixels, tie_rel=tie_rel)
+                        pixels=pixels, tie_rel=tie_rel, tie_rel_T=tie_rel_T)
     return dict(tiles_per_gauss=tpg, keys=keys, flatten_ids=ids, offsets=offsets), fwd

@@ -260,9 +260,12 @@ int orc_tile_offsets(const uint64_t* keys, int64_t n, int C, int tile_width, int
 //   stats[1] += pairs composited
 //   stats[2] += pixels flagged near-tie (below)
 //   near_tie[pixel] = 1 when a decision was taken within a relative margin:
-//     |alpha - cutoff| <= tie_rel * cutoff, |T - threshold| <= tie_rel *
-//     threshold after a composite, or 0 < |s| <= tie_rel.  At such pixels an
-//     exp or rounding-order difference of a few ulp can flip the decision.
+//     |alpha - cutoff| <= tie_rel * cutoff, 0 < |s| <= tie_rel, or
+//     |T - threshold| <= tie_rel_T * threshold after a composite.  At such
+//     pixels an exp or rounding-order difference of a few ulp can flip the
+//     decision (T carries the accumulated error of every 1 - alpha, which is
+//     large relative to itself for alpha near 0.99, hence its own margin).
+//   tie_splats[g] = 1 for every splat g that took part in such a decision.
 struct FwdArgs {
     const float* means2d;
     const float* conics;
@@ -280,7 +283,7 @@ struct FwdArgs {
 
 static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
                       float* out_alpha, int32_t* out_last, int64_t* stats, uint8_t* near_tie,
-                      float tie_rel) {
+                      float tie_rel, float tie_rel_T, uint8_t* tie_splats) {
     int64_t tiles = (int64_t)a.C * a.tile_height * a.tile_width;
     int64_t t = (c * a.tile_height + y / a.tile_size) * a.tile_width + x / a.tile_size;
     int64_t start = a.offsets[t];
@@ -301,11 +304,17 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             float dy = a.means2d[2 * g + 1] - py;
             const float* q = a.conics + 3 * (int64_t)g;
             float s = 0.5f * (q[0] * dx * dx + q[2] * dy * dy) + q[1] * dx * dy;
-            if (s != 0.0f && std::fabs(s) <= tie_rel) tie = true;
-            if (!(s >= 0.0f)) continue;
+            bool pair_tie = s != 0.0f && std::fabs(s) <= tie_rel;
+            if (!(s >= 0.0f)) {
+                if (pair_tie && tie_splats) tie_splats[g] = 1;
+                tie |= pair_tie;
+                continue;
+            }
             float raw = a.opacities[g] * std::exp(-s);
             float alpha = raw > kAlphaClamp ? kAlphaClamp : raw;
-            if (std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff) tie = true;
+            pair_tie |= std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff;
+            if (pair_tie && tie_splats) tie_splats[g] = 1;
+            tie |= pair_tie;
             if (alpha < a.alpha_cutoff) continue;
             float w = T * alpha;
             const float* col = a.colors + (int64_t)a.channels * g;
@@ -314,8 +323,10 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             last = (int32_t)j;
             ++composited;
             if (std::fabs(T - a.transmittance_threshold) <=
-                tie_rel * a.transmittance_threshold)
+                tie_rel_T * a.transmittance_threshold) {
                 tie = true;
+                if (tie_splats) tie_splats[g] = 1;
+            }
             if (T < a.transmittance_threshold) break;
         }
     }
@@ -345,7 +356,8 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
                       const int32_t* flatten_ids, int64_t n_isects, float alpha_cutoff,
                       float transmittance_threshold, const int64_t* pixels, int64_t n_pixels,
                       float* render_colors, float* render_alphas, int32_t* last_ids,
-                      int64_t* stats, uint8_t* near_tie, float tie_rel) {
+                      int64_t* stats, uint8_t* near_tie, float tie_rel, float tie_rel_T,
+                      uint8_t* tie_splats) {
     if (channels < 1 || channels > 64) return 1;
     FwdArgs a = {means2d,   conics,     colors,      opacities, backgrounds,
                  masks,     C,          N,           channels,  width,
@@ -356,14 +368,14 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
             for (int y = 0; y < height; ++y)
                 for (int x = 0; x < width; ++x)
                     fwd_pixel(a, c, x, y, render_colors, render_alphas, last_ids, stats,
-                              near_tie, tie_rel);
+                              near_tie, tie_rel, tie_rel_T, tie_splats);
     } else {
         for (int64_t k = 0; k < n_pixels; ++k) {
             int64_t p = pixels[k];
             int64_t c = p / ((int64_t)width * height);
             int64_t r = p % ((int64_t)width * height);
             fwd_pixel(a, c, (int)(r % width), (int)(r / width), render_colors, render_alphas,
-                      last_ids, stats, near_tie, tie_rel);
+                      last_ids, stats, near_tie, tie_rel, tie_rel_T, tie_splats);
         }
     }
     return 0;
@@ -447,7 +459,8 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
 // Per-pair terms are float as listed; they are summed in double and rounded
 // to float once.  pixels/n_pixels restricts the walk to listed pixels.
 // near_tie (optional, per pixel) marks pixels where alpha was within tie_rel
-// of the cutoff or raw alpha within tie_rel of the clamp.
+// of the cutoff or raw alpha within tie_rel of the clamp; tie_splats
+// (optional, per splat) marks the splats of those pairs.
 // magnitudes (optional, double) receives, per gradient element, the sum of
 // the absolute values of its per-pair terms, laid out as grad_means2d (2CN),
 // grad_conics (3CN), grad_colors (channels*CN), grad_opacities (CN): the
@@ -462,7 +475,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                       const int64_t* pixels, int64_t n_pixels, float* grad_means2d,
                       float* grad_conics, float* grad_colors, float* grad_opacities,
                       float* grad_backgrounds, float* grad_means2d_abs, uint8_t* near_tie,
-                      float tie_rel, double* magnitudes) {
+                      float tie_rel, double* magnitudes, uint8_t* tie_splats) {
     if (channels < 1 || channels > 64) return 1;
     int64_t CN = C * N;
     std::vector<double> gm(2 * CN, 0.0), gq(3 * CN, 0.0), gc((size_t)channels * CN, 0.0),
@@ -509,8 +522,10 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             bool valid = ra > 0.0f && s >= 0.0f && alpha >= alpha_cutoff && last >= j &&
                          Tc < 1.0f && alpha < 1.0f;
             if (last >= j && s >= 0.0f) {
-                if (std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff) tie = true;
-                if (std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp) tie = true;
+                bool pair_tie = std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff ||
+                                std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp;
+                if (pair_tie && tie_splats) tie_splats[g] = 1;
+                tie |= pair_tie;
             }
             if (!valid) continue;
             float Tb = Tc / (1.0f - alpha);

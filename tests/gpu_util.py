@@ -10,11 +10,14 @@ from tile_gaussian_splat_gb300 import binding as gs
 
 DEV = "cuda:0"
 
-# near-tie margin: pixels where the oracle took a skip/stop decision within
+# near-tie margins: pixels where the oracle took a skip/stop decision within
 # this relative distance of its threshold are left out of the exact
-# comparisons (exp implementations and rounding order differ by a few ulp,
-# transmittance accumulates them over hundreds of steps)
-TIE_REL = 1e-4
+# comparisons.  alpha vs the cutoff: libm expf and __expf differ by a few ulp
+# (< 1e-6 relative) and s is computed in the same rounding order on both
+# sides.  T vs the threshold: T carries every 1 - alpha, whose relative error
+# is alpha / (1 - alpha) times alpha's (1e-4 for alpha = 0.99).
+TIE_ALPHA = 1e-5
+TIE_T = 1e-3
 RGBA_ATOL = 1e-5
 
 

@@ -1,21 +1,29 @@
-// Forward compositing and its reverse-walk backward, one 256-thread block per
-// 16x16 tile, one pixel per thread.
+// Forward compositing and its reverse-walk backward, one block per 16x16
+// tile, PPT pixels per thread in a vertical strip (thread t owns column
+// t % 16 and rows (t / 16) * PPT .. + PPT - 1 of the tile).
+//
+// Why strips: a splat record read from shared memory serves PPT pixels, and
+// the terms of the quadratic form that depend only on dx (a dx dx, b dx) are
+// computed once per thread and entry -- in the same rounding order as the
+// per-pixel formula, so results do not change.  In the backward a warp covers
+// 32 * PPT pixels, so the shuffle reduction of a splat's terms (and its
+// atomics) is paid once per 32 * PPT pixels.
 //
 // Forward: the tile's sorted list is streamed through shared memory in
-// batches of 256 splat records (gathered through flatten_ids, one record per
-// thread); every thread walks the batch for its pixel.  A block stops as soon
-// as every pixel has T < threshold (__syncthreads_count vote).
+// batches (records gathered through flatten_ids); a warp skips a batch when
+// all its pixels have stopped, and the block ends when every pixel has
+// (__syncthreads_count vote).
 //
 // Backward (gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel): the
-// list is walked from the last position any pixel of the tile used down to
-// the tile's start, in batches staged the same way.  Each warp sums the
-// per-splat terms of its 32 pixels with shuffles before one atomic per
-// gradient field (the shuffle-then-atomic pattern of the mxnet depthwise
-// backward-filter kernel), and skips the sum when none of its pixels had a
-// valid pair.
+// list is walked from the largest last_id of the tile down to the tile's
+// start; a warp skips entries beyond the largest last_id of its own pixels.
+// Each thread sums its pixels' terms in registers, the warp sums them with
+// shuffles, and lane 0 adds them to the gradients with one atomic per field
+// (the shuffle-then-atomic pattern of the mxnet depthwise backward-filter
+// kernel).  Warps with no valid pair for an entry skip both.
 //
-// alpha is computed by the same inline function in both kernels, so the
-// backward makes exactly the forward's skip/composite decisions.
+// alpha is computed by the same inline code in both kernels, so the backward
+// makes exactly the forward's skip/composite decisions.
 #include <cstdint>
 
 #include "gs_device.cuh"
@@ -26,24 +34,37 @@ namespace gs {
 namespace {
 
 constexpr int kTile = 16;
-constexpr int kThreads = kTile * kTile;
+constexpr int kPPT = 4;                          // pixels per thread
+constexpr int kThreads = kTile * kTile / kPPT;   // 64
+constexpr int kBatch = 2 * kThreads;             // records staged per batch
 constexpr float kAlphaClamp = 0.99f;
 
-struct PairEval {
-    float dx, dy, s, resp, raw, alpha;
+// Per-entry terms shared by the PPT pixels of one column.
+struct ColumnTerms {
+    float dx, qa, bdx;  // dx = mx - px, qa = (a dx) dx, bdx = b dx
 };
 
-// s = 0.5 (a dx^2 + c dy^2) + b dx dy, rounded as written (no FMA
+__device__ __forceinline__ ColumnTerms column_terms(float mx, float a, float b, float px) {
+    ColumnTerms t;
+    t.dx = __fsub_rn(mx, px);
+    t.qa = __fmul_rn(__fmul_rn(a, t.dx), t.dx);
+    t.bdx = __fmul_rn(b, t.dx);
+    return t;
+}
+
+struct PairEval {
+    float dy, s, resp, raw, alpha;
+};
+
+// s = 0.5 (a dx^2 + c dy^2) + b dx dy rounded exactly as written (no FMA
 // contraction), alpha = min(0.99, o exp(-s)).
-__device__ __forceinline__ PairEval eval_pair(float mx, float my, float a, float b, float c,
-                                              float op, float px, float py) {
+__device__ __forceinline__ PairEval eval_pair(const ColumnTerms& ct, float my, float c, float op,
+                                              float py) {
     PairEval e;
-    e.dx = __fsub_rn(mx, px);
     e.dy = __fsub_rn(my, py);
-    const float qa = __fmul_rn(__fmul_rn(a, e.dx), e.dx);
     const float qc = __fmul_rn(__fmul_rn(c, e.dy), e.dy);
-    const float qb = __fmul_rn(__fmul_rn(b, e.dx), e.dy);
-    e.s = __fadd_rn(__fmul_rn(0.5f, __fadd_rn(qa, qc)), qb);
+    const float qb = __fmul_rn(ct.bdx, e.dy);
+    e.s = __fadd_rn(__fmul_rn(0.5f, __fadd_rn(ct.qa, qc)), qb);
     e.resp = __expf(-e.s);
     e.raw = __fmul_rn(op, e.resp);
     e.alpha = e.raw > kAlphaClamp ? kAlphaClamp : e.raw;
@@ -97,67 +118,91 @@ __device__ __forceinline__ int32_t stage_record(const RasterArgs& a, int64_t j, 
     return (int32_t)g;
 }
 
+struct PixelSlot {
+    int x, y0;  // column and first row of the thread's strip
+};
+
+__device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
+    PixelSlot p;
+    p.x = tr.tx * kTile + (threadIdx.x & (kTile - 1));
+    p.y0 = tr.ty * kTile + (threadIdx.x / kTile) * kPPT;
+    return p;
+}
+
 template <bool COUNT>
 __global__ void __launch_bounds__(kThreads)
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
                  int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts) {
-    __shared__ float4 s_mo[kThreads];  // mx, my, opacity, -
-    __shared__ float4 s_q[kThreads];   // a, b, c, -
-    __shared__ float4 s_col[kThreads]; // r, g, b, -
+    __shared__ float4 s_mo[kBatch];   // mx, my, opacity, -
+    __shared__ float4 s_q[kBatch];    // a, b, c, -
+    __shared__ float4 s_col[kBatch];  // r, g, b, -
     const TileRange tr = tile_range(a);
     const int tid = threadIdx.x;
-    const int x = tr.tx * kTile + (tid & (kTile - 1));
-    const int y = tr.ty * kTile + (tid / kTile);
-    const bool inside = x < a.width && y < a.height;
-    const float px = (float)x + 0.5f, py = (float)y + 0.5f;
-    float T = 1.0f, cr = 0.0f, cg = 0.0f, cb = 0.0f;
-    int32_t last = -1;
-    int32_t n_eval = 0, n_comp = 0;
-    bool done = !inside;
-    for (int64_t b0 = tr.start; b0 < tr.end; b0 += kThreads) {
-        if (__syncthreads_count(done) == kThreads) break;
-        const int64_t j = b0 + tid;
-        if (j < tr.end) stage_record(a, j, s_mo, s_q, s_col, tid);
+    const PixelSlot ps = pixel_slot(tr);
+    const float px = (float)ps.x + 0.5f;
+    float T[kPPT], cr[kPPT], cg[kPPT], cb[kPPT], py[kPPT];
+    int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT];
+    bool done[kPPT];
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+        T[k] = 1.0f;
+        cr[k] = cg[k] = cb[k] = 0.0f;
+        last[k] = -1;
+        n_eval[k] = n_comp[k] = 0;
+        done[k] = !(ps.x < a.width && ps.y0 + k < a.height);
+        py[k] = (float)(ps.y0 + k) + 0.5f;
+    }
+    for (int64_t b0 = tr.start; b0 < tr.end; b0 += kBatch) {
+        bool all_done = true;
+#pragma unroll
+        for (int k = 0; k < kPPT; ++k) all_done &= done[k];
+        if (__syncthreads_count(all_done) == kThreads) break;
+        const int nb = (int)min((int64_t)kBatch, tr.end - b0);
+        for (int i = tid; i < nb; i += kThreads) stage_record(a, b0 + i, s_mo, s_q, s_col, i);
         __syncthreads();
-        const int nb = (int)min((int64_t)kThreads, tr.end - b0);
-        if (!done) {
-            for (int k = 0; k < nb; ++k) {
-                const float4 mo = s_mo[k];
-                const float4 q = s_q[k];
-                const PairEval e = eval_pair(mo.x, mo.y, q.x, q.y, q.z, mo.z, px, py);
-                if (COUNT) ++n_eval;
+        if (__all_sync(0xffffffffu, all_done)) continue;
+        for (int i = 0; i < nb; ++i) {
+            const float4 mo = s_mo[i];
+            const float4 q = s_q[i];
+            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+#pragma unroll
+            for (int k = 0; k < kPPT; ++k) {
+                if (done[k]) continue;
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                if (COUNT) ++n_eval[k];
                 if (!(e.s >= 0.0f) || e.alpha < a.alpha_cutoff) continue;
-                if (COUNT) ++n_comp;
-                const float4 col = s_col[k];
-                const float w = T * e.alpha;
-                cr += w * col.x;
-                cg += w * col.y;
-                cb += w * col.z;
-                T = T * (1.0f - e.alpha);
-                last = (int32_t)(b0 + k);
-                if (T < a.transmittance_threshold) {
-                    done = true;
-                    break;
-                }
+                if (COUNT) ++n_comp[k];
+                const float4 col = s_col[i];
+                const float w = T[k] * e.alpha;
+                cr[k] += w * col.x;
+                cg[k] += w * col.y;
+                cb[k] += w * col.z;
+                T[k] = T[k] * (1.0f - e.alpha);
+                last[k] = (int32_t)(b0 + i);
+                if (T[k] < a.transmittance_threshold) done[k] = true;
             }
         }
     }
-    if (inside) {
-        const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + x;
-        float br = 0.0f, bgc = 0.0f, bb = 0.0f;
-        if (a.backgrounds) {
-            br = a.backgrounds[3 * tr.c];
-            bgc = a.backgrounds[3 * tr.c + 1];
-            bb = a.backgrounds[3 * tr.c + 2];
-        }
-        out_rgb[3 * p] = cr + T * br;
-        out_rgb[3 * p + 1] = cg + T * bgc;
-        out_rgb[3 * p + 2] = cb + T * bb;
-        out_alpha[p] = 1.0f - T;
-        out_last[p] = last;
-        if (COUNT) {
-            out_counts[2 * p] = n_eval;
-            out_counts[2 * p + 1] = n_comp;
+    float br = 0.0f, bgc = 0.0f, bb = 0.0f;
+    if (a.backgrounds) {
+        br = a.backgrounds[3 * tr.c];
+        bgc = a.backgrounds[3 * tr.c + 1];
+        bb = a.backgrounds[3 * tr.c + 2];
+    }
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+        const int y = ps.y0 + k;
+        if (ps.x < a.width && y < a.height) {
+            const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
+            out_rgb[3 * p] = cr[k] + T[k] * br;
+            out_rgb[3 * p + 1] = cg[k] + T[k] * bgc;
+            out_rgb[3 * p + 2] = cb[k] + T[k] * bb;
+            out_alpha[p] = 1.0f - T[k];
+            out_last[p] = last[k];
+            if (COUNT) {
+                out_counts[2 * p] = n_eval[k];
+                out_counts[2 * p + 1] = n_comp[k];
+            }
         }
     }
 }
@@ -168,47 +213,64 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    k_raster_bwd(RasterArgs a, RasterGrads gr) {
-    __shared__ float4 s_mo[kThreads];
-    __shared__ float4 s_q[kThreads];
-    __shared__ float4 s_col[kThreads];
-    __shared__ int32_t s_gid[kThreads];
+template <bool ABS>
+__global__ void __launch_bounds__(kThreads) k_raster_bwd(RasterArgs a, RasterGrads gr) {
+    __shared__ float4 s_mo[kBatch];
+    __shared__ float4 s_q[kBatch];
+    __shared__ float4 s_col[kBatch];
+    __shared__ int32_t s_gid[kBatch];
     __shared__ float s_bg[kThreads / kWarp][3];
     __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int x = tr.tx * kTile + (tid & (kTile - 1));
-    const int y = tr.ty * kTile + (tid / kTile);
-    const bool inside = x < a.width && y < a.height;
-    const float px = (float)x + 0.5f, py = (float)y + 0.5f;
-    const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + x;
-    float ra = 0.0f, ga = 0.0f, g0 = 0.0f, g1 = 0.0f, g2 = 0.0f;
-    int32_t last = -1;
-    if (inside) {
-        ra = gr.render_alphas[p];
-        last = gr.last_ids[p];
-        g0 = gr.grad_render_colors[3 * p];
-        g1 = gr.grad_render_colors[3 * p + 1];
-        g2 = gr.grad_render_colors[3 * p + 2];
-        ga = gr.grad_render_alphas[p];
-    }
-    float Tc = 1.0f - ra;
-    float Ta = 1.0f;
-    float rem0 = 0.0f, rem1 = 0.0f, rem2 = 0.0f;
+    const PixelSlot ps = pixel_slot(tr);
+    const float px = (float)ps.x + 0.5f;
+
+    float ra[kPPT], g0[kPPT], g1[kPPT], g2[kPPT], ga[kPPT], py[kPPT];
+    float Tc[kPPT], Ta[kPPT], r0[kPPT], r1[kPPT], r2[kPPT];
+    int32_t last[kPPT];
+    float bg0 = 0.0f, bg1 = 0.0f, bg2 = 0.0f;
     if (a.backgrounds) {
-        rem0 = a.backgrounds[3 * tr.c];
-        rem1 = a.backgrounds[3 * tr.c + 1];
-        rem2 = a.backgrounds[3 * tr.c + 2];
+        bg0 = a.backgrounds[3 * tr.c];
+        bg1 = a.backgrounds[3 * tr.c + 1];
+        bg2 = a.backgrounds[3 * tr.c + 2];
+    }
+    int my_max = -1;
+    float sb0 = 0.0f, sb1 = 0.0f, sb2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+        const int y = ps.y0 + k;
+        py[k] = (float)y + 0.5f;
+        ra[k] = g0[k] = g1[k] = g2[k] = ga[k] = 0.0f;
+        last[k] = -1;
+        if (ps.x < a.width && y < a.height) {
+            const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
+            ra[k] = gr.render_alphas[p];
+            last[k] = gr.last_ids[p];
+            g0[k] = gr.grad_render_colors[3 * p];
+            g1[k] = gr.grad_render_colors[3 * p + 1];
+            g2[k] = gr.grad_render_colors[3 * p + 2];
+            ga[k] = gr.grad_render_alphas[p];
+        }
+        Tc[k] = 1.0f - ra[k];
+        Ta[k] = 1.0f;
+        r0[k] = bg0;
+        r1[k] = bg1;
+        r2[k] = bg2;
+        sb0 += g0[k] * Tc[k];
+        sb1 += g1[k] * Tc[k];
+        sb2 += g2[k] * Tc[k];
+        if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
     if (tid == 0) s_jmax = -1;
     if (gr.grad_backgrounds) {
-        const float t = inside ? Tc : 0.0f;
-        const float b0 = warp_sum(g0 * t), b1 = warp_sum(g1 * t), b2 = warp_sum(g2 * t);
+        sb0 = warp_sum(sb0);
+        sb1 = warp_sum(sb1);
+        sb2 = warp_sum(sb2);
         if (lane == 0) {
-            s_bg[warp][0] = b0;
-            s_bg[warp][1] = b1;
-            s_bg[warp][2] = b2;
+            s_bg[warp][0] = sb0;
+            s_bg[warp][1] = sb1;
+            s_bg[warp][2] = sb2;
         }
     }
     __syncthreads();
@@ -218,51 +280,66 @@ __global__ void __launch_bounds__(kThreads)
         atomicAdd(&gr.grad_backgrounds[3 * tr.c + tid], v);
     }
     if (tr.masked || tr.start == tr.end) return;
-    if (inside && ra > 0.0f && last >= 0) atomicMax(&s_jmax, last);
+    const int warp_max = __reduce_max_sync(0xffffffffu, my_max);
+    if (lane == 0) atomicMax(&s_jmax, warp_max);
     __syncthreads();
     const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
-    for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kThreads) {
-        const int64_t b0 = max(tr.start, b1 - kThreads);
+    for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
+        const int64_t b0 = max(tr.start, b1 - kBatch);
         const int nb = (int)(b1 - b0);
         __syncthreads();
-        if (tid < nb) s_gid[tid] = stage_record(a, b1 - 1 - tid, s_mo, s_q, s_col, tid);
+        for (int i = tid; i < nb; i += kThreads)
+            s_gid[i] = stage_record(a, b1 - 1 - i, s_mo, s_q, s_col, i);
         __syncthreads();
-        for (int k = 0; k < nb; ++k) {
-            const int64_t j = b1 - 1 - k;
-            const float4 mo = s_mo[k];
-            const float4 q = s_q[k];
-            const PairEval e = eval_pair(mo.x, mo.y, q.x, q.y, q.z, mo.z, px, py);
-            const bool valid = ra > 0.0f && e.s >= 0.0f && e.alpha >= a.alpha_cutoff &&
-                               (int64_t)last >= j && Tc < 1.0f && e.alpha < 1.0f;
-            if (!__any_sync(0xffffffffu, valid)) continue;
+        // entries of this batch beyond the warp's largest last_id are skipped
+        const int first = (int)max((int64_t)0, b1 - 1 - (int64_t)warp_max);
+        for (int i = first; i < nb; ++i) {
+            const int64_t j = b1 - 1 - i;
+            const float4 mo = s_mo[i];
+            const float4 q = s_q[i];
+            const float4 col = s_col[i];
+            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+            const float hdx2 = 0.5f * ct.dx * ct.dx;
             float v_c0 = 0.f, v_c1 = 0.f, v_c2 = 0.f, v_op = 0.f, v_mx = 0.f, v_my = 0.f;
             float v_qa = 0.f, v_qb = 0.f, v_qc = 0.f, v_ax = 0.f, v_ay = 0.f;
-            if (valid) {
-                const float4 col = s_col[k];
+            bool any = false;
+#pragma unroll
+            for (int k = 0; k < kPPT; ++k) {
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                const bool valid = ra[k] > 0.0f && e.s >= 0.0f && e.alpha >= a.alpha_cutoff &&
+                                   (int64_t)last[k] >= j && Tc[k] < 1.0f && e.alpha < 1.0f;
+                if (!valid) continue;
+                any = true;
                 const float one_m = 1.0f - e.alpha;
-                const float Tb = __fdividef(Tc, one_m);
+                const float Tb = __fdividef(Tc[k], one_m);
                 const float vis = Tb * e.alpha;
-                v_c0 = g0 * vis;
-                v_c1 = g1 * vis;
-                v_c2 = g2 * vis;
-                const float dot = g0 * (col.x - rem0) + g1 * (col.y - rem1) + g2 * (col.z - rem2);
-                const float g_alpha = Tb * (dot + ga * Ta);
+                v_c0 += g0[k] * vis;
+                v_c1 += g1[k] * vis;
+                v_c2 += g2[k] * vis;
+                const float dot = g0[k] * (col.x - r0[k]) + g1[k] * (col.y - r1[k]) +
+                                  g2[k] * (col.z - r2[k]);
+                const float g_alpha = Tb * (dot + ga[k] * Ta[k]);
                 const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
-                v_op = g_raw * e.resp;
+                v_op += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
-                v_mx = g_s * (q.x * e.dx + q.y * e.dy);
-                v_my = g_s * (q.z * e.dy + q.y * e.dx);
-                v_ax = fabsf(v_mx);
-                v_ay = fabsf(v_my);
-                v_qa = g_s * 0.5f * e.dx * e.dx;
-                v_qb = g_s * e.dx * e.dy;
-                v_qc = g_s * 0.5f * e.dy * e.dy;
-                rem0 = e.alpha * col.x + one_m * rem0;
-                rem1 = e.alpha * col.y + one_m * rem1;
-                rem2 = e.alpha * col.z + one_m * rem2;
-                Ta *= one_m;
-                Tc = Tb;
+                const float mx = g_s * (q.x * ct.dx + q.y * e.dy);
+                const float my = g_s * (q.z * e.dy + q.y * ct.dx);
+                v_mx += mx;
+                v_my += my;
+                if (ABS) {
+                    v_ax += fabsf(mx);
+                    v_ay += fabsf(my);
+                }
+                v_qa += g_s * hdx2;
+                v_qb += g_s * (ct.dx * e.dy);
+                v_qc += g_s * (0.5f * e.dy * e.dy);
+                r0[k] = e.alpha * col.x + one_m * r0[k];
+                r1[k] = e.alpha * col.y + one_m * r1[k];
+                r2[k] = e.alpha * col.z + one_m * r2[k];
+                Ta[k] *= one_m;
+                Tc[k] = Tb;
             }
+            if (!__any_sync(0xffffffffu, any)) continue;
             v_c0 = warp_sum(v_c0);
             v_c1 = warp_sum(v_c1);
             v_c2 = warp_sum(v_c2);
@@ -272,12 +349,12 @@ __global__ void __launch_bounds__(kThreads)
             v_qa = warp_sum(v_qa);
             v_qb = warp_sum(v_qb);
             v_qc = warp_sum(v_qc);
-            if (gr.grad_means2d_abs) {
+            if (ABS) {
                 v_ax = warp_sum(v_ax);
                 v_ay = warp_sum(v_ay);
             }
-            if (lane == 0 && s_gid[k] >= 0) {
-                const int64_t g = s_gid[k];
+            if (lane == 0 && s_gid[i] >= 0) {
+                const int64_t g = s_gid[i];
                 atomicAdd(&gr.grad_colors[3 * g], v_c0);
                 atomicAdd(&gr.grad_colors[3 * g + 1], v_c1);
                 atomicAdd(&gr.grad_colors[3 * g + 2], v_c2);
@@ -287,7 +364,7 @@ __global__ void __launch_bounds__(kThreads)
                 atomicAdd(&gr.grad_conics[3 * g], v_qa);
                 atomicAdd(&gr.grad_conics[3 * g + 1], v_qb);
                 atomicAdd(&gr.grad_conics[3 * g + 2], v_qc);
-                if (gr.grad_means2d_abs) {
+                if (ABS) {
                     atomicAdd(&gr.grad_means2d_abs[2 * g], v_ax);
                     atomicAdd(&gr.grad_means2d_abs[2 * g + 1], v_ay);
                 }
@@ -313,7 +390,10 @@ void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_
 void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
-    k_raster_bwd<<<(unsigned)tiles, kThreads, 0, s>>>(a, g);
+    if (g.grad_means2d_abs)
+        k_raster_bwd<true><<<(unsigned)tiles, kThreads, 0, s>>>(a, g);
+    else
+        k_raster_bwd<false><<<(unsigned)tiles, kThreads, 0, s>>>(a, g);
 }
 
 }  // namespace gs
