@@ -226,6 +226,34 @@ int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit,
                   int end_bit, void* workspace, size_t workspace_bytes,
                   int32_t* d_status, void* stream);
 
+/* Largest n gs_sort_pairs_noalloc accepts. */
+#define GS_SORT_NOALLOC_MAX_PAIRS (1 << 20)
+
+/*
+ * gs_sort_pairs_noalloc -- no counterpart on the pages: a convenience for
+ * callers of this library that cannot allocate device memory, such as code
+ * running inside a host framework that owns every device allocation and
+ * forbids others, or a loop that must never pay for an allocation, and
+ * therefore cannot hand gs_sort_pairs its workspace.
+ * Same result as gs_sort_pairs (stable, ascending by key bits
+ * [begin_bit, end_bit), in place), but it allocates nothing and takes no
+ * workspace: its scratch space is one fixed device array inside the library
+ * (about 17.6 MB, held on every GPU that loads the library until the process
+ * exits), sized for n <= GS_SORT_NOALLOC_MAX_PAIRS.
+ *   - n > GS_SORT_NOALLOC_MAX_PAIRS returns GS_ERR_CAPACITY, nothing enqueued.
+ *   - It runs on the current device.  Its first call on a device looks up the
+ *     array's device address there (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one array and clears what must start at zero, so
+ *     calls whose GPU work overlaps (other streams, other host threads on the
+ *     same device) race: order them on one stream or synchronise between them.
+ *   - keys, values: caller-owned device arrays; d_status, stream: as for every
+ *     call of this library.
+ */
+int gs_sort_pairs_noalloc(uint64_t* keys, int32_t* values, int64_t n,
+                          int begin_bit, int end_bit, int32_t* d_status,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,7 @@ SIGNATURES = {
                                P, P, P, P, P, P, P, P, P, P, P, P]),
     "gs_sort_workspace_size": (SZ, [I64]),
     "gs_sort_pairs": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
+    "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
 }
 
 
@@ -224,4 +225,17 @@ def gs_sort_pairs(keys, values, begin_bit=0, end_bit=64, d_status=None, workspac
         _empty(max(need, 1), torch.uint8, keys.device)
     _check(lib().gs_sort_pairs(_ptr(keys), _ptr(values), n, begin_bit, end_bit, _ptr(ws),
                                ws.numel(), _ptr(d_status), _stream(stream)), "gs_sort_pairs")
+    return keys, values
+
+
+SORT_NOALLOC_MAX_PAIRS = 1 << 20
+
+
+def gs_sort_pairs_noalloc(keys, values, begin_bit=0, end_bit=64, d_status=None, stream=None):
+    """gs_sort_pairs without a workspace: the library's own fixed scratch
+    array is used (n <= SORT_NOALLOC_MAX_PAIRS; calls on one device must not
+    overlap on the GPU)."""
+    _check(lib().gs_sort_pairs_noalloc(_ptr(keys), _ptr(values), keys.numel(), begin_bit,
+                                       end_bit, _ptr(d_status), _stream(stream)),
+           "gs_sort_pairs_noalloc")
     return keys, values
