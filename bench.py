@@ -162,6 +162,7 @@ class Path:
         self.rgb = torch.empty((s.C, s.height, s.width, 3), dtype=torch.float32, device=dev)
         self.alpha = torch.empty((s.C, s.height, s.width, 1), dtype=torch.float32, device=dev)
         self.last = torch.empty((s.C, s.height, s.width), dtype=torch.int32, device=dev)
+        self.trace = torch.empty((I, 8), dtype=torch.int32, device=dev)
         self.grads = dict(
             grad_means2d=torch.empty((s.C, s.N, 2), dtype=torch.float32, device=dev),
             grad_conics=torch.empty((s.C, s.N, 3), dtype=torch.float32, device=dev),
@@ -198,14 +199,16 @@ class Path:
         self.gs.gs_rasterize_fwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None,
                                  None, s.width, s.height, s.tile_size, self.offsets, self.ids,
                                  s.alpha_cutoff, s.transmittance_threshold, d_status=self.status,
-                                 out=(self.rgb, self.alpha, self.last), pair_counts=pair_counts)
+                                 out=(self.rgb, self.alpha, self.last), pair_counts=pair_counts,
+                                 trace=self.trace)
 
     def backward(self):
         s, d = self.s, self.d
         self.gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None,
                                  None, s.width, s.height, s.tile_size, self.offsets, self.ids,
                                  s.alpha_cutoff, self.alpha, self.last, d["grad_render_colors"],
-                                 d["grad_render_alphas"], d_status=self.status, out=self.grads)
+                                 d["grad_render_alphas"], d_status=self.status, out=self.grads,
+                                 trace=self.trace)
 
     def step(self, ev=None):
         """ev: 6 CUDA events recorded between the stages, or None."""
@@ -285,19 +288,13 @@ def run_ours(args, rank, world, scene):
     path.gs.check_status(path.status, "warmup")
 
     # work measures for the roofline (outside the timed region)
-    counts = torch.zeros((s.C, s.height, s.width, 2), dtype=torch.int32, device=dev)
+    counts = torch.zeros((s.C, s.height, s.width, 3), dtype=torch.int32, device=dev)
     path.forward(pair_counts=counts)
     n_eval = int(counts[..., 0].sum(dtype=torch.int64))
     n_comp = int(counts[..., 1].sum(dtype=torch.int64))
+    bwd_eval = int(counts[..., 2].sum(dtype=torch.int64))
     offs = path.offsets.reshape(-1).to(torch.int64)
     ends = torch.cat([offs[1:], torch.tensor([path.I], device=dev)])
-    ty = torch.arange(s.height, device=dev) // 16
-    tx = torch.arange(s.width, device=dev) // 16
-    tile = (torch.arange(s.C, device=dev)[:, None, None] * s.tile_height + ty[None, :, None]) \
-        * s.tile_width + tx[None, None, :]
-    start = offs[tile]
-    last = path.last.to(torch.int64)
-    bwd_eval = int(torch.where(last >= 0, last - start + 1, torch.zeros_like(last)).sum())
     list_len = (ends - offs)
     max_list = int(list_len.max())
 

@@ -151,9 +151,17 @@ int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
  *   (C,TH,TW) or NULL, offsets int32 (C,TH,TW), flatten_ids int32
  *   (n_isects) -- flatten ids index the (C*N) splat arrays.
  * Outputs: render_colors float32 (C,H,W,channels), render_alphas float32
- *   (C,H,W,1), last_ids int32 (C,H,W); pair_counts int32 (C,H,W,2) or NULL:
- *   per pixel the list entries visited before it stopped and the entries it
- *   composited (a work measure, e.g. for throughput accounting).
+ *   (C,H,W,1), last_ids int32 (C,H,W); pair_counts int32 (C,H,W,3) or NULL:
+ *   a work measure per pixel -- the list entries evaluated before the pixel
+ *   stopped, the entries composited, and the entries evaluated up to and
+ *   including the last composited one (entries whose splat cannot reach the
+ *   cutoff anywhere in the tile are skipped unevaluated and not counted).
+ *   trace uint32 (n_isects, 8) or NULL, 16-byte aligned: per list entry, a
+ *   256-bit mask of the tile's pixels that composited it (the forward's
+ *   decisions, for gs_rasterize_bwd).  Words of entries past the point where
+ *   every pixel of the tile had stopped are not written.  Bit layout: word
+ *   w (0..7), bit l covers tile pixel column (32 (w / 4) + l) % 16, row
+ *   4 ((32 (w / 4) + l) / 16) + w % 4.
  * Supported: channels == 3, tile_size == 16; TH = ceil(H/16), TW = ceil(W/16).
  */
 int gs_rasterize_fwd(const float* means2d, const float* conics,
@@ -164,7 +172,7 @@ int gs_rasterize_fwd(const float* means2d, const float* conics,
                      const int32_t* flatten_ids, int64_t n_isects,
                      float alpha_cutoff, float transmittance_threshold,
                      float* render_colors, float* render_alphas,
-                     int32_t* last_ids, int32_t* pair_counts,
+                     int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
                      int32_t* d_status, void* stream);
 
 /*
@@ -185,6 +193,10 @@ int gs_rasterize_fwd(const float* means2d, const float* conics,
  *   rem = alpha color + (1 - alpha) rem; T_after *= 1 - alpha; T = T_before
  * dL/dbackgrounds += g_rgb (1 - render_alpha) per pixel.
  * grad_means2d_abs (absgrad, optional) sums |dL/dmeans2d| per pixel term.
+ * trace (optional): the mask table gs_rasterize_fwd wrote for the same
+ * inputs.  With it, only the pairs the forward composited are revisited;
+ * without it, alpha is re-evaluated for every entry up to each pixel's
+ * last_id.  Both give the same result (each pair is re-tested either way).
  * Inputs: the forward's inputs (means2d ... n_isects, alpha_cutoff),
  *   render_alphas float32 (C,H,W,1), last_ids int32 (C,H,W),
  *   grad_render_colors float32 (C,H,W,channels),
@@ -207,8 +219,8 @@ int gs_rasterize_bwd(const float* means2d, const float* conics,
                      const float* grad_render_alphas, float* grad_means2d,
                      float* grad_conics, float* grad_colors,
                      float* grad_opacities, float* grad_backgrounds,
-                     float* grad_means2d_abs, int32_t* d_status,
-                     void* stream);
+                     float* grad_means2d_abs, const uint32_t* trace,
+                     int32_t* d_status, void* stream);
 
 /* Bytes of workspace gs_sort_pairs needs for n pairs. */
 size_t gs_sort_workspace_size(int64_t n);

@@ -68,7 +68,7 @@ def test_argument_errors_without_gpu(lib):
     assert lib.gs_tile_offsets(None, 5, 1, 4, 4, P(8), None, None) == 1
     assert lib.gs_rasterize_fwd(P(8), P(8), P(8), P(8), None, None, 1, 10, 4, 64, 64, 16, P(8),
                                 P(8), 10, ct.c_float(0.1), ct.c_float(0.1), P(8), P(8), P(8),
-                                None, None, None) == 1
+                                None, None, None, None) == 1
     assert lib.gs_sort_pairs(None, None, 5, 0, 64, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 65, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 64, None, 0, None, None) == 4

@@ -162,16 +162,30 @@ def test_backward_masks_and_dense_stack():
     _compare_grads(rb, got, excluded)
 
 
-def test_forward_then_backward_on_gpu_state():
+def _gpu_fwd_with_trace(s, d, masks=None):
+    f = gpu_forward(s, d, masks=masks)
+    trace = torch.empty((f["flatten_ids"].numel(), 8), dtype=torch.int32, device=DEV)
+    gs.gs_rasterize_fwd(d["means2d"], d["conics"], d["colors"], d["opacities"], d["backgrounds"],
+                        None if masks is None else to_dev(masks), s.width, s.height, 16,
+                        f["offsets"], f["flatten_ids"], s.alpha_cutoff,
+                        s.transmittance_threshold, trace=trace,
+                        out=(f["render_colors"], f["render_alphas"], f["last_ids"]))
+    return f, trace
+
+
+@pytest.mark.parametrize("trace", [False, True])
+def test_forward_then_backward_on_gpu_state(trace):
     # end to end on the GPU: the backward consumes the GPU forward's outputs
+    # (and, with trace, its per-entry composite masks)
     s = scenes.random_small(11, C=1, N=3000, W=128, H=128, sigma=(0.5, 8.0))
     d = scene_to_dev(s)
-    f = gpu_forward(s, d)
+    f, tr = _gpu_fwd_with_trace(s, d)
     g_rgb, g_a = scenes.upstream_grads(1, 128, 128, seed=1)
     got = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"],
                               d["backgrounds"], None, 128, 128, 16, f["offsets"],
                               f["flatten_ids"], s.alpha_cutoff, f["render_alphas"],
-                              f["last_ids"], to_dev(g_rgb), to_dev(g_a))
+                              f["last_ids"], to_dev(g_rgb), to_dev(g_a),
+                              trace=tr if trace else None)
     iso, ref = _oracle_forward(s)
     rb = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None,
                               128, 128, 16, iso["offsets"], iso["flatten_ids"], s.alpha_cutoff,
@@ -192,3 +206,34 @@ def test_raster_argument_errors():
         gs.gs_rasterize_fwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None, None,
                             32, 32, 8, off, ids, 1 / 255, 1e-4)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("case", ["w2", "ragged_bg_masks", "dense"])
+def test_backward_trace_equals_recompute(case):
+    # the trace only tells the backward which pairs to revisit: the gradients
+    # must match the re-evaluating path up to the order of float atomics
+    masks = None
+    if case == "w2":
+        s = scenes.workload(2)
+    elif case == "ragged_bg_masks":
+        s = scenes.random_small(3, C=2, N=4000, W=150, H=90, sigma=(0.5, 10.0))
+        masks = np.random.default_rng(1).integers(0, 2, (2, 6, 10)).astype(np.int32)
+    else:
+        s = scenes.random_small(6, C=1, N=6000, W=64, H=64, sigma=(3.0, 12.0),
+                                opacity=(0.5, 0.99))
+    d = scene_to_dev(s)
+    f, tr = _gpu_fwd_with_trace(s, d, masks=masks)
+    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, seed=2)
+    args = (d["means2d"], d["conics"], d["colors"], d["opacities"], d["backgrounds"],
+            None if masks is None else to_dev(masks), s.width, s.height, 16, f["offsets"],
+            f["flatten_ids"], s.alpha_cutoff, f["render_alphas"], f["last_ids"], to_dev(g_rgb),
+            to_dev(g_a))
+    a = gs.gs_rasterize_bwd(*args, absgrad=True)
+    b = gs.gs_rasterize_bwd(*args, absgrad=True, trace=tr)
+    for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities",
+              "grad_means2d_abs", "grad_backgrounds"):
+        if a[k] is None:
+            continue
+        x, y = a[k].cpu().numpy(), b[k].cpu().numpy()
+        scale = np.abs(x).max() + 1e-30
+        np.testing.assert_allclose(y, x, rtol=1e-4, atol=1e-6 * scale, err_msg=k)

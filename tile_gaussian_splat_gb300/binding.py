@@ -35,9 +35,9 @@ SIGNATURES = {
                              P, P]),
     "gs_tile_offsets": (I32, [P, I64, I32, I32, I32, P, P, P]),
     "gs_rasterize_fwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I64, F32,
-                               F32, P, P, P, P, P, P]),
+                               F32, P, P, P, P, P, P, P]),
     "gs_rasterize_bwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I64, F32,
-                               P, P, P, P, P, P, P, P, P, P, P, P]),
+                               P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "gs_sort_workspace_size": (SZ, [I64]),
     "gs_sort_pairs": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
     "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
@@ -164,10 +164,12 @@ def gs_tile_offsets(keys, C, tile_width, tile_height, d_status=None, out=None, s
 
 def gs_rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                      tile_size, offsets, flatten_ids, alpha_cutoff, transmittance_threshold,
-                     d_status=None, out=None, pair_counts=None, stream=None):
+                     d_status=None, out=None, pair_counts=None, trace=None, stream=None):
     """Returns (render_colors (C,H,W,ch), render_alphas (C,H,W,1), last_ids (C,H,W)).
-    pair_counts: optional int32 (C,H,W,2) tensor that receives per pixel the
-    entries visited and the entries composited."""
+    pair_counts: optional int32 (C,H,W,3) tensor that receives per pixel the
+    entries evaluated, the entries composited and the entries evaluated up
+    to the last composited one.  trace: optional int32 (n_isects, 8) tensor
+    that receives the per-entry composite masks for gs_rasterize_bwd."""
     C, N = means2d.shape[:2]
     ch = colors.shape[-1]
     dev = means2d.device
@@ -180,17 +182,18 @@ def gs_rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, wid
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
         _ptr(masks), C, N, ch, width, height, tile_size, _ptr(offsets), _ptr(flatten_ids),
         flatten_ids.numel(), float(alpha_cutoff), float(transmittance_threshold), _ptr(rgb),
-        _ptr(alpha), _ptr(last), _ptr(pair_counts), _ptr(d_status), _stream(stream)),
-        "gs_rasterize_fwd")
+        _ptr(alpha), _ptr(last), _ptr(pair_counts), _ptr(trace), _ptr(d_status),
+        _stream(stream)), "gs_rasterize_fwd")
     return rgb, alpha, last
 
 
 def gs_rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                      tile_size, offsets, flatten_ids, alpha_cutoff, render_alphas, last_ids,
                      grad_render_colors, grad_render_alphas, want_grad_backgrounds=None,
-                     absgrad=False, d_status=None, out=None, stream=None):
+                     absgrad=False, d_status=None, out=None, trace=None, stream=None):
     """Returns dict(grad_means2d, grad_conics, grad_colors, grad_opacities,
-    grad_backgrounds (or None), grad_means2d_abs (or None))."""
+    grad_backgrounds (or None), grad_means2d_abs (or None)).  trace: the mask
+    table the forward wrote for the same inputs (optional, faster)."""
     C, N = means2d.shape[:2]
     ch = colors.shape[-1]
     dev = means2d.device
@@ -210,8 +213,8 @@ def gs_rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, wid
         flatten_ids.numel(), float(alpha_cutoff), _ptr(render_alphas), _ptr(last_ids),
         _ptr(grad_render_colors), _ptr(grad_render_alphas), _ptr(out["grad_means2d"]),
         _ptr(out["grad_conics"]), _ptr(out["grad_colors"]), _ptr(out["grad_opacities"]),
-        _ptr(out["grad_backgrounds"]), _ptr(out["grad_means2d_abs"]), _ptr(d_status),
-        _stream(stream)), "gs_rasterize_bwd")
+        _ptr(out["grad_backgrounds"]), _ptr(out["grad_means2d_abs"]), _ptr(trace),
+        _ptr(d_status), _stream(stream)), "gs_rasterize_bwd")
     return out
 
 

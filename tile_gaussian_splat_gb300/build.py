@@ -66,6 +66,6 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
 
 if __name__ == "__main__":
-    extra = [a for a in sys.argv[1:] if a.startswith("-X") or a.startswith("--")]
+    extra = [a for a in sys.argv[1:] if a.startswith(("-X", "--", "-D"))]
     print(build(force="--force" in sys.argv, verbose=True,
                 extra=[a for a in extra if a != "--force"]))

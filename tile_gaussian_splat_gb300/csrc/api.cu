@@ -294,7 +294,7 @@ int gs_rasterize_fwd(const float* means2d, const float* conics, const float* col
                      const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
                      float alpha_cutoff, float transmittance_threshold, float* render_colors,
                      float* render_alphas, int32_t* last_ids, int32_t* pair_counts,
-                     int32_t* d_status, void* stream) {
+                     uint32_t* trace, int32_t* d_status, void* stream) {
     (void)d_status;
     if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
                         tile_size, offsets, flatten_ids, n_isects))
@@ -303,7 +303,8 @@ int gs_rasterize_fwd(const float* means2d, const float* conics, const float* col
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
                  offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold};
-    launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts,
+    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
+    launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts, trace,
                       static_cast<cudaStream_t>(stream));
     return check_launch();
 }
@@ -316,7 +317,7 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
                      const float* grad_render_colors, const float* grad_render_alphas,
                      float* grad_means2d, float* grad_conics, float* grad_colors,
                      float* grad_opacities, float* grad_backgrounds, float* grad_means2d_abs,
-                     int32_t* d_status, void* stream) {
+                     const uint32_t* trace, int32_t* d_status, void* stream) {
     (void)d_status;
     if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
                         tile_size, offsets, flatten_ids, n_isects))
@@ -346,7 +347,8 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
     RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                   grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                   grad_means2d_abs};
-    launch_raster_bwd(a, g, s);
+    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
+    launch_raster_bwd(a, g, trace, s);
     return check_launch();
 }
 

@@ -80,8 +80,10 @@ struct RasterArgs {
     float alpha_cutoff, transmittance_threshold;
 };
 
+// trace (may be null): per list entry 8 words, the tile pixels that composited it.
 void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_alphas,
-                       int32_t* last_ids, int32_t* pair_counts, cudaStream_t s);
+                       int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
+                       cudaStream_t s);
 
 struct RasterGrads {
     const float* render_alphas;
@@ -96,6 +98,7 @@ struct RasterGrads {
     float* grad_means2d_abs;
 };
 
-void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, cudaStream_t s);
+void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
+                       cudaStream_t s);
 
 }  // namespace gs

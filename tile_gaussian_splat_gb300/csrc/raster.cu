@@ -1,29 +1,33 @@
-// Forward compositing and its reverse-walk backward, one block per 16x16
-// tile, PPT pixels per thread in a vertical strip (thread t owns column
-// t % 16 and rows (t / 16) * PPT .. + PPT - 1 of the tile).
+// Forward compositing and its reverse-walk backward, one 64-thread block per
+// 16x16 tile, 4 pixels per thread in a vertical strip (thread t owns column
+// t % 16 and rows 4 (t / 16) .. 4 (t / 16) + 3 of the tile).
 //
-// Why strips: a splat record read from shared memory serves PPT pixels, and
-// the terms of the quadratic form that depend only on dx (a dx dx, b dx) are
-// computed once per thread and entry -- in the same rounding order as the
-// per-pixel formula, so results do not change.  In the backward a warp covers
-// 32 * PPT pixels, so the shuffle reduction of a splat's terms (and its
-// atomics) is paid once per 32 * PPT pixels.
+// Shared by both kernels:
+//  * The tile's sorted list is staged through shared memory in batches of 128
+//    records gathered through flatten_ids.  While staging, an entry whose
+//    splat cannot reach the alpha cutoff at any pixel centre of the tile is
+//    dropped (exact minimum of the quadratic form over the tile's
+//    pixel-centre rectangle, with a margin that covers the rounding of the
+//    per-pixel evaluation and of exp); such an entry is skipped by every
+//    pixel anyway, so results are unchanged.
+//  * A record read from shared memory serves the thread's 4 pixels, and the
+//    dx-only terms of the quadratic form (a dx dx, b dx) are computed once
+//    per entry in the per-pixel formula's own rounding order.
+//  * alpha comes from the same inline code in both kernels, so the backward
+//    makes exactly the forward's skip/composite decisions.
 //
-// Forward: the tile's sorted list is streamed through shared memory in
-// batches (records gathered through flatten_ids); a warp skips a batch when
-// all its pixels have stopped, and the block ends when every pixel has
-// (__syncthreads_count vote).
+// Forward: per-pixel state in registers; a warp skips a batch when all its
+// pixels have stopped; the block ends once every pixel has stopped.
 //
 // Backward (gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel): the
-// list is walked from the largest last_id of the tile down to the tile's
-// start; a warp skips entries beyond the largest last_id of its own pixels.
-// Each thread sums its pixels' terms in registers, the warp sums them with
-// shuffles, and lane 0 adds them to the gradients with one atomic per field
-// (the shuffle-then-atomic pattern of the mxnet depthwise backward-filter
-// kernel).  Warps with no valid pair for an entry skip both.
-//
-// alpha is computed by the same inline code in both kernels, so the backward
-// makes exactly the forward's skip/composite decisions.
+// list is walked from the tile's largest last_id down to its start.  For
+// each entry every thread evaluates alpha for its 4 pixels; the valid
+// (pixel, entry) pairs of the warp are then packed onto consecutive lanes,
+// which run the gradient recurrence for them with the per-pixel state
+// (T, T_after, rem, upstream gradients) kept in shared memory.  Each lane's
+// terms for the entry go to a per-warp shared buffer; every 4 entries the
+// warp sums the buffer column-wise (one lane per (entry, field)) and adds
+// the sums to the gradients with one atomic each.
 #include <cstdint>
 
 #include "gs_device.cuh"
@@ -33,13 +37,27 @@ namespace gs {
 
 namespace {
 
+// Blocks per SM each kernel is compiled to fit (register budget).
+#ifndef GS_FWD_MIN_BLOCKS
+#define GS_FWD_MIN_BLOCKS 12
+#endif
+#ifndef GS_BWD_MIN_BLOCKS
+#define GS_BWD_MIN_BLOCKS 10
+#endif
+
 constexpr int kTile = 16;
 constexpr int kPPT = 4;                          // pixels per thread
 constexpr int kThreads = kTile * kTile / kPPT;   // 64
-constexpr int kBatch = 2 * kThreads;             // records staged per batch
+constexpr int kWarps = kThreads / kWarp;         // 2
+constexpr int kBatchFwd = 2 * kThreads;          // records staged per batch (forward)
+constexpr int kBatchBwd = kThreads;              // records staged per batch (backward)
+constexpr int kWarpPix = kWarp * kPPT;           // pixels per warp (128)
+constexpr int kRedEntries = 2;                   // entries buffered per reduction
 constexpr float kAlphaClamp = 0.99f;
 
-// Per-entry terms shared by the PPT pixels of one column.
+// ---------------------------------------------------------------- per pair
+
+// Per-entry terms shared by the 4 pixels of one column.
 struct ColumnTerms {
     float dx, qa, bdx;  // dx = mx - px, qa = (a dx) dx, bdx = b dx
 };
@@ -71,6 +89,8 @@ __device__ __forceinline__ PairEval eval_pair(const ColumnTerms& ct, float my, f
     return e;
 }
 
+// ---------------------------------------------------------------- per tile
+
 struct TileRange {
     int64_t tile, start, end;
     int c, ty, tx;
@@ -97,25 +117,144 @@ __device__ __forceinline__ TileRange tile_range(const RasterArgs& a) {
     return r;
 }
 
-// Stages the record of list entry j into shared slot k.  A flatten id outside
-// [0, C*N) (only from corrupted input) becomes a record with opacity 0, which
-// never passes the cutoff.
-__device__ __forceinline__ int32_t stage_record(const RasterArgs& a, int64_t j, float4* s_mo,
-                                                float4* s_q, float4* s_col, int k) {
-    const int64_t g = a.flatten_ids[j];
-    if ((uint64_t)g >= (uint64_t)((int64_t)a.C * a.N)) {
-        s_mo[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        s_q[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        s_col[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        return -1;
+// Pixel-centre rectangle of the tile (clipped to the image) for the
+// cannot-reach test.
+struct TileBox {
+    float xlo, xhi, ylo, yhi, log_cut;
+    bool cull;
+};
+
+__device__ __forceinline__ TileBox tile_box(const RasterArgs& a, const TileRange& tr) {
+    TileBox b;
+    b.xlo = (float)(tr.tx * kTile) + 0.5f;
+    b.xhi = (float)min(tr.tx * kTile + kTile, a.width) - 0.5f;
+    b.ylo = (float)(tr.ty * kTile) + 0.5f;
+    b.yhi = (float)min(tr.ty * kTile + kTile, a.height) - 0.5f;
+    b.cull = a.alpha_cutoff > 0.0f && isfinite(a.alpha_cutoff);
+    b.log_cut = b.cull ? logf(a.alpha_cutoff) : 0.0f;
+    return b;
+}
+
+// True when o exp(-s) < cutoff at every pixel centre of the tile, with room
+// to spare: s is at least its minimum over the (continuous) pixel-centre
+// rectangle, which for a positive-definite form is 0 inside and otherwise
+// the smallest of the four edge minima (a 1-D quadratic each).  The margin
+// (1e-3 + 1e-5 of the form's magnitude over the rectangle) is far above the
+// rounding of the per-pixel float evaluation and of __expf, so an entry
+// dropped here fails the per-pixel alpha test at every pixel.
+__device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float my, float a,
+                                             float b, float c, float op) {
+    if (!t.cull) return false;
+    if (op <= 0.0f) return true;       // raw <= 0 < cutoff everywhere
+    if (!(op > 0.0f)) return false;    // NaN: leave it to the per-pixel path
+    if (!(a > 0.0f && c > 0.0f)) return false;
+    if (!(a * c - b * b > 1e-6f * (a * c))) return false;  // not clearly positive definite
+    float smin = 0.0f;
+    const bool inside = mx >= t.xlo && mx <= t.xhi && my >= t.ylo && my <= t.yhi;
+    if (!inside) {
+        smin = INFINITY;
+        const float xe[2] = {t.xlo, t.xhi};
+        const float ye[2] = {t.ylo, t.yhi};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float dx = mx - xe[k];
+            const float dy = fminf(fmaxf(__fdividef(-b * dx, c), my - t.yhi), my - t.ylo);
+            smin = fminf(smin, 0.5f * (a * dx * dx + c * dy * dy) + b * dx * dy);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float dy = my - ye[k];
+            const float dx = fminf(fmaxf(__fdividef(-b * dy, a), mx - t.xhi), mx - t.xlo);
+            smin = fminf(smin, 0.5f * (a * dx * dx + c * dy * dy) + b * dx * dy);
+        }
     }
-    const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
-    const float* q = a.conics + 3 * g;
-    const float* col = a.colors + 3 * g;
-    s_mo[k] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
-    s_q[k] = make_float4(q[0], q[1], q[2], 0.0f);
-    s_col[k] = make_float4(col[0], col[1], col[2], 0.0f);
-    return (int32_t)g;
+    const float DX = fmaxf(fabsf(mx - t.xlo), fabsf(mx - t.xhi));
+    const float DY = fmaxf(fabsf(my - t.ylo), fabsf(my - t.yhi));
+    const float M = 0.5f * (a * DX * DX + c * DY * DY) + fabsf(b) * DX * DY;
+    return smin > __logf(op) - t.log_cut + 1e-3f + 1e-5f * M;
+}
+
+
+// Trace words per list entry: one 32-bit mask per (warp, pixel slot) of the
+// tile, bit = lane.  Word w = warp * kPPT + k covers the pixels of slot k of
+// the threads of warp `warp`.
+constexpr int kTraceWords = kWarps * kPPT;  // 8 -> 256 pixels
+
+template <int BATCH, bool TRACE_IN>
+struct StageSmem {
+    static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
+    float4 mo[BATCH];   // mx, my, opacity, -
+    float4 q[BATCH];    // a, b, c, -
+    float4 col[BATCH];  // r, g, b, -
+    int32_t gid[BATCH];
+    int32_t j[BATCH];   // list position
+    uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
+    int32_t cnt[kPerThread * kWarps];
+};
+
+// Stages the entries [lo, hi) of the tile's list that can reach the cutoff,
+// in processing order (ascending positions, or descending when REVERSE),
+// packed from slot 0; with TRACE_IN also their trace words.  Returns how
+// many were staged.  Contains two __syncthreads.  A flatten id outside
+// [0, C*N) (only from corrupted input) is dropped.
+template <bool REVERSE, bool TRACE_IN, int BATCH>
+__device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox& box, int64_t lo,
+                                           int64_t hi, const uint32_t* __restrict__ trace,
+                                           StageSmem<BATCH, TRACE_IN>& st) {
+    constexpr int kPerThread = StageSmem<BATCH, TRACE_IN>::kPerThread;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = (int)(hi - lo);
+    const int64_t CN = (int64_t)a.C * a.N;
+    float4 mo[kPerThread], q[kPerThread];
+    int32_t gid[kPerThread];
+    int64_t jj[kPerThread];
+    unsigned ball[kPerThread];
+    bool keep[kPerThread];
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+        const int i = r * kThreads + tid;
+        keep[r] = false;
+        if (i < n) {
+            jj[r] = REVERSE ? hi - 1 - i : lo + i;
+            const int64_t g = a.flatten_ids[jj[r]];
+            if ((uint64_t)g < (uint64_t)CN) {
+                const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
+                const float* qq = a.conics + 3 * g;
+                mo[r] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
+                q[r] = make_float4(qq[0], qq[1], qq[2], 0.0f);
+                gid[r] = (int32_t)g;
+                keep[r] = !cannot_reach(box, m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
+            }
+        }
+        ball[r] = __ballot_sync(0xffffffffu, keep[r]);
+        if (lane == 0) st.cnt[r * kWarps + warp] = __popc(ball[r]);
+    }
+    __syncthreads();
+    int total = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThread * kWarps; ++k) total += st.cnt[k];
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+        int base = 0;
+        for (int k = 0; k < r * kWarps + warp; ++k) base += st.cnt[k];
+        if (keep[r]) {
+            const int pos = base + __popc(ball[r] & lt);
+            const float* cc = a.colors + 3 * (int64_t)gid[r];
+            st.mo[pos] = mo[r];
+            st.q[pos] = q[r];
+            st.col[pos] = make_float4(cc[0], cc[1], cc[2], 0.0f);
+            st.gid[pos] = gid[r];
+            st.j[pos] = (int32_t)jj[r];
+            if (TRACE_IN) {
+                const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = t[w];
+            }
+        }
+    }
+    __syncthreads();
+    return total;
 }
 
 struct PixelSlot {
@@ -129,26 +268,31 @@ __device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
     return p;
 }
 
-template <bool COUNT>
-__global__ void __launch_bounds__(kThreads)
+// ------------------------------------------------------------------ forward
+
+// At most 85 registers, so 12 blocks (24 warps) fit on an SM.
+template <bool COUNT, bool TRACE>
+__global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
-                 int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts) {
-    __shared__ float4 s_mo[kBatch];   // mx, my, opacity, -
-    __shared__ float4 s_q[kBatch];    // a, b, c, -
-    __shared__ float4 s_col[kBatch];  // r, g, b, -
+                 int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts,
+                 uint32_t* __restrict__ trace) {
+    constexpr int kBatch = kBatchFwd;
+    __shared__ StageSmem<kBatch, false> st;
+    __shared__ uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
     const TileRange tr = tile_range(a);
-    const int tid = threadIdx.x;
+    const TileBox box = tile_box(a, tr);
     const PixelSlot ps = pixel_slot(tr);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float px = (float)ps.x + 0.5f;
     float T[kPPT], cr[kPPT], cg[kPPT], cb[kPPT], py[kPPT];
-    int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT];
+    int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT], n_last[kPPT];
     bool done[kPPT];
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         T[k] = 1.0f;
         cr[k] = cg[k] = cb[k] = 0.0f;
         last[k] = -1;
-        n_eval[k] = n_comp[k] = 0;
+        n_eval[k] = n_comp[k] = n_last[k] = 0;
         done[k] = !(ps.x < a.width && ps.y0 + k < a.height);
         py[k] = (float)(ps.y0 + k) + 0.5f;
     }
@@ -157,30 +301,65 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int k = 0; k < kPPT; ++k) all_done &= done[k];
         if (__syncthreads_count(all_done) == kThreads) break;
-        const int nb = (int)min((int64_t)kBatch, tr.end - b0);
-        for (int i = tid; i < nb; i += kThreads) stage_record(a, b0 + i, s_mo, s_q, s_col, i);
-        __syncthreads();
-        if (__all_sync(0xffffffffu, all_done)) continue;
-        for (int i = 0; i < nb; ++i) {
-            const float4 mo = s_mo[i];
-            const float4 q = s_q[i];
-            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+        const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
+        if (TRACE)
+            for (int i = tid; i < kBatch * kTraceWords; i += kThreads) (&s_trace[0][0])[i] = 0u;
+        const int nb = stage_batch<false, false, kBatch>(a, box, b0, b0 + n_raw, nullptr, st);
+        if (!__all_sync(0xffffffffu, all_done)) {
+            for (int i = 0; i < nb; ++i) {
+                const float4 mo = st.mo[i];
+                const float4 q = st.q[i];
+                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+                const int32_t j = st.j[i];
+                // the 4 evaluations are independent and branch-free, so they
+                // interleave; only compositing branches
+                float alpha[kPPT];
+                bool took[kPPT];
 #pragma unroll
-            for (int k = 0; k < kPPT; ++k) {
-                if (done[k]) continue;
-                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                if (COUNT) ++n_eval[k];
-                if (!(e.s >= 0.0f) || e.alpha < a.alpha_cutoff) continue;
-                if (COUNT) ++n_comp[k];
-                const float4 col = s_col[i];
-                const float w = T[k] * e.alpha;
-                cr[k] += w * col.x;
-                cg[k] += w * col.y;
-                cb[k] += w * col.z;
-                T[k] = T[k] * (1.0f - e.alpha);
-                last[k] = (int32_t)(b0 + i);
-                if (T[k] < a.transmittance_threshold) done[k] = true;
+                for (int k = 0; k < kPPT; ++k) {
+                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                    alpha[k] = e.alpha;
+                    took[k] = !done[k] && e.s >= 0.0f && e.alpha >= a.alpha_cutoff;
+                    if (COUNT) n_eval[k] += done[k] ? 0 : 1;
+                }
+#pragma unroll
+                for (int k = 0; k < kPPT; ++k) {
+                    if (!took[k]) continue;
+                    const float4 col = st.col[i];
+                    const PairEval e{0.0f, 0.0f, 0.0f, 0.0f, alpha[k]};
+                    const float w = T[k] * e.alpha;
+                    cr[k] += w * col.x;
+                    cg[k] += w * col.y;
+                    cb[k] += w * col.z;
+                    T[k] = T[k] * (1.0f - e.alpha);
+                    last[k] = j;
+                    if (COUNT) {
+                        ++n_comp[k];
+                        n_last[k] = n_eval[k];
+                    }
+                    if (T[k] < a.transmittance_threshold) done[k] = true;
+                }
+                if (TRACE) {
+#pragma unroll
+                    for (int k = 0; k < kPPT; ++k) {
+                        const unsigned m = __ballot_sync(0xffffffffu, took[k]);
+                        if (lane == k) s_trace[j - b0][warp * kPPT + k] = m;
+                    }
+                }
+                // leave the batch early once every pixel of the warp has stopped
+                if ((i & 15) == 15) {
+                    bool d = true;
+#pragma unroll
+                    for (int k = 0; k < kPPT; ++k) d &= done[k];
+                    if (__all_sync(0xffffffffu, d)) break;
+                }
             }
+        }
+        if (TRACE) {
+            __syncthreads();
+            uint4* dst = reinterpret_cast<uint4*>(trace + b0 * kTraceWords);
+            const uint4* src = reinterpret_cast<const uint4*>(&s_trace[0][0]);
+            for (int i = tid; i < n_raw * (kTraceWords / 4); i += kThreads) dst[i] = src[i];
         }
     }
     float br = 0.0f, bgc = 0.0f, bb = 0.0f;
@@ -200,34 +379,85 @@ __global__ void __launch_bounds__(kThreads)
             out_alpha[p] = 1.0f - T[k];
             out_last[p] = last[k];
             if (COUNT) {
-                out_counts[2 * p] = n_eval[k];
-                out_counts[2 * p + 1] = n_comp[k];
+                out_counts[3 * p] = n_eval[k];
+                out_counts[3 * p + 1] = n_comp[k];
+                out_counts[3 * p + 2] = n_last[k];
             }
         }
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+// ----------------------------------------------------------------- backward
+
+// Per-pixel state of one warp's 128 pixels.  Pixel (slot k, lane l) lives at
+// k * 32 + ((l + 8 k) & 31): an owner's accesses for one slot hit 32
+// distinct banks, and the 4 pixels of one column (same lane, slots 0..3)
+// fall in 4 different banks when other lanes gather them.
+enum StateField { kTc = 0, kTa, kR0, kR1, kR2, kG0, kG1, kG2, kGA, kRA, kStateFields };
+// Gradient fields in the reduction buffer.
+enum GradField { kC0 = 0, kC1, kC2, kOp, kMx, kMy, kQa, kQb, kQc, kAx, kAy };
+
+__device__ __forceinline__ int sidx(int p) {  // p = k * 32 + lane
+    return (p & ~31) | ((p + ((p >> 5) << 3)) & 31);
 }
 
-template <bool ABS>
-__global__ void __launch_bounds__(kThreads) k_raster_bwd(RasterArgs a, RasterGrads gr) {
-    __shared__ float4 s_mo[kBatch];
-    __shared__ float4 s_q[kBatch];
-    __shared__ float4 s_col[kBatch];
-    __shared__ int32_t s_gid[kBatch];
-    __shared__ float s_bg[kThreads / kWarp][3];
+template <int F>
+struct BwdWarpSmem {
+    float state[kStateFields][kWarpPix];
+    int32_t last[kWarpPix];
+    int16_t list[kWarpPix];       // packed valid pairs: k * 32 + owner lane
+    float red[kRedEntries][F][kWarp + 1];
+    int32_t red_gid[kRedEntries];
+};
+
+template <int F>
+__device__ __forceinline__ void flush_reduction(BwdWarpSmem<F>& w, int nslots, const RasterGrads& gr,
+                                                int lane) {
+    __syncwarp();
+    for (int t = lane; t < nslots * F; t += kWarp) {
+        const int e = t / F, f = t - (t / F) * F;
+        const float* row = w.red[e][f];
+        float sum = 0.0f;
+#pragma unroll 8
+        for (int l = 0; l < kWarp; ++l) sum += row[l];
+        if (sum == 0.0f) continue;
+        const int64_t g = w.red_gid[e];
+        float* dst;
+        switch (f) {
+            case kC0: case kC1: case kC2: dst = gr.grad_colors + 3 * g + (f - kC0); break;
+            case kOp: dst = gr.grad_opacities + g; break;
+            case kMx: case kMy: dst = gr.grad_means2d + 2 * g + (f - kMx); break;
+            case kQa: case kQb: case kQc: dst = gr.grad_conics + 3 * g + (f - kQa); break;
+            default: dst = gr.grad_means2d_abs + 2 * g + (f - kAx); break;
+        }
+        atomicAdd(dst, sum);
+    }
+    __syncwarp();
+}
+
+// For each entry the warp's valid (pixel, entry) pairs -- from the forward's
+// trace masks with TRACE, else by re-evaluating alpha -- are packed onto
+// consecutive lanes, which run the gradient recurrence with the per-pixel
+// state in shared memory.  Each packed pair is re-evaluated with the
+// forward's arithmetic and re-tested in full before its gradient is taken,
+// so both paths give the same result.
+template <bool ABS, bool TRACE>
+__global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
+    k_raster_bwd(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
+    constexpr int F = ABS ? 11 : 9;
+    constexpr int kBatch = kBatchBwd;
+    __shared__ StageSmem<kBatch, TRACE> st;
+    __shared__ BwdWarpSmem<F> ws[kWarps];
+    __shared__ float s_bg[kWarps][3];
     __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
+    const TileBox box = tile_box(a, tr);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    BwdWarpSmem<F>& w = ws[warp];
     const PixelSlot ps = pixel_slot(tr);
     const float px = (float)ps.x + 0.5f;
 
-    float ra[kPPT], g0[kPPT], g1[kPPT], g2[kPPT], ga[kPPT], py[kPPT];
-    float Tc[kPPT], Ta[kPPT], r0[kPPT], r1[kPPT], r2[kPPT];
+    float ra[kPPT], py[kPPT];
     int32_t last[kPPT];
     float bg0 = 0.0f, bg1 = 0.0f, bg2 = 0.0f;
     if (a.backgrounds) {
@@ -240,33 +470,45 @@ __global__ void __launch_bounds__(kThreads) k_raster_bwd(RasterArgs a, RasterGra
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         const int y = ps.y0 + k;
+        const int si = sidx(k * kWarp + lane);
         py[k] = (float)y + 0.5f;
-        ra[k] = g0[k] = g1[k] = g2[k] = ga[k] = 0.0f;
+        ra[k] = 0.0f;
         last[k] = -1;
+        float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, ga = 0.0f;
         if (ps.x < a.width && y < a.height) {
             const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
             ra[k] = gr.render_alphas[p];
             last[k] = gr.last_ids[p];
-            g0[k] = gr.grad_render_colors[3 * p];
-            g1[k] = gr.grad_render_colors[3 * p + 1];
-            g2[k] = gr.grad_render_colors[3 * p + 2];
-            ga[k] = gr.grad_render_alphas[p];
+            g0 = gr.grad_render_colors[3 * p];
+            g1 = gr.grad_render_colors[3 * p + 1];
+            g2 = gr.grad_render_colors[3 * p + 2];
+            ga = gr.grad_render_alphas[p];
         }
-        Tc[k] = 1.0f - ra[k];
-        Ta[k] = 1.0f;
-        r0[k] = bg0;
-        r1[k] = bg1;
-        r2[k] = bg2;
-        sb0 += g0[k] * Tc[k];
-        sb1 += g1[k] * Tc[k];
-        sb2 += g2[k] * Tc[k];
+        const float Tc = 1.0f - ra[k];
+        w.state[kTc][si] = Tc;
+        w.state[kTa][si] = 1.0f;
+        w.state[kR0][si] = bg0;
+        w.state[kR1][si] = bg1;
+        w.state[kR2][si] = bg2;
+        w.state[kG0][si] = g0;
+        w.state[kG1][si] = g1;
+        w.state[kG2][si] = g2;
+        w.state[kGA][si] = ga;
+        w.state[kRA][si] = ra[k];
+        w.last[si] = last[k];
+        sb0 += g0 * Tc;
+        sb1 += g1 * Tc;
+        sb2 += g2 * Tc;
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
     if (tid == 0) s_jmax = -1;
     if (gr.grad_backgrounds) {
-        sb0 = warp_sum(sb0);
-        sb1 = warp_sum(sb1);
-        sb2 = warp_sum(sb2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sb0 += __shfl_xor_sync(0xffffffffu, sb0, o);
+            sb1 += __shfl_xor_sync(0xffffffffu, sb1, o);
+            sb2 += __shfl_xor_sync(0xffffffffu, sb2, o);
+        }
         if (lane == 0) {
             s_bg[warp][0] = sb0;
             s_bg[warp][1] = sb1;
@@ -276,7 +518,7 @@ __global__ void __launch_bounds__(kThreads) k_raster_bwd(RasterArgs a, RasterGra
     __syncthreads();
     if (gr.grad_backgrounds && tid < 3) {
         float v = 0.0f;
-        for (int w = 0; w < kThreads / kWarp; ++w) v += s_bg[w][tid];
+        for (int k = 0; k < kWarps; ++k) v += s_bg[k][tid];
         atomicAdd(&gr.grad_backgrounds[3 * tr.c + tid], v);
     }
     if (tr.masked || tr.start == tr.end) return;
@@ -284,116 +526,149 @@ __global__ void __launch_bounds__(kThreads) k_raster_bwd(RasterArgs a, RasterGra
     if (lane == 0) atomicMax(&s_jmax, warp_max);
     __syncthreads();
     const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
+    const unsigned lt = lanemask_lt();
+    const int x_tile = tr.tx * kTile;
+    const int y_tile = tr.ty * kTile;
+    int nslots = 0;
     for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
         const int64_t b0 = max(tr.start, b1 - kBatch);
-        const int nb = (int)(b1 - b0);
-        __syncthreads();
-        for (int i = tid; i < nb; i += kThreads)
-            s_gid[i] = stage_record(a, b1 - 1 - i, s_mo, s_q, s_col, i);
-        __syncthreads();
-        // entries of this batch beyond the warp's largest last_id are skipped
-        const int first = (int)max((int64_t)0, b1 - 1 - (int64_t)warp_max);
-        for (int i = first; i < nb; ++i) {
-            const int64_t j = b1 - 1 - i;
-            const float4 mo = s_mo[i];
-            const float4 q = s_q[i];
-            const float4 col = s_col[i];
-            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
-            const float hdx2 = 0.5f * ct.dx * ct.dx;
-            float v_c0 = 0.f, v_c1 = 0.f, v_c2 = 0.f, v_op = 0.f, v_mx = 0.f, v_my = 0.f;
-            float v_qa = 0.f, v_qb = 0.f, v_qc = 0.f, v_ax = 0.f, v_ay = 0.f;
-            bool any = false;
+        const int nb = stage_batch<true, TRACE, kBatch>(a, box, b0, b1, trace, st);
+        for (int i = 0; i < nb; ++i) {
+            const int32_t j = st.j[i];
+            if (j > warp_max) continue;  // warp-uniform
+            const float4 mo = st.mo[i];
+            const float4 q = st.q[i];
+            // 1. which pixels of the warp have a valid pair with this entry
+            int count = 0;
+            if (TRACE) {
+                const uint4 m4 = st.tr[i][warp];
+                const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int k = 0; k < kPPT; ++k) {
-                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                const bool valid = ra[k] > 0.0f && e.s >= 0.0f && e.alpha >= a.alpha_cutoff &&
-                                   (int64_t)last[k] >= j && Tc[k] < 1.0f && e.alpha < 1.0f;
-                if (!valid) continue;
-                any = true;
+                for (int k = 0; k < kPPT; ++k) {
+                    if ((m[k] >> lane) & 1u)
+                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                    count += __popc(m[k]);
+                }
+            } else {
+                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+#pragma unroll
+                for (int k = 0; k < kPPT; ++k) {
+                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                    bool valid = ra[k] > 0.0f && e.s >= 0.0f && e.alpha >= a.alpha_cutoff &&
+                                 last[k] >= j && e.alpha < 1.0f;
+                    if (valid) valid = w.state[kTc][sidx(k * kWarp + lane)] < 1.0f;
+                    const unsigned m = __ballot_sync(0xffffffffu, valid);
+                    if (valid) w.list[count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
+                    count += __popc(m);
+                }
+            }
+            if (count == 0) continue;  // warp-uniform
+            __syncwarp();
+            // 2. the packed pairs, one per lane
+            float v[F];
+#pragma unroll
+            for (int f = 0; f < F; ++f) v[f] = 0.0f;
+            const float4 col = st.col[i];
+            for (int L = lane; L < count; L += kWarp) {
+                const int p = w.list[L];
+                const int si = sidx(p);
+                const int ol = p & 31;
+                const int row = ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
+                const ColumnTerms ct =
+                    column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
+                const float Tc = w.state[kTc][si];
+                if (TRACE) {
+                    const bool valid = w.state[kRA][si] > 0.0f && e.s >= 0.0f &&
+                                       e.alpha >= a.alpha_cutoff && w.last[si] >= j &&
+                                       Tc < 1.0f && e.alpha < 1.0f;
+                    if (!valid) continue;
+                }
+                const float Ta = w.state[kTa][si];
+                const float r0 = w.state[kR0][si], r1 = w.state[kR1][si], r2 = w.state[kR2][si];
+                const float g0 = w.state[kG0][si], g1 = w.state[kG1][si], g2 = w.state[kG2][si];
+                const float ga = w.state[kGA][si];
                 const float one_m = 1.0f - e.alpha;
-                const float Tb = __fdividef(Tc[k], one_m);
+                const float Tb = __fdividef(Tc, one_m);
                 const float vis = Tb * e.alpha;
-                v_c0 += g0[k] * vis;
-                v_c1 += g1[k] * vis;
-                v_c2 += g2[k] * vis;
-                const float dot = g0[k] * (col.x - r0[k]) + g1[k] * (col.y - r1[k]) +
-                                  g2[k] * (col.z - r2[k]);
-                const float g_alpha = Tb * (dot + ga[k] * Ta[k]);
+                v[kC0] += g0 * vis;
+                v[kC1] += g1 * vis;
+                v[kC2] += g2 * vis;
+                const float dot = g0 * (col.x - r0) + g1 * (col.y - r1) + g2 * (col.z - r2);
+                const float g_alpha = Tb * (dot + ga * Ta);
                 const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
-                v_op += g_raw * e.resp;
+                v[kOp] += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
-                const float mx = g_s * (q.x * ct.dx + q.y * e.dy);
-                const float my = g_s * (q.z * e.dy + q.y * ct.dx);
-                v_mx += mx;
-                v_my += my;
+                const float gmx = g_s * (q.x * ct.dx + q.y * e.dy);
+                const float gmy = g_s * (q.z * e.dy + q.y * ct.dx);
+                v[kMx] += gmx;
+                v[kMy] += gmy;
+                v[kQa] += g_s * (0.5f * ct.dx * ct.dx);
+                v[kQb] += g_s * (ct.dx * e.dy);
+                v[kQc] += g_s * (0.5f * e.dy * e.dy);
                 if (ABS) {
-                    v_ax += fabsf(mx);
-                    v_ay += fabsf(my);
+                    v[kAx] += fabsf(gmx);
+                    v[kAy] += fabsf(gmy);
                 }
-                v_qa += g_s * hdx2;
-                v_qb += g_s * (ct.dx * e.dy);
-                v_qc += g_s * (0.5f * e.dy * e.dy);
-                r0[k] = e.alpha * col.x + one_m * r0[k];
-                r1[k] = e.alpha * col.y + one_m * r1[k];
-                r2[k] = e.alpha * col.z + one_m * r2[k];
-                Ta[k] *= one_m;
-                Tc[k] = Tb;
+                w.state[kR0][si] = e.alpha * col.x + one_m * r0;
+                w.state[kR1][si] = e.alpha * col.y + one_m * r1;
+                w.state[kR2][si] = e.alpha * col.z + one_m * r2;
+                w.state[kTa][si] = Ta * one_m;
+                w.state[kTc][si] = Tb;
             }
-            if (!__any_sync(0xffffffffu, any)) continue;
-            v_c0 = warp_sum(v_c0);
-            v_c1 = warp_sum(v_c1);
-            v_c2 = warp_sum(v_c2);
-            v_op = warp_sum(v_op);
-            v_mx = warp_sum(v_mx);
-            v_my = warp_sum(v_my);
-            v_qa = warp_sum(v_qa);
-            v_qb = warp_sum(v_qb);
-            v_qc = warp_sum(v_qc);
-            if (ABS) {
-                v_ax = warp_sum(v_ax);
-                v_ay = warp_sum(v_ay);
-            }
-            if (lane == 0 && s_gid[i] >= 0) {
-                const int64_t g = s_gid[i];
-                atomicAdd(&gr.grad_colors[3 * g], v_c0);
-                atomicAdd(&gr.grad_colors[3 * g + 1], v_c1);
-                atomicAdd(&gr.grad_colors[3 * g + 2], v_c2);
-                atomicAdd(&gr.grad_opacities[g], v_op);
-                atomicAdd(&gr.grad_means2d[2 * g], v_mx);
-                atomicAdd(&gr.grad_means2d[2 * g + 1], v_my);
-                atomicAdd(&gr.grad_conics[3 * g], v_qa);
-                atomicAdd(&gr.grad_conics[3 * g + 1], v_qb);
-                atomicAdd(&gr.grad_conics[3 * g + 2], v_qc);
-                if (ABS) {
-                    atomicAdd(&gr.grad_means2d_abs[2 * g], v_ax);
-                    atomicAdd(&gr.grad_means2d_abs[2 * g + 1], v_ay);
-                }
+            // 3. this entry's terms into the warp's reduction buffer
+#pragma unroll
+            for (int f = 0; f < F; ++f) w.red[nslots][f][lane] = v[f];
+            if (lane == 0) w.red_gid[nslots] = st.gid[i];
+            if (++nslots == kRedEntries) {
+                flush_reduction<F>(w, nslots, gr, lane);
+                nslots = 0;
+            } else {
+                __syncwarp();
             }
         }
     }
+    if (nslots) flush_reduction<F>(w, nslots, gr, lane);
 }
 
 }  // namespace
 
 void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_alphas,
-                       int32_t* last_ids, int32_t* pair_counts, cudaStream_t s) {
+                       int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
+                       cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
-    if (pair_counts)
-        k_raster_fwd<true><<<(unsigned)tiles, kThreads, 0, s>>>(a, render_colors, render_alphas,
-                                                                last_ids, pair_counts);
+    const dim3 g((unsigned)tiles), b(kThreads);
+    if (pair_counts && trace)
+        k_raster_fwd<true, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                 pair_counts, trace);
+    else if (pair_counts)
+        k_raster_fwd<true, false><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                  pair_counts, nullptr);
+    else if (trace)
+        k_raster_fwd<false, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                  nullptr, trace);
     else
-        k_raster_fwd<false><<<(unsigned)tiles, kThreads, 0, s>>>(a, render_colors, render_alphas,
-                                                                 last_ids, nullptr);
+        k_raster_fwd<false, false><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                   nullptr, nullptr);
 }
 
-void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, cudaStream_t s) {
+void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
+                       cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
-    if (g.grad_means2d_abs)
-        k_raster_bwd<true><<<(unsigned)tiles, kThreads, 0, s>>>(a, g);
-    else
-        k_raster_bwd<false><<<(unsigned)tiles, kThreads, 0, s>>>(a, g);
+    const dim3 gd((unsigned)tiles), b(kThreads);
+    if (g.grad_means2d_abs) {
+        if (trace)
+            k_raster_bwd<true, true><<<gd, b, 0, s>>>(a, g, trace);
+        else
+            k_raster_bwd<true, false><<<gd, b, 0, s>>>(a, g, nullptr);
+    } else {
+        if (trace)
+            k_raster_bwd<false, true><<<gd, b, 0, s>>>(a, g, trace);
+        else
+            k_raster_bwd<false, false><<<gd, b, 0, s>>>(a, g, nullptr);
+    }
 }
 
 }  // namespace gs
