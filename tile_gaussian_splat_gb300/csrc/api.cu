@@ -98,7 +98,7 @@ IsectLayout carve_isect(void* ws, const IsectPlan& p, int64_t n_isects, bool que
     L.hist_depth = cv.take<uint32_t>(4 * 256);
     L.hist_up = cv.take<uint32_t>(4 * 256);
     if (!query) {
-        L.lb_emit = cv.take<uint64_t>((size_t)((p.CN + kIsectThreads - 1) / kIsectThreads));
+        L.lb_emit = cv.take<uint64_t>((size_t)((p.CN + kEmitChunk - 1) / kEmitChunk));
         if (p.presort)
             for (int i = 0; i < 4; ++i)
                 L.lb_depth[i] = cv.take<uint64_t>((size_t)sort_blocks(p.CN, kTile32) * 256);

@@ -16,8 +16,8 @@ struct LookbackScratch {
 
 // ---- sort.cu
 constexpr int kSortThreads = 256;
-constexpr int kItems64 = 12;  // keys per thread, 64-bit keys
-constexpr int kItems32 = 16;  // keys per thread, 32-bit keys
+constexpr int kItems64 = 8;   // keys per thread, 64-bit keys
+constexpr int kItems32 = 12;  // keys per thread, 32-bit keys
 constexpr int kTile64 = kSortThreads * kItems64;
 constexpr int kTile32 = kSortThreads * kItems32;
 
@@ -47,6 +47,7 @@ void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32
 
 // ---- isect.cu
 constexpr int kIsectThreads = 256;
+constexpr int kEmitChunk = 2 * kIsectThreads;  // splats per emit block
 
 void launch_isect_count(const float* means2d, const float* radii, int elliptical, int64_t CN,
                         int tile_size, int tile_width, int tile_height, int32_t* tiles_per_gauss,

@@ -52,14 +52,15 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0 && sum) atomicAdd(total, (unsigned long long)sum);
 }
 
+constexpr int kEmitSplats = kEmitChunk;  // splats per emit block (2 per thread)
+
 struct EmitSmem {
-    int32_t incl[kThreads];   // inclusive prefix of counts in the chunk
-    int32_t x0[kThreads];
-    int32_t y0[kThreads];
-    int32_t w[kThreads];      // rect width in tiles
-    uint32_t upper[kThreads];  // camera << tile_bits
-    uint32_t dbits[kThreads];
-    int32_t sid[kThreads];
+    int32_t incl[kEmitSplats];  // inclusive prefix of counts in the chunk
+    int32_t rect[kEmitSplats];  // x0 | y0 << 16
+    int32_t w[kEmitSplats];     // rect width in tiles
+    uint32_t upper[kEmitSplats];  // camera << tile_bits
+    uint32_t dbits[kEmitSplats];
+    int32_t sid[kEmitSplats];
     uint32_t hist[4][256];
     int64_t scratch[32];
     int64_t base;
@@ -71,6 +72,35 @@ __device__ __forceinline__ void hist_inc(uint32_t* bins, uint32_t d, bool valid)
     if (!valid) return;
     unsigned peers = __match_any_sync(act, d);
     if ((peers & lanemask_lt()) == 0) atomicAdd(&bins[d], (uint32_t)__popc(peers));
+}
+
+// Exclusive prefix of this chunk's total over earlier chunks, by warp 0: the
+// 32 nearest predecessors' words are read at once (each lane waits on one),
+// summed up to the nearest inclusive prefix, and the window moves back until
+// one is found.  Lane 0 then publishes this chunk's inclusive prefix.
+__device__ __forceinline__ int64_t chunk_lookback(uint64_t* lookback, int64_t blk, int64_t total,
+                                                  const ErrorSink& err) {
+    const int lane = threadIdx.x & 31;
+    if (blk == 0) {
+        if (lane == 0) st_relaxed_u64(lookback, ((uint64_t)total << 2) | kFlagPrefix);
+        return 0;
+    }
+    if (lane == 0) st_relaxed_u64(lookback + blk, ((uint64_t)total << 2) | kFlagAggregate);
+    int64_t prefix = 0;
+    for (int64_t top = blk - 1;; top -= kWarp) {
+        const int64_t p = top - lane;
+        const uint64_t v = p >= 0 ? wait_published(lookback + p, err) : kFlagPrefix;
+        const unsigned pre = __ballot_sync(0xffffffffu, (v & kFlagMask) == kFlagPrefix);
+        // lanes up to (and including) the nearest inclusive prefix contribute
+        const int stop = pre ? __ffs(pre) - 1 : kWarp - 1;
+        int64_t c = lane <= stop ? (int64_t)(v >> 2) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        prefix += c;
+        if (pre) break;
+    }
+    if (lane == 0) st_relaxed_u64(lookback + blk, ((uint64_t)(prefix + total) << 2) | kFlagPrefix);
+    return prefix;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -88,53 +118,49 @@ __global__ void __launch_bounds__(kThreads)
         for (int i = tid; i < 4 * 256; i += kThreads) (&sm.hist[0][0])[i] = 0;
     __syncthreads();
     const int64_t blk = sm.blk;
-    const int64_t k = blk * kThreads + tid;
-    int cnt = 0;
-    if (k < CN) {
-        const int64_t s = order ? (int64_t)order[k] : k;
-        const float2 m = reinterpret_cast<const float2*>(means2d)[s];
-        float rx, ry;
-        if (elliptical) {
-            const float2 r = reinterpret_cast<const float2*>(radii)[s];
-            rx = r.x;
-            ry = r.y;
-        } else {
-            rx = ry = radii[s];
+    // splats 2 tid and 2 tid + 1 of the chunk
+    int cnt[2];
+    int64_t local = 0;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int slot = 2 * tid + u;
+        const int64_t k = blk * kEmitSplats + slot;
+        cnt[u] = 0;
+        if (k < CN) {
+            const int64_t s = order ? (int64_t)order[k] : k;
+            const float2 m = reinterpret_cast<const float2*>(means2d)[s];
+            float rx, ry;
+            if (elliptical) {
+                const float2 r = reinterpret_cast<const float2*>(radii)[s];
+                rx = r.x;
+                ry = r.y;
+            } else {
+                rx = ry = radii[s];
+            }
+            const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+            cnt[u] = (r.x1 - r.x0) * (r.y1 - r.y0);
+            sm.rect[slot] = r.x0 | (r.y0 << 16);
+            sm.w[slot] = r.x1 - r.x0;
+            sm.upper[slot] = (uint32_t)((uint64_t)(s / N) << tile_bits);
+            sm.dbits[slot] = __float_as_uint(depths[s]);
+            sm.sid[slot] = (int32_t)s;
+            if (tiles_per_gauss) tiles_per_gauss[s] = cnt[u];
         }
-        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
-        cnt = (r.x1 - r.x0) * (r.y1 - r.y0);
-        sm.x0[tid] = r.x0;
-        sm.y0[tid] = r.y0;
-        sm.w[tid] = r.x1 - r.x0;
-        sm.upper[tid] = (uint32_t)((uint64_t)(s / N) << tile_bits);
-        sm.dbits[tid] = __float_as_uint(depths[s]);
-        sm.sid[tid] = (int32_t)s;
-        if (tiles_per_gauss) tiles_per_gauss[s] = cnt;
+        local += cnt[u];
     }
     int64_t chunk_total;
-    const int64_t excl = block_exclusive_scan<kThreads>(cnt, sm.scratch, &chunk_total);
-    sm.incl[tid] = (int32_t)(excl + cnt);
-
-    // decoupled look-back over earlier chunks (thread 0)
-    if (tid == 0) {
-        uint64_t* mine = lookback + blk;
-        int64_t prefix = 0;
-        if (blk == 0) {
-            st_relaxed_u64(mine, ((uint64_t)chunk_total << 2) | kFlagPrefix);
-        } else {
-            st_relaxed_u64(mine, ((uint64_t)chunk_total << 2) | kFlagAggregate);
-            for (int64_t p = blk - 1;; --p) {
-                const uint64_t v = wait_published(lookback + p, err);
-                prefix += (int64_t)(v >> 2);
-                if ((v & kFlagMask) == kFlagPrefix || p == 0) break;
-            }
-            st_relaxed_u64(mine, ((uint64_t)(prefix + chunk_total) << 2) | kFlagPrefix);
+    const int64_t excl = block_exclusive_scan<kThreads>(local, sm.scratch, &chunk_total);
+    sm.incl[2 * tid] = (int32_t)(excl + cnt[0]);
+    sm.incl[2 * tid + 1] = (int32_t)(excl + cnt[0] + cnt[1]);
+    if (tid < kWarp) {
+        const int64_t prefix = chunk_lookback(lookback, blk, chunk_total, err);
+        if (tid == 0) {
+            sm.base = prefix;
+            const int64_t nchunks = (CN + kEmitSplats - 1) / kEmitSplats;
+            if (prefix + chunk_total > capacity) err.raise(GS_ERR_COUNT_MISMATCH);
+            if (blk == nchunks - 1 && prefix + chunk_total != capacity)
+                err.raise(GS_ERR_COUNT_MISMATCH);
         }
-        sm.base = prefix;
-        const int64_t nchunks = (CN + kThreads - 1) / kThreads;
-        if (prefix + chunk_total > capacity) err.raise(GS_ERR_COUNT_MISMATCH);
-        if (blk == nchunks - 1 && prefix + chunk_total != capacity)
-            err.raise(GS_ERR_COUNT_MISMATCH);
     }
     __syncthreads();
     const int64_t base = sm.base;
@@ -146,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
         uint32_t upper = 0;
         if (valid) {
             // owner: first o with incl[o] > q
-            int lo = 0, hi = kThreads - 1;
+            int lo = 0, hi = kEmitSplats - 1;
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
                 if (sm.incl[mid] > q) hi = mid;
@@ -156,8 +182,9 @@ __global__ void __launch_bounds__(kThreads)
             const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
             const int w = sm.w[o];
             const int dy = li / w;
-            const int ty = sm.y0[o] + dy;
-            const int tx = sm.x0[o] + (li - dy * w);
+            const int rc = sm.rect[o];
+            const int ty = (rc >> 16) + dy;
+            const int tx = (rc & 0xffff) + (li - dy * w);
             upper = sm.upper[o] | (uint32_t)(ty * tile_width + tx);
             const int64_t pos = base + q;
             if (pos < capacity) {
@@ -236,7 +263,7 @@ void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
                        LookbackScratch lb, uint32_t* up_hist, int up_passes,
                        int32_t* abort_flag, int32_t* d_status, cudaStream_t s) {
     if (CN <= 0) return;
-    const int64_t chunks = (CN + kThreads - 1) / kThreads;
+    const int64_t chunks = (CN + kEmitSplats - 1) / kEmitSplats;
     k_isect_emit<<<(unsigned)chunks, kThreads, 0, s>>>(
         means2d, radii, elliptical, depths, order, CN, (float)tile_size, tile_width, tile_height,
         N, tile_bits, keys, ids, capacity, tiles_per_gauss, lb.words, lb.ticket, up_hist,

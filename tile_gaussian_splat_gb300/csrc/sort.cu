@@ -40,38 +40,44 @@ __host__ __device__ __forceinline__ uint32_t digit_mask(int shift, int end_bit) 
     return bits <= 0 ? 0u : ((1u << bits) - 1u);
 }
 
-// Adds one to bin d of a shared histogram, one atomic per distinct digit in
-// the warp (equal digits are common: constant high bits of keys).
-__device__ __forceinline__ void warp_aggregated_inc(uint32_t* bins, uint32_t d, bool valid) {
-    unsigned act = __ballot_sync(0xffffffffu, valid);
-    if (!valid) return;
-    unsigned peers = __match_any_sync(act, d);
-    if ((peers & lanemask_lt()) == 0) atomicAdd(&bins[d], (uint32_t)__popc(peers));
-}
+constexpr int kHistPasses = 4;  // digit passes per histogram launch
 
 template <typename K>
 __global__ void __launch_bounds__(kThreads) k_digit_hist(const K* __restrict__ keys, int64_t n,
                                                          int shift0, int npasses, int end_bit,
                                                          uint32_t* __restrict__ hist) {
-    __shared__ uint32_t sh[8][256];
-    for (int i = threadIdx.x; i < 8 * 256; i += kThreads) (&sh[0][0])[i] = 0;
+    // one private histogram per warp: only lanes of one warp ever contend on
+    // an address, and a digit shared by the whole warp (common in high key
+    // bits) is added once by lane 0
+    __shared__ uint32_t sh[kWarps][kHistPasses][256];
+    for (int i = threadIdx.x; i < kWarps * kHistPasses * 256; i += kThreads) (&sh[0][0][0])[i] = 0;
     __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     // every lane of a warp runs the same trip count so the warp votes agree
     const int64_t begin = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t rounds = (n + stride - 1) / stride;
     for (int64_t r = 0; r < rounds; ++r) {
-        int64_t i = begin + r * stride;
-        bool valid = i < n;
-        K k = valid ? keys[i] : K(0);
-        for (int p = 0; p < npasses; ++p)
-            warp_aggregated_inc(sh[p],
-                                digit_of(k, shift0 + 8 * p, digit_mask(shift0 + 8 * p, end_bit)),
-                                valid);
+        const int64_t i = begin + r * stride;
+        const bool valid = i < n;
+        const K k = valid ? keys[i] : K(0);
+        const bool full = __all_sync(0xffffffffu, valid);
+        for (int p = 0; p < npasses; ++p) {
+            const int sh_p = shift0 + 8 * p;
+            const uint32_t d = digit_of(k, sh_p, digit_mask(sh_p, end_bit));
+            const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+            if (full && __all_sync(0xffffffffu, d == d0)) {
+                if (lane == 0) sh[warp][p][d] += 32u;
+            } else if (valid) {
+                atomicAdd(&sh[warp][p][d], 1u);
+            }
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < npasses * 256; i += kThreads) {
-        uint32_t v = (&sh[0][0])[i];
+        uint32_t v = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += (&sh[w][0][0])[i];
         if (v) atomicAdd(&hist[i], v);
     }
 }
@@ -89,7 +95,7 @@ struct OnesweepSmem {
 };
 
 template <typename K, int ITEMS, bool IOTA>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
     k_onesweep(const K* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
                K* __restrict__ keys_out, int32_t* __restrict__ vals_out, int64_t n, int shift,
                uint32_t dmask, const uint32_t* __restrict__ hist, uint64_t* __restrict__ lookback,
@@ -200,20 +206,26 @@ int hist_grid(int64_t n) {
 
 }  // namespace
 
-void launch_digit_hist_u64(const uint64_t* keys, int64_t n, int shift0, int end_bit,
-                           uint32_t* hist, cudaStream_t s) {
+template <typename K>
+void digit_hist(const K* keys, int64_t n, int shift0, int end_bit, uint32_t* hist,
+                cudaStream_t s) {
     const int npasses = (end_bit - shift0 + 7) / 8;
     if (n <= 0 || npasses <= 0) return;
-    k_digit_hist<uint64_t><<<hist_grid(n), kThreads, 0, s>>>(keys, n, shift0, npasses, end_bit,
-                                                            hist);
+    for (int p0 = 0; p0 < npasses; p0 += kHistPasses) {
+        const int np = npasses - p0 < kHistPasses ? npasses - p0 : kHistPasses;
+        k_digit_hist<K><<<hist_grid(n), kThreads, 0, s>>>(keys, n, shift0 + 8 * p0, np, end_bit,
+                                                         hist + 256 * p0);
+    }
+}
+
+void launch_digit_hist_u64(const uint64_t* keys, int64_t n, int shift0, int end_bit,
+                           uint32_t* hist, cudaStream_t s) {
+    digit_hist<uint64_t>(keys, n, shift0, end_bit, hist, s);
 }
 
 void launch_digit_hist_u32(const uint32_t* keys, int64_t n, int shift0, int end_bit,
                            uint32_t* hist, cudaStream_t s) {
-    const int npasses = (end_bit - shift0 + 7) / 8;
-    if (n <= 0 || npasses <= 0) return;
-    k_digit_hist<uint32_t><<<hist_grid(n), kThreads, 0, s>>>(keys, n, shift0, npasses, end_bit,
-                                                            hist);
+    digit_hist<uint32_t>(keys, n, shift0, end_bit, hist, s);
 }
 
 void launch_onesweep_u64(const uint64_t* keys_in, const int32_t* vals_in, uint64_t* keys_out,
