@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 // k * 32 + ((l + 8 k) & 31): an owner's accesses for one slot hit 32
 // distinct banks, and the 4 pixels of one column (same lane, slots 0..3)
 // fall in 4 different banks when other lanes gather them.
-enum StateField { kTc = 0, kTa, kR0, kR1, kR2, kG0, kG1, kG2, kGA, kRA, kStateFields };
+enum StateField { kTc = 0, kTa, kR0, kR1, kR2, kG0, kG1, kG2, kGA, kStateFields };
 // Gradient fields in the reduction buffer.
 enum GradField { kC0 = 0, kC1, kC2, kOp, kMx, kMy, kQa, kQb, kQc, kAx, kAy };
 
@@ -404,10 +404,10 @@ __device__ __forceinline__ int sidx(int p) {  // p = k * 32 + lane
 template <int F>
 struct BwdWarpSmem {
     float state[kStateFields][kWarpPix];
-    int32_t last[kWarpPix];
     int16_t list[kWarpPix];       // packed valid pairs: k * 32 + owner lane
     float red[kRedEntries][F][kWarp + 1];
     int32_t red_gid[kRedEntries];
+    int32_t red_n[kRedEntries];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
 };
 
 template <int F>
@@ -417,9 +417,9 @@ __device__ __forceinline__ void flush_reduction(BwdWarpSmem<F>& w, int nslots, c
     for (int t = lane; t < nslots * F; t += kWarp) {
         const int e = t / F, f = t - (t / F) * F;
         const float* row = w.red[e][f];
+        const int n = w.red_n[e];
         float sum = 0.0f;
-#pragma unroll 8
-        for (int l = 0; l < kWarp; ++l) sum += row[l];
+        for (int l = 0; l < n; ++l) sum += row[l];
         if (sum == 0.0f) continue;
         const int64_t g = w.red_gid[e];
         float* dst;
@@ -494,8 +494,6 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         w.state[kG1][si] = g1;
         w.state[kG2][si] = g2;
         w.state[kGA][si] = ga;
-        w.state[kRA][si] = ra[k];
-        w.last[si] = last[k];
         sb0 += g0 * Tc;
         sb1 += g1 * Tc;
         sb2 += g2 * Tc;
@@ -578,12 +576,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
                 const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
                 const float Tc = w.state[kTc][si];
-                if (TRACE) {
-                    const bool valid = w.state[kRA][si] > 0.0f && e.s >= 0.0f &&
-                                       e.alpha >= a.alpha_cutoff && w.last[si] >= j &&
-                                       Tc < 1.0f && e.alpha < 1.0f;
-                    if (!valid) continue;
-                }
+                // the trace holds the forward's composite decisions (which imply
+                // render_alpha > 0, s >= 0, alpha >= cutoff and last_id >= j);
+                // the T < 1 guard depends on the walk and is tested here
+                if (TRACE && !(Tc < 1.0f && e.alpha < 1.0f)) continue;
                 const float Ta = w.state[kTa][si];
                 const float r0 = w.state[kR0][si], r1 = w.state[kR1][si], r2 = w.state[kR2][si];
                 const float g0 = w.state[kG0][si], g1 = w.state[kG1][si], g2 = w.state[kG2][si];
@@ -619,7 +615,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
             for (int f = 0; f < F; ++f) w.red[nslots][f][lane] = v[f];
-            if (lane == 0) w.red_gid[nslots] = st.gid[i];
+            if (lane == 0) {
+                w.red_gid[nslots] = st.gid[i];
+                w.red_n[nslots] = min(count, kWarp);
+            }
             if (++nslots == kRedEntries) {
                 flush_reduction<F>(w, nslots, gr, lane);
                 nslots = 0;
