@@ -154,8 +154,9 @@ int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
  *   (C,H,W,1), last_ids int32 (C,H,W); pair_counts int32 (C,H,W,3) or NULL:
  *   a work measure per pixel -- the list entries evaluated before the pixel
  *   stopped, the entries composited, and the entries evaluated up to and
- *   including the last composited one (entries whose splat cannot reach the
- *   cutoff anywhere in the tile are skipped unevaluated and not counted).
+ *   including the last composited one (entries whose splat provably cannot
+ *   reach the cutoff at the pixel -- anywhere in its 8-row half of the tile --
+ *   are skipped unevaluated and not counted).
  *   trace uint32 (n_isects, 8) or NULL, 16-byte aligned: per list entry, a
  *   256-bit mask of the tile's pixels that composited it (the forward's
  *   decisions, for gs_rasterize_bwd).  Words of entries past the point where

@@ -117,25 +117,28 @@ __device__ __forceinline__ TileRange tile_range(const RasterArgs& a) {
     return r;
 }
 
-// Pixel-centre rectangle of the tile (clipped to the image) for the
-// cannot-reach test.
+// Pixel-centre rectangle of one warp's pixels (the tile's columns, 8 of its
+// rows; clipped to the image) for the cannot-reach test.
 struct TileBox {
     float xlo, xhi, ylo, yhi, log_cut;
-    bool cull;
+    bool cull, empty;
 };
 
-__device__ __forceinline__ TileBox tile_box(const RasterArgs& a, const TileRange& tr) {
+__device__ __forceinline__ TileBox warp_box(const RasterArgs& a, const TileRange& tr, int warp) {
+    constexpr int kRows = kTile / kWarps;  // rows per warp
     TileBox b;
+    const int y0 = tr.ty * kTile + warp * kRows;
     b.xlo = (float)(tr.tx * kTile) + 0.5f;
     b.xhi = (float)min(tr.tx * kTile + kTile, a.width) - 0.5f;
-    b.ylo = (float)(tr.ty * kTile) + 0.5f;
-    b.yhi = (float)min(tr.ty * kTile + kTile, a.height) - 0.5f;
+    b.ylo = (float)y0 + 0.5f;
+    b.yhi = (float)min(y0 + kRows, a.height) - 0.5f;
+    b.empty = y0 >= a.height;  // the warp has no pixel inside the image
     b.cull = a.alpha_cutoff > 0.0f && isfinite(a.alpha_cutoff);
     b.log_cut = b.cull ? logf(a.alpha_cutoff) : 0.0f;
     return b;
 }
 
-// True when o exp(-s) < cutoff at every pixel centre of the tile, with room
+// True when o exp(-s) < cutoff at every pixel centre of the box, with room
 // to spare: s is at least its minimum over the (continuous) pixel-centre
 // rectangle, which for a positive-definite form is 0 inside and otherwise
 // the smallest of the four edge minima (a 1-D quadratic each).  The margin
@@ -144,6 +147,7 @@ __device__ __forceinline__ TileBox tile_box(const RasterArgs& a, const TileRange
 // dropped here fails the per-pixel alpha test at every pixel.
 __device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float my, float a,
                                              float b, float c, float op) {
+    if (t.empty) return true;          // no pixel to reach
     if (!t.cull) return false;
     if (op <= 0.0f) return true;       // raw <= 0 < cutoff everywhere
     if (!(op > 0.0f)) return false;    // NaN: leave it to the per-pixel path
@@ -189,17 +193,22 @@ struct StageSmem {
     int32_t gid[BATCH];
     int32_t j[BATCH];   // list position
     uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
-    int32_t cnt[kPerThread * kWarps];
+    uint8_t idx[kWarps][BATCH];  // per warp: staged slots that can reach its pixels
+    int32_t nw[kWarps];          // per warp: length of idx
+    int32_t cnt[1 + kWarps][kPerThread * kWarps];
 };
 
-// Stages the entries [lo, hi) of the tile's list that can reach the cutoff,
-// in processing order (ascending positions, or descending when REVERSE),
-// packed from slot 0; with TRACE_IN also their trace words.  Returns how
-// many were staged.  Contains two __syncthreads.  A flatten id outside
-// [0, C*N) (only from corrupted input) is dropped.
+// Stages the entries [lo, hi) of the tile's list that can reach the cutoff
+// at some pixel of the tile, in processing order (ascending positions, or
+// descending when REVERSE), packed from slot 0; with TRACE_IN also their
+// trace words.  For each warp, st.idx[w][0 .. st.nw[w]) lists (in the same
+// order) the staged slots whose splat can reach one of that warp's pixels.
+// Returns how many were staged.  Contains two __syncthreads.  A flatten id
+// outside [0, C*N) (only from corrupted input) is dropped.
 template <bool REVERSE, bool TRACE_IN, int BATCH>
-__device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox& box, int64_t lo,
-                                           int64_t hi, const uint32_t* __restrict__ trace,
+__device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&box)[kWarps],
+                                           int64_t lo, int64_t hi,
+                                           const uint32_t* __restrict__ trace,
                                            StageSmem<BATCH, TRACE_IN>& st) {
     constexpr int kPerThread = StageSmem<BATCH, TRACE_IN>::kPerThread;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -208,12 +217,13 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox& b
     float4 mo[kPerThread], q[kPerThread];
     int32_t gid[kPerThread];
     int64_t jj[kPerThread];
-    unsigned ball[kPerThread];
-    bool keep[kPerThread];
+    unsigned ball[kPerThread][1 + kWarps];
 #pragma unroll
     for (int r = 0; r < kPerThread; ++r) {
         const int i = r * kThreads + tid;
-        keep[r] = false;
+        bool reach[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) reach[w] = false;
         if (i < n) {
             jj[r] = REVERSE ? hi - 1 - i : lo + i;
             const int64_t g = a.flatten_ids[jj[r]];
@@ -223,23 +233,40 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox& b
                 mo[r] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
                 q[r] = make_float4(qq[0], qq[1], qq[2], 0.0f);
                 gid[r] = (int32_t)g;
-                keep[r] = !cannot_reach(box, m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w)
+                    reach[w] = !cannot_reach(box[w], m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
             }
         }
-        ball[r] = __ballot_sync(0xffffffffu, keep[r]);
-        if (lane == 0) st.cnt[r * kWarps + warp] = __popc(ball[r]);
+        bool keep = false;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) keep |= reach[w];
+        ball[r][0] = __ballot_sync(0xffffffffu, keep);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) ball[r][1 + w] = __ballot_sync(0xffffffffu, reach[w]);
+        if (lane == 0)
+#pragma unroll
+            for (int l = 0; l <= kWarps; ++l) st.cnt[l][r * kWarps + warp] = __popc(ball[r][l]);
     }
     __syncthreads();
-    int total = 0;
+    int total[1 + kWarps];
 #pragma unroll
-    for (int k = 0; k < kPerThread * kWarps; ++k) total += st.cnt[k];
+    for (int l = 0; l <= kWarps; ++l) {
+        total[l] = 0;
+#pragma unroll
+        for (int k = 0; k < kPerThread * kWarps; ++k) total[l] += st.cnt[l][k];
+    }
     const unsigned lt = lanemask_lt();
 #pragma unroll
     for (int r = 0; r < kPerThread; ++r) {
-        int base = 0;
-        for (int k = 0; k < r * kWarps + warp; ++k) base += st.cnt[k];
-        if (keep[r]) {
-            const int pos = base + __popc(ball[r] & lt);
+        int base[1 + kWarps];
+#pragma unroll
+        for (int l = 0; l <= kWarps; ++l) {
+            base[l] = 0;
+            for (int k = 0; k < r * kWarps + warp; ++k) base[l] += st.cnt[l][k];
+        }
+        if ((ball[r][0] >> lane) & 1u) {
+            const int pos = base[0] + __popc(ball[r][0] & lt);
             const float* cc = a.colors + 3 * (int64_t)gid[r];
             st.mo[pos] = mo[r];
             st.q[pos] = q[r];
@@ -251,10 +278,17 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox& b
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = t[w];
             }
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                if ((ball[r][1 + w] >> lane) & 1u)
+                    st.idx[w][base[1 + w] + __popc(ball[r][1 + w] & lt)] = (uint8_t)pos;
         }
     }
+    if (tid == 0)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) st.nw[w] = total[1 + w];
     __syncthreads();
-    return total;
+    return total[0];
 }
 
 struct PixelSlot {
@@ -280,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     __shared__ StageSmem<kBatch, false> st;
     __shared__ uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
     const TileRange tr = tile_range(a);
-    const TileBox box = tile_box(a, tr);
+    TileBox box[kWarps];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) box[w] = warp_box(a, tr, w);
     const PixelSlot ps = pixel_slot(tr);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float px = (float)ps.x + 0.5f;
@@ -304,9 +340,11 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
         const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
         if (TRACE)
             for (int i = tid; i < kBatch * kTraceWords; i += kThreads) (&s_trace[0][0])[i] = 0u;
-        const int nb = stage_batch<false, false, kBatch>(a, box, b0, b0 + n_raw, nullptr, st);
+        stage_batch<false, false, kBatch>(a, box, b0, b0 + n_raw, nullptr, st);
         if (!__all_sync(0xffffffffu, all_done)) {
-            for (int i = 0; i < nb; ++i) {
+            const int nw = st.nw[warp];
+            for (int ii = 0; ii < nw; ++ii) {
+                const int i = st.idx[warp][ii];
                 const float4 mo = st.mo[i];
                 const float4 q = st.q[i];
                 const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
@@ -347,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                     }
                 }
                 // leave the batch early once every pixel of the warp has stopped
-                if ((i & 15) == 15) {
+                if ((ii & 15) == 15) {
                     bool d = true;
 #pragma unroll
                     for (int k = 0; k < kPPT; ++k) d &= done[k];
@@ -451,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     __shared__ float s_bg[kWarps][3];
     __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
-    const TileBox box = tile_box(a, tr);
+    TileBox box[kWarps];
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) box[k] = warp_box(a, tr, k);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     BwdWarpSmem<F>& w = ws[warp];
     const PixelSlot ps = pixel_slot(tr);
@@ -530,8 +570,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     int nslots = 0;
     for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
         const int64_t b0 = max(tr.start, b1 - kBatch);
-        const int nb = stage_batch<true, TRACE, kBatch>(a, box, b0, b1, trace, st);
-        for (int i = 0; i < nb; ++i) {
+        stage_batch<true, TRACE, kBatch>(a, box, b0, b1, trace, st);
+        const int nw = st.nw[warp];
+        for (int ii = 0; ii < nw; ++ii) {
+            const int i = st.idx[warp][ii];
             const int32_t j = st.j[i];
             if (j > warp_max) continue;  // warp-uniform
             const float4 mo = st.mo[i];
