@@ -31,12 +31,12 @@ def _setup(s):
     return iso
 
 
-def _fwd(s, iso, masks=None, ids=None, tie_rel=0.0, cut=None, thr=None):
+def _fwd(s, iso, masks=None, ids=None, tie_rel=0.0, cut=None, thr=None, tie_rel_T=None):
     return oracle.rasterize_fwd(
         s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, masks, s.width, s.height,
         s.tile_size, iso["offsets"], iso["ids"] if ids is None else ids,
         s.alpha_cutoff if cut is None else cut,
-        s.transmittance_threshold if thr is None else thr, tie_rel=tie_rel)
+        s.transmittance_threshold if thr is None else thr, tie_rel=tie_rel, tie_rel_T=tie_rel_T)
 
 
 def _scene(means, conics, colors, opac, depths, radii, W, H, bg=None):
@@ -385,3 +385,21 @@ def test_backward_masked_tiles_only_background():
     for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities"):
         assert (got[k] == 0).all()
     np.testing.assert_allclose(got["grad_backgrounds"], [[1024.0] * 3])
+
+
+@pytest.mark.parametrize("seed", [0, 5])
+def test_double_twin_matches_float_forward(seed):
+    # the double-precision forward (used for finite differences) is the same
+    # recurrence: away from decisions it agrees with the float forward to
+    # float rounding, which pins it to everything the float forward is pinned to
+    s = scenes.random_small(seed, C=2, N=20, W=48, H=32)
+    iso = _setup(s)
+    f32 = _fwd(s, iso, tie_rel=1e-3, tie_rel_T=1e-2)
+    rgb, alpha, _ = oracle.rasterize_fwd_f64(
+        s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, s.width, s.height,
+        s.tile_size, iso["offsets"], iso["ids"], float(s.alpha_cutoff),
+        float(s.transmittance_threshold))
+    ok = f32["near_tie"] == 0
+    assert ok.mean() > 0.9
+    np.testing.assert_allclose(f32["render_colors"][ok], rgb[ok], atol=2e-6, rtol=0)
+    np.testing.assert_allclose(f32["render_alphas"][..., 0][ok], alpha[ok], atol=2e-6, rtol=0)
