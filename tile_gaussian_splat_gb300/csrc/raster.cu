@@ -202,7 +202,8 @@ struct StageSmem {
 // at some pixel of the tile, in processing order (ascending positions, or
 // descending when REVERSE), packed from slot 0; with TRACE_IN also their
 // trace words.  For each warp, st.idx[w][0 .. st.nw[w]) lists (in the same
-// order) the staged slots whose splat can reach one of that warp's pixels.
+// order) the staged slots whose splat can reach one of that warp's pixels --
+// with TRACE_IN, exactly those some pixel of the warp composited.
 // Returns how many were staged.  Contains two __syncthreads.  A flatten id
 // outside [0, C*N) (only from corrupted input) is dropped.
 template <bool REVERSE, bool TRACE_IN, int BATCH>
@@ -217,6 +218,7 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
     float4 mo[kPerThread], q[kPerThread];
     int32_t gid[kPerThread];
     int64_t jj[kPerThread];
+    uint4 tw[TRACE_IN ? kPerThread : 1][kWarps];
     unsigned ball[kPerThread][1 + kWarps];
 #pragma unroll
     for (int r = 0; r < kPerThread; ++r) {
@@ -233,9 +235,20 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
                 mo[r] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
                 q[r] = make_float4(qq[0], qq[1], qq[2], 0.0f);
                 gid[r] = (int32_t)g;
+                if (TRACE_IN) {
+                    // the forward's masks say exactly which warps composited it
+                    const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w)
-                    reach[w] = !cannot_reach(box[w], m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
+                    for (int w = 0; w < kWarps; ++w) {
+                        tw[r][w] = t[w];
+                        reach[w] = (tw[r][w].x | tw[r][w].y | tw[r][w].z | tw[r][w].w) != 0u;
+                    }
+                } else {
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w)
+                        reach[w] =
+                            !cannot_reach(box[w], m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
+                }
             }
         }
         bool keep = false;
@@ -274,9 +287,8 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
             st.gid[pos] = gid[r];
             st.j[pos] = (int32_t)jj[r];
             if (TRACE_IN) {
-                const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = t[w];
+                for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = tw[r][w];
             }
 #pragma unroll
             for (int w = 0; w < kWarps; ++w)
@@ -442,7 +454,7 @@ __device__ __forceinline__ int sidx(int p) {  // p = k * 32 + lane
 template <int F>
 struct BwdWarpSmem {
     float state[kStateFields][kWarpPix];
-    int16_t list[kWarpPix];       // packed valid pairs: k * 32 + owner lane
+    int16_t list[2][kWarpPix];    // packed valid pairs: k * 32 + owner lane (double buffer)
     float red[kRedEntries][F][kWarp + 1];
     int32_t red_gid[kRedEntries];
     int32_t red_n[kRedEntries];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
@@ -568,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     const int x_tile = tr.tx * kTile;
     const int y_tile = tr.ty * kTile;
     int nslots = 0;
+    int lb = 0;  // list buffer of the current entry
     for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
         const int64_t b0 = max(tr.start, b1 - kBatch);
         stage_batch<true, TRACE, kBatch>(a, box, b0, b1, trace, st);
@@ -586,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
 #pragma unroll
                 for (int k = 0; k < kPPT; ++k) {
                     if ((m[k] >> lane) & 1u)
-                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                        w.list[lb][count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
                     count += __popc(m[k]);
                 }
             } else {
@@ -594,11 +607,12 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
 #pragma unroll
                 for (int k = 0; k < kPPT; ++k) {
                     const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                    bool valid = ra[k] > 0.0f && e.s >= 0.0f && e.alpha >= a.alpha_cutoff &&
-                                 last[k] >= j && e.alpha < 1.0f;
-                    if (valid) valid = w.state[kTc][sidx(k * kWarp + lane)] < 1.0f;
+                    // T < 1 depends on pairs still being run; the lane that
+                    // runs this pair tests it
+                    const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
+                                       e.alpha >= a.alpha_cutoff && last[k] >= j;
                     const unsigned m = __ballot_sync(0xffffffffu, valid);
-                    if (valid) w.list[count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
+                    if (valid) w.list[lb][count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
                     count += __popc(m);
                 }
             }
@@ -610,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             for (int f = 0; f < F; ++f) v[f] = 0.0f;
             const float4 col = st.col[i];
             for (int L = lane; L < count; L += kWarp) {
-                const int p = w.list[L];
+                const int p = w.list[lb][L];
                 const int si = sidx(p);
                 const int ol = p & 31;
                 const int row = ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
@@ -618,10 +632,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
                 const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
                 const float Tc = w.state[kTc][si];
-                // the trace holds the forward's composite decisions (which imply
-                // render_alpha > 0, s >= 0, alpha >= cutoff and last_id >= j);
-                // the T < 1 guard depends on the walk and is tested here
-                if (TRACE && !(Tc < 1.0f && e.alpha < 1.0f)) continue;
+                // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
+                // cutoff and last_id >= j (from the trace, or tested while
+                // packing); the T < 1 guard depends on the walk and is tested here
+                if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
                 const float Ta = w.state[kTa][si];
                 const float r0 = w.state[kR0][si], r1 = w.state[kR1][si], r2 = w.state[kR2][si];
                 const float g0 = w.state[kG0][si], g1 = w.state[kG1][si], g2 = w.state[kG2][si];
@@ -661,11 +675,12 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 w.red_gid[nslots] = st.gid[i];
                 w.red_n[nslots] = min(count, kWarp);
             }
+            // the next entry packs into the other list buffer; the warp sync
+            // after that packing orders this entry's reads before its reuse
+            lb ^= 1;
             if (++nslots == kRedEntries) {
                 flush_reduction<F>(w, nslots, gr, lane);
                 nslots = 0;
-            } else {
-                __syncwarp();
             }
         }
     }
