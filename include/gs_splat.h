@@ -131,6 +131,9 @@ int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
                     int tile_width, int tile_height, int32_t* offsets,
                     int32_t* d_status, void* stream);
 
+/* Largest channel count the rasterizer accepts. */
+#define GS_MAX_CHANNELS 1024
+
 /*
  * gs_rasterize_fwd -- front-to-back compositing (the recurrence whose
  * reverse walk is gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel;
@@ -163,7 +166,9 @@ int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
  *   every pixel of the tile had stopped are not written.  Bit layout: word
  *   w (0..7), bit l covers tile pixel column (32 (w / 4) + l) % 16, row
  *   4 ((32 (w / 4) + l) / 16) + w % 4.
- * Supported: channels == 3, tile_size == 16; TH = ceil(H/16), TW = ceil(W/16).
+ * Supported: 1 <= channels <= GS_MAX_CHANNELS, tile_size == 16;
+ *   TH = ceil(H/16), TW = ceil(W/16).  Channels are composited in chunks of
+ *   up to 4 per kernel launch (the walk is repeated per chunk).
  */
 int gs_rasterize_fwd(const float* means2d, const float* conics,
                      const float* colors, const float* opacities,
@@ -207,7 +212,12 @@ int gs_rasterize_fwd(const float* means2d, const float* conics,
  *   grad_means2d (C,N,2), grad_conics (C,N,3), grad_colors (C,N,channels),
  *   grad_opacities (C,N); grad_backgrounds (C,channels) or NULL;
  *   grad_means2d_abs (C,N,2) or NULL.
- * Supported: channels == 3, tile_size == 16.
+ * Supported: 1 <= channels <= GS_MAX_CHANNELS, tile_size == 16;
+ *   grad_means2d_abs only with channels <= 4 (else GS_ERR_INVALID_ARG: the
+ *   absolute value of a sum over all channels cannot be formed from
+ *   per-chunk parts).  More than 4 channels run as chunks of up to 4, whose
+ *   contributions add up: every term above is linear in the per-channel
+ *   products.
  */
 int gs_rasterize_bwd(const float* means2d, const float* conics,
                      const float* colors, const float* opacities,

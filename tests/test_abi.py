@@ -66,9 +66,11 @@ def test_argument_errors_without_gpu(lib):
     assert lib.gs_isect_tiles(P(8), P(8), 0, P(8), 1, 10, 16, 4, 4, 1, None, ct.byref(total),
                               None, None, 0, None, 0, None, None) == 4
     assert lib.gs_tile_offsets(None, 5, 1, 4, 4, P(8), None, None) == 1
-    assert lib.gs_rasterize_fwd(P(8), P(8), P(8), P(8), None, None, 1, 10, 4, 64, 64, 16, P(8),
-                                P(8), 10, ct.c_float(0.1), ct.c_float(0.1), P(8), P(8), P(8),
-                                None, None, None, None) == 1
+    # channel counts outside 1..GS_MAX_CHANNELS (1024) and tile sizes other than 16
+    for ch, ts in ((0, 16), (1025, 16), (3, 8)):
+        assert lib.gs_rasterize_fwd(P(8), P(8), P(8), P(8), None, None, 1, 10, ch, 64, 64, ts,
+                                    P(8), P(8), 10, ct.c_float(0.1), ct.c_float(0.1), P(8), P(8),
+                                    P(8), None, None, None, None) == 1
     assert lib.gs_sort_pairs(None, None, 5, 0, 64, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 65, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 64, None, 0, None, None) == 4

@@ -76,7 +76,7 @@ def _bwd_case(s, masks=None, absgrad=True, seed=1, nudges=1):
     their opacity scaled by 1 % (`nudges` rounds, a deterministic change of
     the seeded input that moves them off the decision); splats in the walked
     part of any pixel that still has such a pair are left out."""
-    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, seed=seed)
+    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, channels=s.channels, seed=seed)
     for it in range(nudges + 1):
         iso, ref = _oracle_forward(s, masks=masks)
         rb = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds,
@@ -117,7 +117,8 @@ def _compare_grads(rb, got, excluded, rtol=1e-3, atol=1e-6):
     4e-6 of that sum instead.  Returns (checked, cancellation-bound) counts."""
     stats = [0, 0]
     for name, mag, w in [("grad_means2d", "mag_means2d", 2), ("grad_conics", "mag_conics", 3),
-                         ("grad_colors", "mag_colors", 3), ("grad_opacities", "mag_opacities", 1)]:
+                         ("grad_colors", "mag_colors", rb["grad_colors"].shape[-1]),
+                         ("grad_opacities", "mag_opacities", 1)]:
         g = got[name].cpu().numpy().astype(np.float64)
         r = rb[name].astype(np.float64)
         m = rb[mag]

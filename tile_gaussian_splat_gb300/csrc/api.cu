@@ -141,7 +141,7 @@ int raster_args_ok(const float* means2d, const float* conics, const float* color
                    int tile_size, const int32_t* offsets, const int32_t* flatten_ids,
                    int64_t n_isects) {
     if (C < 1 || N < 0 || width < 1 || height < 1) return 0;
-    if (channels != 3 || tile_size != 16) return 0;
+    if (channels < 1 || channels > GS_MAX_CHANNELS || tile_size != 16) return 0;
     if ((int64_t)C * N >= ((int64_t)1 << 31) || n_isects < 0 || n_isects >= ((int64_t)1 << 31))
         return 0;
     if (!offsets) return 0;
@@ -302,7 +302,8 @@ int gs_rasterize_fwd(const float* means2d, const float* conics, const float* col
     if (!render_colors || !render_alphas || !last_ids) return GS_ERR_INVALID_ARG;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
-                 offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold};
+                 offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold,
+                 channels, 0, 1};
     if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts, trace,
                       static_cast<cudaStream_t>(stream));
@@ -328,22 +329,24 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
     if (CN > 0 && (!grad_means2d || !grad_conics || !grad_colors || !grad_opacities))
         return GS_ERR_INVALID_ARG;
     if (grad_backgrounds && !backgrounds) return GS_ERR_INVALID_ARG;
+    // |.| of a sum over channels is not the sum over channel chunks of |.|
+    if (grad_means2d_abs && channels > 4) return GS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t f = sizeof(float);
     if (CN > 0) {
         if (cudaMemsetAsync(grad_means2d, 0, CN * 2 * f, s) != cudaSuccess ||
             cudaMemsetAsync(grad_conics, 0, CN * 3 * f, s) != cudaSuccess ||
-            cudaMemsetAsync(grad_colors, 0, CN * 3 * f, s) != cudaSuccess ||
+            cudaMemsetAsync(grad_colors, 0, CN * channels * f, s) != cudaSuccess ||
             cudaMemsetAsync(grad_opacities, 0, CN * f, s) != cudaSuccess)
             return GS_ERR_CUDA;
         if (grad_means2d_abs && cudaMemsetAsync(grad_means2d_abs, 0, CN * 2 * f, s) != cudaSuccess)
             return GS_ERR_CUDA;
     }
-    if (grad_backgrounds && cudaMemsetAsync(grad_backgrounds, 0, (size_t)C * 3 * f, s) != cudaSuccess)
+    if (grad_backgrounds && cudaMemsetAsync(grad_backgrounds, 0, (size_t)C * channels * f, s) != cudaSuccess)
         return GS_ERR_CUDA;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
-                 offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f};
+                 offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f, channels, 0, 1};
     RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                   grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                   grad_means2d_abs};

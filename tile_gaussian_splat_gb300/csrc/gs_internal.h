@@ -79,10 +79,17 @@ struct RasterArgs {
     const int32_t* flatten_ids;
     int64_t n_isects;
     float alpha_cutoff, transmittance_threshold;
+    // channel chunk of this launch: colours, backgrounds, render_colors and
+    // their gradients have `channels` per splat / pixel; the launch handles
+    // channels [ch_off, ch_off + chunk width)
+    int channels, ch_off;
+    int first_chunk;  // forward: writes alphas, last ids, counts, trace;
+                      // backward: adds the render_alpha gradient's terms
 };
 
 // trace (may be null): per list entry 8 words, the tile pixels that composited it.
-void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_alphas,
+// Runs one launch per chunk of up to 4 channels.
+void launch_raster_fwd(RasterArgs a, float* render_colors, float* render_alphas,
                        int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
                        cudaStream_t s);
 
@@ -99,7 +106,7 @@ struct RasterGrads {
     float* grad_means2d_abs;
 };
 
-void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
+void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace,
                        cudaStream_t s);
 
 }  // namespace gs

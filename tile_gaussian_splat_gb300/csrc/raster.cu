@@ -189,7 +189,7 @@ struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
     float4 mo[BATCH];   // mx, my, opacity, -
     float4 q[BATCH];    // a, b, c, -
-    float4 col[BATCH];  // r, g, b, -
+    float4 col[BATCH];  // up to 4 channels of the launch's chunk
     int32_t gid[BATCH];
     int32_t j[BATCH];   // list position
     uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
@@ -206,7 +206,7 @@ struct StageSmem {
 // with TRACE_IN, exactly those some pixel of the warp composited.
 // Returns how many were staged.  Contains two __syncthreads.  A flatten id
 // outside [0, C*N) (only from corrupted input) is dropped.
-template <bool REVERSE, bool TRACE_IN, int BATCH>
+template <bool REVERSE, bool TRACE_IN, int BATCH, int CH>
 __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&box)[kWarps],
                                            int64_t lo, int64_t hi,
                                            const uint32_t* __restrict__ trace,
@@ -280,10 +280,11 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
         }
         if ((ball[r][0] >> lane) & 1u) {
             const int pos = base[0] + __popc(ball[r][0] & lt);
-            const float* cc = a.colors + 3 * (int64_t)gid[r];
+            const float* cc = a.colors + (int64_t)gid[r] * a.channels + a.ch_off;
             st.mo[pos] = mo[r];
             st.q[pos] = q[r];
-            st.col[pos] = make_float4(cc[0], cc[1], cc[2], 0.0f);
+            st.col[pos] = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
+                                      CH > 3 ? cc[3] : 0.0f);
             st.gid[pos] = gid[r];
             st.j[pos] = (int32_t)jj[r];
             if (TRACE_IN) {
@@ -317,7 +318,7 @@ __device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
 // ------------------------------------------------------------------ forward
 
 // At most 85 registers, so 12 blocks (24 warps) fit on an SM.
-template <bool COUNT, bool TRACE>
+template <int CH, bool COUNT, bool TRACE>
 __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
                  int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts,
@@ -332,13 +333,13 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     const PixelSlot ps = pixel_slot(tr);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float px = (float)ps.x + 0.5f;
-    float T[kPPT], cr[kPPT], cg[kPPT], cb[kPPT], py[kPPT];
+    float T[kPPT], acc[kPPT][4], py[kPPT];
     int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT], n_last[kPPT];
     bool done[kPPT];
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         T[k] = 1.0f;
-        cr[k] = cg[k] = cb[k] = 0.0f;
+        acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.0f;
         last[k] = -1;
         n_eval[k] = n_comp[k] = n_last[k] = 0;
         done[k] = !(ps.x < a.width && ps.y0 + k < a.height);
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
         const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
         if (TRACE)
             for (int i = tid; i < kBatch * kTraceWords; i += kThreads) (&s_trace[0][0])[i] = 0u;
-        stage_batch<false, false, kBatch>(a, box, b0, b0 + n_raw, nullptr, st);
+        stage_batch<false, false, kBatch, CH>(a, box, b0, b0 + n_raw, nullptr, st);
         if (!__all_sync(0xffffffffu, all_done)) {
             const int nw = st.nw[warp];
             for (int ii = 0; ii < nw; ++ii) {
@@ -378,9 +379,10 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                     const float4 col = st.col[i];
                     const PairEval e{0.0f, 0.0f, 0.0f, 0.0f, alpha[k]};
                     const float w = T[k] * e.alpha;
-                    cr[k] += w * col.x;
-                    cg[k] += w * col.y;
-                    cb[k] += w * col.z;
+                    acc[k][0] += w * col.x;
+                    if (CH > 1) acc[k][1] += w * col.y;
+                    if (CH > 2) acc[k][2] += w * col.z;
+                    if (CH > 3) acc[k][3] += w * col.w;
                     T[k] = T[k] * (1.0f - e.alpha);
                     last[k] = j;
                     if (COUNT) {
@@ -412,20 +414,20 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
             for (int i = tid; i < n_raw * (kTraceWords / 4); i += kThreads) dst[i] = src[i];
         }
     }
-    float br = 0.0f, bgc = 0.0f, bb = 0.0f;
-    if (a.backgrounds) {
-        br = a.backgrounds[3 * tr.c];
-        bgc = a.backgrounds[3 * tr.c + 1];
-        bb = a.backgrounds[3 * tr.c + 2];
-    }
+    float bg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (a.backgrounds)
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+            bg[c] = a.backgrounds[(int64_t)tr.c * a.channels + a.ch_off + c];
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         const int y = ps.y0 + k;
         if (ps.x < a.width && y < a.height) {
             const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
-            out_rgb[3 * p] = cr[k] + T[k] * br;
-            out_rgb[3 * p + 1] = cg[k] + T[k] * bgc;
-            out_rgb[3 * p + 2] = cb[k] + T[k] * bb;
+            float* o = out_rgb + p * a.channels + a.ch_off;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) o[c] = acc[k][c] + T[k] * bg[c];
+            if (!a.first_chunk) continue;
             out_alpha[p] = 1.0f - T[k];
             out_last[p] = last[k];
             if (COUNT) {
@@ -443,26 +445,38 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 // k * 32 + ((l + 8 k) & 31): an owner's accesses for one slot hit 32
 // distinct banks, and the 4 pixels of one column (same lane, slots 0..3)
 // fall in 4 different banks when other lanes gather them.
-enum StateField { kTc = 0, kTa, kR0, kR1, kR2, kG0, kG1, kG2, kGA, kStateFields };
-// Gradient fields in the reduction buffer.
-enum GradField { kC0 = 0, kC1, kC2, kOp, kMx, kMy, kQa, kQb, kQc, kAx, kAy };
+// Fields: T, T_after, rem[CH], upstream colour gradient[CH], upstream alpha
+// gradient.
+template <int CH>
+struct StateLayout {
+    static constexpr int kTc = 0, kTa = 1, kR = 2, kG = 2 + CH, kGA = 2 + 2 * CH;
+    static constexpr int kFields = 3 + 2 * CH;
+};
+// Gradient fields in the reduction buffer: colours[CH], then these.
+template <int CH>
+struct GradLayout {
+    static constexpr int kOp = CH, kMx = CH + 1, kMy = CH + 2, kQa = CH + 3, kQb = CH + 4,
+                         kQc = CH + 5, kAx = CH + 6, kAy = CH + 7;
+};
 
 __device__ __forceinline__ int sidx(int p) {  // p = k * 32 + lane
     return (p & ~31) | ((p + ((p >> 5) << 3)) & 31);
 }
 
-template <int F>
+template <int CH, int F>
 struct BwdWarpSmem {
-    float state[kStateFields][kWarpPix];
+    float state[StateLayout<CH>::kFields][kWarpPix];
     int16_t list[2][kWarpPix];    // packed valid pairs: k * 32 + owner lane (double buffer)
     float red[kRedEntries][F][kWarp + 1];
     int32_t red_gid[kRedEntries];
     int32_t red_n[kRedEntries];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
 };
 
-template <int F>
-__device__ __forceinline__ void flush_reduction(BwdWarpSmem<F>& w, int nslots, const RasterGrads& gr,
+template <int CH, int F>
+__device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslots,
+                                                const RasterArgs& a, const RasterGrads& gr,
                                                 int lane) {
+    using G = GradLayout<CH>;
     __syncwarp();
     for (int t = lane; t < nslots * F; t += kWarp) {
         const int e = t / F, f = t - (t / F) * F;
@@ -473,13 +487,11 @@ __device__ __forceinline__ void flush_reduction(BwdWarpSmem<F>& w, int nslots, c
         if (sum == 0.0f) continue;
         const int64_t g = w.red_gid[e];
         float* dst;
-        switch (f) {
-            case kC0: case kC1: case kC2: dst = gr.grad_colors + 3 * g + (f - kC0); break;
-            case kOp: dst = gr.grad_opacities + g; break;
-            case kMx: case kMy: dst = gr.grad_means2d + 2 * g + (f - kMx); break;
-            case kQa: case kQb: case kQc: dst = gr.grad_conics + 3 * g + (f - kQa); break;
-            default: dst = gr.grad_means2d_abs + 2 * g + (f - kAx); break;
-        }
+        if (f < CH) dst = gr.grad_colors + g * a.channels + a.ch_off + f;
+        else if (f == G::kOp) dst = gr.grad_opacities + g;
+        else if (f <= G::kMy) dst = gr.grad_means2d + 2 * g + (f - G::kMx);
+        else if (f <= G::kQc) dst = gr.grad_conics + 3 * g + (f - G::kQa);
+        else dst = gr.grad_means2d_abs + 2 * g + (f - G::kAx);
         atomicAdd(dst, sum);
     }
     __syncwarp();
@@ -491,34 +503,36 @@ __device__ __forceinline__ void flush_reduction(BwdWarpSmem<F>& w, int nslots, c
 // state in shared memory.  Each packed pair is re-evaluated with the
 // forward's arithmetic and re-tested in full before its gradient is taken,
 // so both paths give the same result.
-template <bool ABS, bool TRACE>
+template <int CH, bool ABS, bool TRACE>
 __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     k_raster_bwd(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
-    constexpr int F = ABS ? 11 : 9;
+    using S = StateLayout<CH>;
+    using G = GradLayout<CH>;
+    constexpr int F = CH + (ABS ? 8 : 6);
     constexpr int kBatch = kBatchBwd;
     __shared__ StageSmem<kBatch, TRACE> st;
-    __shared__ BwdWarpSmem<F> ws[kWarps];
-    __shared__ float s_bg[kWarps][3];
+    __shared__ BwdWarpSmem<CH, F> ws[kWarps];
+    __shared__ float s_bg[kWarps][4];
     __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
     TileBox box[kWarps];
 #pragma unroll
     for (int k = 0; k < kWarps; ++k) box[k] = warp_box(a, tr, k);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    BwdWarpSmem<F>& w = ws[warp];
+    BwdWarpSmem<CH, F>& w = ws[warp];
     const PixelSlot ps = pixel_slot(tr);
     const float px = (float)ps.x + 0.5f;
 
     float ra[kPPT], py[kPPT];
     int32_t last[kPPT];
-    float bg0 = 0.0f, bg1 = 0.0f, bg2 = 0.0f;
-    if (a.backgrounds) {
-        bg0 = a.backgrounds[3 * tr.c];
-        bg1 = a.backgrounds[3 * tr.c + 1];
-        bg2 = a.backgrounds[3 * tr.c + 2];
-    }
+    float bgv[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+        bgv[c] = a.backgrounds ? a.backgrounds[(int64_t)tr.c * a.channels + a.ch_off + c] : 0.0f;
     int my_max = -1;
-    float sb0 = 0.0f, sb1 = 0.0f, sb2 = 0.0f;
+    float sb[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) sb[c] = 0.0f;
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         const int y = ps.y0 + k;
@@ -526,50 +540,44 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         py[k] = (float)y + 0.5f;
         ra[k] = 0.0f;
         last[k] = -1;
-        float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, ga = 0.0f;
+        float gc[CH], ga = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) gc[c] = 0.0f;
         if (ps.x < a.width && y < a.height) {
             const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
             ra[k] = gr.render_alphas[p];
             last[k] = gr.last_ids[p];
-            g0 = gr.grad_render_colors[3 * p];
-            g1 = gr.grad_render_colors[3 * p + 1];
-            g2 = gr.grad_render_colors[3 * p + 2];
-            ga = gr.grad_render_alphas[p];
+#pragma unroll
+            for (int c = 0; c < CH; ++c) gc[c] = gr.grad_render_colors[p * a.channels + a.ch_off + c];
+            // the render_alpha gradient's terms are added by the first chunk only
+            ga = a.first_chunk ? gr.grad_render_alphas[p] : 0.0f;
         }
         const float Tc = 1.0f - ra[k];
-        w.state[kTc][si] = Tc;
-        w.state[kTa][si] = 1.0f;
-        w.state[kR0][si] = bg0;
-        w.state[kR1][si] = bg1;
-        w.state[kR2][si] = bg2;
-        w.state[kG0][si] = g0;
-        w.state[kG1][si] = g1;
-        w.state[kG2][si] = g2;
-        w.state[kGA][si] = ga;
-        sb0 += g0 * Tc;
-        sb1 += g1 * Tc;
-        sb2 += g2 * Tc;
+        w.state[S::kTc][si] = Tc;
+        w.state[S::kTa][si] = 1.0f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            w.state[S::kR + c][si] = bgv[c];
+            w.state[S::kG + c][si] = gc[c];
+            sb[c] += gc[c] * Tc;
+        }
+        w.state[S::kGA][si] = ga;
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
     if (tid == 0) s_jmax = -1;
     if (gr.grad_backgrounds) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sb0 += __shfl_xor_sync(0xffffffffu, sb0, o);
-            sb1 += __shfl_xor_sync(0xffffffffu, sb1, o);
-            sb2 += __shfl_xor_sync(0xffffffffu, sb2, o);
-        }
-        if (lane == 0) {
-            s_bg[warp][0] = sb0;
-            s_bg[warp][1] = sb1;
-            s_bg[warp][2] = sb2;
+        for (int c = 0; c < CH; ++c) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sb[c] += __shfl_xor_sync(0xffffffffu, sb[c], o);
+            if (lane == 0) s_bg[warp][c] = sb[c];
         }
     }
     __syncthreads();
-    if (gr.grad_backgrounds && tid < 3) {
+    if (gr.grad_backgrounds && tid < CH) {
         float v = 0.0f;
         for (int k = 0; k < kWarps; ++k) v += s_bg[k][tid];
-        atomicAdd(&gr.grad_backgrounds[3 * tr.c + tid], v);
+        atomicAdd(&gr.grad_backgrounds[(int64_t)tr.c * a.channels + a.ch_off + tid], v);
     }
     if (tr.masked || tr.start == tr.end) return;
     const int warp_max = __reduce_max_sync(0xffffffffu, my_max);
@@ -583,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     int lb = 0;  // list buffer of the current entry
     for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
         const int64_t b0 = max(tr.start, b1 - kBatch);
-        stage_batch<true, TRACE, kBatch>(a, box, b0, b1, trace, st);
+        stage_batch<true, TRACE, kBatch, CH>(a, box, b0, b1, trace, st);
         const int nw = st.nw[warp];
         for (int ii = 0; ii < nw; ++ii) {
             const int i = st.idx[warp][ii];
@@ -631,42 +639,43 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 const ColumnTerms ct =
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
                 const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
-                const float Tc = w.state[kTc][si];
+                const float Tc = w.state[S::kTc][si];
                 // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
                 // cutoff and last_id >= j (from the trace, or tested while
                 // packing); the T < 1 guard depends on the walk and is tested here
                 if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
-                const float Ta = w.state[kTa][si];
-                const float r0 = w.state[kR0][si], r1 = w.state[kR1][si], r2 = w.state[kR2][si];
-                const float g0 = w.state[kG0][si], g1 = w.state[kG1][si], g2 = w.state[kG2][si];
-                const float ga = w.state[kGA][si];
+                const float Ta = w.state[S::kTa][si];
+                const float ga = w.state[S::kGA][si];
+                const float colv[4] = {col.x, col.y, col.z, col.w};
                 const float one_m = 1.0f - e.alpha;
                 const float Tb = __fdividef(Tc, one_m);
                 const float vis = Tb * e.alpha;
-                v[kC0] += g0 * vis;
-                v[kC1] += g1 * vis;
-                v[kC2] += g2 * vis;
-                const float dot = g0 * (col.x - r0) + g1 * (col.y - r1) + g2 * (col.z - r2);
+                float dot = 0.0f;
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    const float gcc = w.state[S::kG + c][si];
+                    const float rc = w.state[S::kR + c][si];
+                    v[c] += gcc * vis;
+                    dot += gcc * (colv[c] - rc);
+                    w.state[S::kR + c][si] = e.alpha * colv[c] + one_m * rc;
+                }
                 const float g_alpha = Tb * (dot + ga * Ta);
                 const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
-                v[kOp] += g_raw * e.resp;
+                v[G::kOp] += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
                 const float gmx = g_s * (q.x * ct.dx + q.y * e.dy);
                 const float gmy = g_s * (q.z * e.dy + q.y * ct.dx);
-                v[kMx] += gmx;
-                v[kMy] += gmy;
-                v[kQa] += g_s * (0.5f * ct.dx * ct.dx);
-                v[kQb] += g_s * (ct.dx * e.dy);
-                v[kQc] += g_s * (0.5f * e.dy * e.dy);
+                v[G::kMx] += gmx;
+                v[G::kMy] += gmy;
+                v[G::kQa] += g_s * (0.5f * ct.dx * ct.dx);
+                v[G::kQb] += g_s * (ct.dx * e.dy);
+                v[G::kQc] += g_s * (0.5f * e.dy * e.dy);
                 if (ABS) {
-                    v[kAx] += fabsf(gmx);
-                    v[kAy] += fabsf(gmy);
+                    v[G::kAx] += fabsf(gmx);
+                    v[G::kAy] += fabsf(gmy);
                 }
-                w.state[kR0][si] = e.alpha * col.x + one_m * r0;
-                w.state[kR1][si] = e.alpha * col.y + one_m * r1;
-                w.state[kR2][si] = e.alpha * col.z + one_m * r2;
-                w.state[kTa][si] = Ta * one_m;
-                w.state[kTc][si] = Tb;
+                w.state[S::kTa][si] = Ta * one_m;
+                w.state[S::kTc][si] = Tb;
             }
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
@@ -679,51 +688,91 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             // after that packing orders this entry's reads before its reuse
             lb ^= 1;
             if (++nslots == kRedEntries) {
-                flush_reduction<F>(w, nslots, gr, lane);
+                flush_reduction<CH, F>(w, nslots, a, gr, lane);
                 nslots = 0;
             }
         }
     }
-    if (nslots) flush_reduction<F>(w, nslots, gr, lane);
+    if (nslots) flush_reduction<CH, F>(w, nslots, a, gr, lane);
+}
+
+template <int CH>
+void fwd_chunk(const RasterArgs& a, float* render_colors, float* render_alphas,
+               int32_t* last_ids, int32_t* pair_counts, uint32_t* trace, cudaStream_t s) {
+    const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
+    const dim3 g((unsigned)tiles), b(kThreads);
+    if (pair_counts && trace)
+        k_raster_fwd<CH, true, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                     pair_counts, trace);
+    else if (pair_counts)
+        k_raster_fwd<CH, true, false><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                      pair_counts, nullptr);
+    else if (trace)
+        k_raster_fwd<CH, false, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
+                                                      nullptr, trace);
+    else
+        k_raster_fwd<CH, false, false><<<g, b, 0, s>>>(a, render_colors, render_alphas,
+                                                       last_ids, nullptr, nullptr);
+}
+
+template <int CH>
+void bwd_chunk(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
+               cudaStream_t s) {
+    const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
+    const dim3 gd((unsigned)tiles), b(kThreads);
+    if (g.grad_means2d_abs) {
+        if (trace)
+            k_raster_bwd<CH, true, true><<<gd, b, 0, s>>>(a, g, trace);
+        else
+            k_raster_bwd<CH, true, false><<<gd, b, 0, s>>>(a, g, nullptr);
+    } else {
+        if (trace)
+            k_raster_bwd<CH, false, true><<<gd, b, 0, s>>>(a, g, trace);
+        else
+            k_raster_bwd<CH, false, false><<<gd, b, 0, s>>>(a, g, nullptr);
+    }
 }
 
 }  // namespace
 
-void launch_raster_fwd(const RasterArgs& a, float* render_colors, float* render_alphas,
+// Channels are processed in chunks of up to 4 (one launch each): compositing
+// is independent per channel, and every per-splat term of the backward is
+// linear in the per-channel sum, so the chunks' atomic contributions add up
+// to the full gradient (the render_alpha term is added by the first chunk).
+void launch_raster_fwd(RasterArgs a, float* render_colors, float* render_alphas,
                        int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
                        cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
-    const dim3 g((unsigned)tiles), b(kThreads);
-    if (pair_counts && trace)
-        k_raster_fwd<true, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
-                                                 pair_counts, trace);
-    else if (pair_counts)
-        k_raster_fwd<true, false><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
-                                                  pair_counts, nullptr);
-    else if (trace)
-        k_raster_fwd<false, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
-                                                  nullptr, trace);
-    else
-        k_raster_fwd<false, false><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
-                                                   nullptr, nullptr);
+    for (int off = 0; off < a.channels; off += 4) {
+        a.ch_off = off;
+        a.first_chunk = off == 0;
+        const int ch = a.channels - off < 4 ? a.channels - off : 4;
+        int32_t* pc = off == 0 ? pair_counts : nullptr;
+        uint32_t* tr = off == 0 ? trace : nullptr;
+        switch (ch) {
+            case 1: fwd_chunk<1>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
+            case 2: fwd_chunk<2>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
+            case 3: fwd_chunk<3>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
+            default: fwd_chunk<4>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
+        }
+    }
 }
 
-void launch_raster_bwd(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
+void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace,
                        cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
-    const dim3 gd((unsigned)tiles), b(kThreads);
-    if (g.grad_means2d_abs) {
-        if (trace)
-            k_raster_bwd<true, true><<<gd, b, 0, s>>>(a, g, trace);
-        else
-            k_raster_bwd<true, false><<<gd, b, 0, s>>>(a, g, nullptr);
-    } else {
-        if (trace)
-            k_raster_bwd<false, true><<<gd, b, 0, s>>>(a, g, trace);
-        else
-            k_raster_bwd<false, false><<<gd, b, 0, s>>>(a, g, nullptr);
+    for (int off = 0; off < a.channels; off += 4) {
+        a.ch_off = off;
+        a.first_chunk = off == 0;
+        const int ch = a.channels - off < 4 ? a.channels - off : 4;
+        switch (ch) {
+            case 1: bwd_chunk<1>(a, g, trace, s); break;
+            case 2: bwd_chunk<2>(a, g, trace, s); break;
+            case 3: bwd_chunk<3>(a, g, trace, s); break;
+            default: bwd_chunk<4>(a, g, trace, s); break;
+        }
     }
 }
 

@@ -199,22 +199,24 @@ def upstream_grads(C: int, H: int, W: int, channels: int = 3, seed: int = 1):
 
 def random_small(seed: int, C: int = 1, N: int = 16, W: int = 32, H: int = 32,
                  tile_size: int = 16, elliptical: bool = True, sigma=(1.0, 5.0),
-                 opacity=(0.05, 0.95), background: bool = True, radius_scale: float = 3.0) -> Scene:
-    """Small generic scene (tests): uniform means inside the image, uniform sigmas."""
+                 opacity=(0.05, 0.95), background: bool = True, radius_scale: float = 3.0,
+                 channels: int = 3) -> Scene:
+    """Small generic scene (tests): uniform means inside the image, uniform sigmas,
+    `channels` colour channels per splat uniform in [0, 1)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     means = rng.uniform([0.0, 0.0], [W, H], (C, N, 2))
     sig = rng.uniform(sigma[0], sigma[1], (C, N, 2))
     theta = rng.uniform(0.0, math.pi, (C, N))
     depth = rng.uniform(1.0, 10.0, (C, N))
     opac = rng.uniform(opacity[0], opacity[1], (C, N))
-    rgb = rng.uniform(0.0, 1.0, (C, N, 3))
+    rgb = rng.uniform(0.0, 1.0, (C, N, channels))
     sxx, sxy, syy = _covariance_from_axes(sig[..., 0], sig[..., 1], theta)
     if elliptical:
         radii = np.stack([np.ceil(radius_scale * np.sqrt(sxx)),
                           np.ceil(radius_scale * np.sqrt(syy))], axis=-1)
     else:
         radii = np.ceil(radius_scale * sig.max(axis=-1))
-    bg = rng.uniform(0.0, 1.0, (C, 3)) if background else None
+    bg = rng.uniform(0.0, 1.0, (C, channels)) if background else None
     return _finish(f"small_{seed}", C, N, W, H, tile_size, means, radii, depth,
                    _conic(sxx, sxy, syy), rgb, opac, bg)
 
