@@ -55,6 +55,9 @@ def lib():
                                         P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
                                         F32, P, P]
         L.orc_rasterize_bwd.restype = I32
+        L.orc_project.argtypes = [P, P, P, P, I64, I64, I32, I32, F32, F32, F32, F32, I32, P, P,
+                                  P, P, P]
+        L.orc_project.restype = I32
         _lib = L
     return _lib
 
@@ -261,3 +264,27 @@ def render(scene, sort=True, pixels=None, tie_rel=0.0, tie_rel_T=None):
                         offsets, ids, scene.alpha_cutoff, scene.transmittance_threshold,
                         pixels=pixels, tie_rel=tie_rel, tie_rel_T=tie_rel_T)
     return dict(tiles_per_gauss=tpg, keys=keys, flatten_ids=ids, offsets=offsets), fwd
+
+
+def project(means, covars, viewmats, intrinsics, width, height, eps2d=0.3, near_plane=0.01,
+            far_plane=1e10, radius_clip=0.0, compensation=False, orthographic=False):
+    """EWA projection (project.cpp).  means (N,3), covars (N,3,3), viewmats
+    (C,4,4), intrinsics (C,3,3).  Returns dict(radii int32 (C,N,2), means2d
+    (C,N,2), depths (C,N), conics (C,N,3), compensations (C,N) or None)."""
+    means = _c(means, np.float32)
+    covars = _c(covars, np.float32)
+    viewmats = _c(viewmats, np.float32)
+    intrinsics = _c(intrinsics, np.float32)
+    N = means.shape[0]
+    C = viewmats.shape[0]
+    out = dict(radii=np.empty((C, N, 2), np.int32), means2d=np.empty((C, N, 2), np.float32),
+               depths=np.empty((C, N), np.float32), conics=np.empty((C, N, 3), np.float32),
+               compensations=np.empty((C, N), np.float32) if compensation else None)
+    rc = lib().orc_project(_ptr(means), _ptr(covars), _ptr(viewmats), _ptr(intrinsics), C, N,
+                           int(width), int(height), float(eps2d), float(near_plane),
+                           float(far_plane), float(radius_clip), int(bool(orthographic)),
+                           _ptr(out["radii"]), _ptr(out["means2d"]), _ptr(out["depths"]),
+                           _ptr(out["conics"]), _ptr(out["compensations"]))
+    if rc:
+        raise ValueError("orc_project: bad sizes")
+    return out

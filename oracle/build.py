@@ -1,4 +1,4 @@
-"""Compile the CPU oracle (oracle.cpp) into oracle/_build/liboracle.so.
+"""Compile the CPU oracle (oracle.cpp, project.cpp) into oracle/_build/liboracle.so.
 
 Test infrastructure: the oracle checks the CUDA library and is never called
 by it.  Plain g++, no contraction of a*b+c into FMA (-ffp-contract=off), so
@@ -10,7 +10,7 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "oracle.cpp")
+SRCS = [os.path.join(HERE, "oracle.cpp"), os.path.join(HERE, "project.cpp")]
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboracle.so")
 
@@ -19,10 +19,11 @@ FLAGS = ["-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-
 
 def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+    if (not force and os.path.exists(LIB)
+            and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SRCS)):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["g++", *FLAGS, SRC, "-o", tmp]
+    cmd = ["g++", *FLAGS, *SRCS, "-o", tmp]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

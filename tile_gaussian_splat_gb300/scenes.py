@@ -234,3 +234,123 @@ def workload(k: int, seed: int = 0) -> Scene:
     if k == 5:
         return workload2(seed)
     return WORKLOADS[k](seed)
+
+
+# ---------------------------------------------------------------------------
+# 3D inputs of the projection that produces the 2D splats.
+#
+#   means       float32 (N, 3)      world-space centres
+#   covars      float32 (N, 3, 3)   world-space covariances (symmetric)
+#   viewmats    float32 (C, 4, 4)   world-to-camera, row-major [R | t; 0 0 0 1]
+#   intrinsics  float32 (C, 3, 3)   [[fx, skew, cx], [0, fy, cy], [0, 0, 1]]
+#
+# Camera convention of the pinhole map: x right, y down, z forward.
+
+
+@dataclasses.dataclass
+class Scene3D:
+    name: str
+    width: int
+    height: int
+    means: np.ndarray
+    covars: np.ndarray
+    viewmats: np.ndarray
+    intrinsics: np.ndarray
+    eps2d: float = 0.3
+    near_plane: float = 0.01
+    far_plane: float = 1e10
+    radius_clip: float = 0.0
+
+    @property
+    def C(self) -> int:
+        return self.viewmats.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.means.shape[0]
+
+
+def random_rotations(rng, n):
+    """n rotation matrices (float64) from uniformly drawn unit quaternions."""
+    q = rng.standard_normal((n, 4))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    w, x, y, z = q[:, 0], q[:, 1], q[:, 2], q[:, 3]
+    return np.stack([
+        1 - 2 * (y * y + z * z), 2 * (x * y - w * z), 2 * (x * z + w * y),
+        2 * (x * y + w * z), 1 - 2 * (x * x + z * z), 2 * (y * z - w * x),
+        2 * (x * z - w * y), 2 * (y * z + w * x), 1 - 2 * (x * x + y * y)], axis=1).reshape(n, 3, 3)
+
+
+def look_at(eye, target, up=(0.0, -1.0, 0.0)):
+    """World-to-camera 4x4 (float64) for a camera at `eye` looking at `target`,
+    z forward, y down (the `up` hint points up in the image)."""
+    eye = np.asarray(eye, np.float64)
+    f = np.asarray(target, np.float64) - eye
+    f /= np.linalg.norm(f)
+    down = -np.asarray(up, np.float64)
+    r = np.cross(down, f)
+    r /= np.linalg.norm(r)
+    d = np.cross(f, r)
+    R = np.stack([r, d, f])  # rows: camera axes in world coordinates
+    V = np.eye(4)
+    V[:3, :3] = R
+    V[:3, 3] = -R @ eye
+    return V
+
+
+def _covars_from_scales(rng, scales):
+    R = random_rotations(rng, scales.shape[0])
+    M = R * scales[:, None, :]
+    return M @ np.transpose(M, (0, 2, 1))
+
+
+def scene3d(seed: int = 0, C: int = 4, N: int = 1_000_000, W: int = 1920, H: int = 1080,
+            focal: float = 1100.0) -> Scene3D:
+    """Gaussians in the cube [-1, 1]^3 (64 clusters, std 0.15, plus 20 %
+    uniform), axis scales log-normal(mean ln 0.01, std 0.8) clipped to
+    [1e-4, 0.5], uniform orientations; C cameras on a circle of radius 3
+    around the origin at height 0.5, all looking at the origin, focal
+    `focal` px, principal point at the image centre."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n_bg = N // 5
+    centres = rng.uniform(-0.8, 0.8, (64, 3))
+    which = rng.integers(0, 64, N - n_bg)
+    means = np.concatenate([centres[which] + rng.normal(0.0, 0.15, (N - n_bg, 3)),
+                            rng.uniform(-1.0, 1.0, (n_bg, 3))])
+    scales = np.clip(np.exp(rng.normal(math.log(0.01), 0.8, (N, 3))), 1e-4, 0.5)
+    covars = _covars_from_scales(rng, scales)
+    views, Ks = [], []
+    for c in range(C):
+        a = 2 * math.pi * c / C + 0.3
+        views.append(look_at((3.0 * math.cos(a), -0.5, 3.0 * math.sin(a)), (0.0, 0.0, 0.0)))
+        Ks.append([[focal, 0.0, W / 2], [0.0, focal, H / 2], [0.0, 0.0, 1.0]])
+    f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+    return Scene3D(name=f"proj_{C}x{N}_{W}x{H}", width=W, height=H, means=f32(means),
+                   covars=f32(covars), viewmats=f32(np.stack(views)), intrinsics=f32(Ks))
+
+
+def scene3d_edge(seed: int = 0, N: int = 4000, W: int = 200, H: int = 120) -> Scene3D:
+    """Small scene (tests) that exercises every branch of the projection: two
+    cameras (one with skew and off-centre principal point), Gaussians in
+    front of, behind and beside the cameras, some far outside the frustum,
+    some at the near plane, a few with degenerate (rank-deficient or zero)
+    and a few with huge covariances."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    means = rng.uniform([-6.0, -4.0, -3.0], [6.0, 4.0, 12.0], (N, 3))
+    scales = np.exp(rng.uniform(math.log(1e-3), math.log(2.0), (N, 3)))
+    covars = _covars_from_scales(rng, scales)
+    k = N // 40
+    covars[:k] = 0.0                                   # zero covariance
+    covars[k:2 * k, 2, :] = 0.0                        # rank-deficient
+    covars[k:2 * k, :, 2] = 0.0
+    covars[2 * k:3 * k] *= 1e12                        # huge radius
+    covars[5 * k:6 * k] *= 1e16                        # radius saturates / det overflows
+    means[3 * k:4 * k, 2] = 0.01                       # on the near plane
+    means[4 * k:5 * k, :2] *= 50.0                     # far outside the frustum
+    views = [look_at((0.0, 0.0, -4.0), (0.0, 0.0, 0.0)),
+             look_at((3.0, -1.0, -3.0), (0.2, 0.1, 1.0))]
+    Ks = [[[180.0, 0.0, W / 2], [0.0, 170.0, H / 2], [0.0, 0.0, 1.0]],
+          [[150.0, 2.5, 0.4 * W], [0.0, 160.0, 0.6 * H], [0.0, 0.0, 1.0]]]
+    f32 = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+    return Scene3D(name=f"proj_edge_{seed}", width=W, height=H, means=f32(means),
+                   covars=f32(covars), viewmats=f32(np.stack(views)), intrinsics=f32(Ks))
