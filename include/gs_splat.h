@@ -2,7 +2,8 @@
  * gs_splat.h -- C ABI of the GB300 (sm_103a) tile-binned Gaussian-splat
  * raster library (libgs_splat_gb300.so).
  *
- * The path has four calls, in order:
+ * The path has four calls, in order (gs_project, before them, makes their
+ * 2D inputs from 3D Gaussians):
  *   gs_isect_tiles    tile rect of every splat, 64-bit intersection keys
  *                     (camera | tile | depth bits) with flatten ids, sorted
  *   gs_tile_offsets   first list position of every tile
@@ -13,6 +14,8 @@
  *   gsplat 1.0.0, data/ext/gsplat_native/intersections.c:
  *       gs_tile_bits, gs_bounds, gs_isect_tiles, gs_radix_sort_without_gvl,
  *       gs_offset_encode
+ *   gsplat 1.0.0, data/ext/gsplat_native/projection.c: gs_project_one,
+ *       gs_projection_forward
  *   gsplat 1.0.0, data/ext/gsplat_native/raster_backward.c and
  *       raster_backward_bridge.c: gs_raster_backward_pixel,
  *       gs_raster_backward_without_gvl, gs_raster_backward
@@ -130,6 +133,44 @@ int gs_isect_tiles(const float* means2d, const float* radii, int elliptical,
 int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C,
                     int tile_width, int tile_height, int32_t* offsets,
                     int32_t* d_status, void* stream);
+
+/*
+ * gs_project -- gsplat 1.0.0, data/ext/gsplat_native/projection.c,
+ * gs_project_one (per camera c and Gaussian n) and gs_projection_forward
+ * (argument and output set).  Produces the 2D inputs of gs_isect_tiles and
+ * gs_rasterize_fwd from 3D Gaussians.
+ *   p = R mean + t, depth = p.z, S = (R Sigma) R^T   (R, t from viewmats[c])
+ *   z = depth, or 1 when depth <= near_plane or depth >= far_plane
+ *   perspective: J = [[fx/z, 0, -fx tx/z^2], [0, fy/z, -fy ty/z^2]] with
+ *     tx/z, ty/z clamped to the image extent widened by 0.15 of the image
+ *     size on each side; means2d = (K row 0, K row 1) . (p.x, p.y, z) / z
+ *   orthographic (orthographic != 0): J = [[fx, 0, 0], [0, fy, 0]],
+ *     means2d = (fx p.x + cx, fy p.y + cy)
+ *   cov = J S J^T; det0 = det(cov); cov += eps2d I; det = det(cov)
+ *   r_i = ceil(3.33 sqrt(max(cov_ii, 0))) (saturating at 2^31 - 1)
+ *   visible = det > 0, near < depth < far, r_x or r_y above radius_clip,
+ *     and the box means2d +- r overlapping [0, W] x [0, H]
+ *   radii = visible ? r : 0; conics = (cov_11, -(cov_01 + cov_10) / 2,
+ *     cov_00) / det' with det' = det, or 1e-10 when det <= 0;
+ *   compensations = sqrt(max(det0 / det', 0)).
+ * Every operation is one IEEE single-precision operation in the order
+ * above (no fused multiply-add), so results are reproducible bit for bit.
+ * Inputs (device, float32): means (N,3), covars (N,3,3) (symmetric),
+ *   viewmats (C,4,4) world-to-camera row-major [R | t], intrinsics (C,3,3)
+ *   [[fx, skew, cx], [k10, fy, cy], [0, 0, 1]].
+ * Outputs, indexed c*N + n: radii int32 (C,N,2), means2d float32 (C,N,2),
+ *   depths (C,N), conics (C,N,3) (written for every pair, visible or not);
+ *   compensations (C,N) or NULL; radii_float float32 (C,N,2) or NULL: the
+ *   radii as floats, the form gs_isect_tiles takes (elliptical).
+ *   radii, means2d and radii_float must be 8-byte aligned.
+ * Limits: C >= 1, N >= 0, C*N < 2^31, width, height >= 1.
+ */
+int gs_project(const float* means, const float* covars, const float* viewmats,
+               const float* intrinsics, int C, int N, int width, int height,
+               float eps2d, float near_plane, float far_plane, float radius_clip,
+               int orthographic, int32_t* radii, float* means2d, float* depths,
+               float* conics, float* compensations, float* radii_float,
+               int32_t* d_status, void* stream);
 
 /* Largest channel count the rasterizer accepts. */
 #define GS_MAX_CHANNELS 1024

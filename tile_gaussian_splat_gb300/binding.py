@@ -38,6 +38,8 @@ SIGNATURES = {
                                F32, P, P, P, P, P, P, P]),
     "gs_rasterize_bwd": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I64, F32,
                                P, P, P, P, P, P, P, P, P, P, P, P, P]),
+    "gs_project": (I32, [P, P, P, P, I32, I32, I32, I32, F32, F32, F32, F32, I32, P, P, P, P, P,
+                         P, P, P]),
     "gs_sort_workspace_size": (SZ, [I64]),
     "gs_sort_pairs": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
     "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
@@ -160,6 +162,33 @@ def gs_tile_offsets(keys, C, tile_width, tile_height, d_status=None, out=None, s
                                  _ptr(offsets), _ptr(d_status), _stream(stream)),
            "gs_tile_offsets")
     return offsets
+
+
+def gs_project(means, covars, viewmats, intrinsics, width, height, eps2d=0.3, near_plane=0.01,
+               far_plane=1e10, radius_clip=0.0, compensation=False, orthographic=False,
+               radii_float=False, d_status=None, out=None, stream=None):
+    """EWA projection.  means (N,3), covars (N,3,3), viewmats (C,4,4),
+    intrinsics (C,3,3), float32 CUDA tensors.  Returns dict(radii int32
+    (C,N,2), means2d (C,N,2), depths (C,N), conics (C,N,3), compensations
+    (C,N) or None, radii_float (C,N,2) or None: the radii as gs_isect_tiles
+    takes them)."""
+    N = means.shape[0]
+    C = viewmats.shape[0]
+    dev = means.device
+    if out is None:
+        out = dict(radii=_empty((C, N, 2), torch.int32, dev),
+                   means2d=_empty((C, N, 2), torch.float32, dev),
+                   depths=_empty((C, N), torch.float32, dev),
+                   conics=_empty((C, N, 3), torch.float32, dev),
+                   compensations=_empty((C, N), torch.float32, dev) if compensation else None,
+                   radii_float=_empty((C, N, 2), torch.float32, dev) if radii_float else None)
+    _check(lib().gs_project(
+        _ptr(means), _ptr(covars), _ptr(viewmats), _ptr(intrinsics), C, N, int(width),
+        int(height), float(eps2d), float(near_plane), float(far_plane), float(radius_clip),
+        int(bool(orthographic)), _ptr(out["radii"]), _ptr(out["means2d"]), _ptr(out["depths"]),
+        _ptr(out["conics"]), _ptr(out["compensations"]), _ptr(out["radii_float"]),
+        _ptr(d_status), _stream(stream)), "gs_project")
+    return out
 
 
 def gs_rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,

@@ -355,6 +355,28 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
     return check_launch();
 }
 
+int gs_project(const float* means, const float* covars, const float* viewmats,
+               const float* intrinsics, int C, int N, int width, int height, float eps2d,
+               float near_plane, float far_plane, float radius_clip, int orthographic,
+               int32_t* radii, float* means2d, float* depths, float* conics,
+               float* compensations, float* radii_float, int32_t* d_status, void* stream) {
+    (void)d_status;
+    if (C < 1 || N < 0 || width < 1 || height < 1) return GS_ERR_INVALID_ARG;
+    if ((int64_t)C * N >= ((int64_t)1 << 31)) return GS_ERR_INVALID_ARG;
+    if (N == 0) return GS_OK;
+    if (!means || !covars || !viewmats || !intrinsics || !radii || !means2d || !depths || !conics)
+        return GS_ERR_INVALID_ARG;
+    // radii, means2d and radii_float are stored as 8-byte pairs
+    if ((reinterpret_cast<uintptr_t>(radii) | reinterpret_cast<uintptr_t>(means2d) |
+         reinterpret_cast<uintptr_t>(radii_float)) & 7u)
+        return GS_ERR_INVALID_ARG;
+    const ProjectArgs pa{width, height, orthographic ? 1 : 0, eps2d, near_plane, far_plane,
+                         radius_clip};
+    launch_project(means, covars, viewmats, intrinsics, C, N, pa, radii, means2d, depths, conics,
+                   compensations, radii_float, static_cast<cudaStream_t>(stream));
+    return check_launch();
+}
+
 size_t gs_sort_workspace_size(int64_t n) {
     if (n < 0) return 0;
     Carver cv{nullptr};

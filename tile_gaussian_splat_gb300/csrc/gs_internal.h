@@ -109,4 +109,16 @@ struct RasterGrads {
 void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace,
                        cudaStream_t s);
 
+// ---- projection (project.cu)
+struct ProjectArgs {
+    int width, height, orthographic;
+    float eps2d, near_plane, far_plane, radius_clip;
+};
+// means (N,3), covars (N,3,3), viewmats (C,4,4), intrinsics (C,3,3); outputs
+// indexed c*N + n; compensations and radii_float may be null.
+void launch_project(const float* means, const float* covars, const float* viewmats,
+                    const float* intrinsics, int C, int N, const ProjectArgs& pa, int32_t* radii,
+                    float* means2d, float* depths, float* conics, float* compensations,
+                    float* radii_float, cudaStream_t s);
+
 }  // namespace gs
