@@ -387,10 +387,14 @@ def run_ours(args, rank, world, scene):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e = float(t.item())
 
+    proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
+
     if rank != 0:
         return None
 
     hbm_peak, peak_kind = _peaks()
+    proj.update(achieved_gbs=round(proj["bytes"] / (proj["ms"] * 1e-3) / 1e9, 1))
+    proj["frac"] = round(proj["achieved_gbs"] / hbm_peak, 4)
     st = stage_ms.mean(axis=0)
     names = ["isect_query", "isect_emit_sort", "tile_ranges", "raster_fwd", "raster_bwd"]
     CN, I = s.C * s.N, path.I
@@ -467,6 +471,7 @@ def run_ours(args, rank, world, scene):
         "work": {"pairs_evaluated_fwd": n_eval, "pairs_composited": n_comp,
                  "pairs_evaluated_bwd": bwd_eval},
         "roofline": roof,
+        "project": proj,
         "e2e": {"value": round(pixels / (e2e * 1e-3) / 1e6 * world, 2),
                 "unit": "Mpixel/s (pinned host inputs -> image + gradients on host, "
                         "uploads/downloads overlapped with the previous/next step)",
@@ -477,6 +482,44 @@ def run_ours(args, rank, world, scene):
         "wall_s_timed": round(t_wall, 3),
     }
     return line
+
+
+def time_projection(dev, flush, warmup, steps):
+    """gs_project on 4 cameras x 1M Gaussians at 1920x1080 (the 3D scene of
+    the same size as workload 3), timed alone: it makes the raster path's
+    inputs and is not part of the raster step.  Outputs include the
+    compensations and the float radii gs_isect_tiles takes."""
+    import torch
+
+    from tile_gaussian_splat_gb300 import binding as gsb
+    from tile_gaussian_splat_gb300 import scenes
+
+    s = scenes.scene3d()
+    t = lambda a: torch.from_numpy(a).to(dev)
+    m, cv, V, K = t(s.means), t(s.covars), t(s.viewmats), t(s.intrinsics)
+    out = gsb.gs_project(m, cv, V, K, s.width, s.height, compensation=True, radii_float=True)
+    for _ in range(warmup):
+        gsb.gs_project(m, cv, V, K, s.width, s.height, out=out)
+        flush.zero_()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        gsb.gs_project(m, cv, V, K, s.width, s.height, out=out)
+        b.record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    CN = s.C * s.N
+    visible = int((out["radii"][..., 0] > 0).sum())
+    return {"kernel": "k_project", "ms": round(ms, 4), "bound": "hbm",
+            "bytes": s.N * 48 + CN * 44,
+            "msplat_per_s": round(CN / (ms * 1e-3) / 1e6, 1),
+            "config": {"scene": s.name, "C": s.C, "N": s.N, "width": s.width,
+                       "height": s.height, "visible_pairs": visible,
+                       "outputs": "radii, means2d, depths, conics, compensations, radii_float",
+                       "l2": "flushed between launches"}}
 
 
 # -------------------------------------------------------- oracle arm

@@ -74,6 +74,17 @@ struct PairEval {
     float dy, s, resp, raw, alpha;
 };
 
+// exp(-s) as 2^(-s log2 e): one rounded multiply and the PTX ex2.approx.ftz
+// instruction (relative error below 2^-22; results below 2^-126 flush to 0,
+// where alpha is far below any cutoff).  Relative to exp(-s) the error is
+// at most about 2.4e-7 + |s| 1e-7.
+__device__ __forceinline__ float exp_neg(float s) {
+    constexpr float kMinusLog2e = -1.44269504088896341f;  // -1 / ln 2
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(__fmul_rn(s, kMinusLog2e)));
+    return y;
+}
+
 // s = 0.5 (a dx^2 + c dy^2) + b dx dy rounded exactly as written (no FMA
 // contraction), alpha = min(0.99, o exp(-s)).
 __device__ __forceinline__ PairEval eval_pair(const ColumnTerms& ct, float my, float c, float op,
@@ -83,10 +94,46 @@ __device__ __forceinline__ PairEval eval_pair(const ColumnTerms& ct, float my, f
     const float qc = __fmul_rn(__fmul_rn(c, e.dy), e.dy);
     const float qb = __fmul_rn(ct.bdx, e.dy);
     e.s = __fadd_rn(__fmul_rn(0.5f, __fadd_rn(ct.qa, qc)), qb);
-    e.resp = __expf(-e.s);
+    e.resp = exp_neg(e.s);
     e.raw = __fmul_rn(op, e.resp);
     e.alpha = e.raw > kAlphaClamp ? kAlphaClamp : e.raw;
     return e;
+}
+
+// Fast form of the same evaluation, for entries whose conic is safely
+// positive definite (ac - b^2 > 1e-4 ac with a, c in [1e-18, 1e18] and
+// |b| <= 1e18), whose mean lies within 1e6 of the origin (so no term
+// overflows and no NaN arises) and whose opacity and colours are finite.
+//   * s >= 0 needs no test there: s is at least 5e-5 of 0.5 (a dx^2 + c dy^2)
+//     while the rounding of the exact-order form is below 5e-7 of it.
+//   * With a/2 and c/2 staged, 0.5 ((a dx) dx + (c dy) dy) becomes
+//     (a/2 dx) dx + (c/2 dy) dy: halving is exact and commutes with
+//     rounding while no value is subnormal, which the ranges above and
+//     |dx|, |dy| >= 6e-8 (or 0, for pixel centres at or beyond 0.5) ensure.
+// So s, and with it alpha, is bit for bit the exact-order result, in one
+// multiply less per pixel, and the compositing that follows can be
+// branch-free.
+struct FastColumn {
+    float dx, qa2, bdx;  // dx = mx - px, qa2 = (a/2 dx) dx, bdx = b dx
+};
+
+// h = (a/2, b, c/2, -)
+__device__ __forceinline__ FastColumn fast_column(float mx, const float4& h, float px) {
+    FastColumn t;
+    t.dx = __fsub_rn(mx, px);
+    t.qa2 = __fmul_rn(__fmul_rn(h.x, t.dx), t.dx);
+    t.bdx = __fmul_rn(h.y, t.dx);
+    return t;
+}
+
+// Per-entry staging of the fast form; returns whether it applies.
+__device__ __forceinline__ bool fast_terms(float mx, float my, float a, float b, float c,
+                                           float op, float4& h) {
+    h = make_float4(0.5f * a, b, 0.5f * c, 0.0f);
+    const float ac = a * c;
+    return fabsf(mx) <= 1e6f && fabsf(my) <= 1e6f && fabsf(op) <= 3.0e38f && a >= 1e-18f &&
+           a <= 1e18f && c >= 1e-18f && c <= 1e18f && fabsf(b) <= 1e18f &&
+           ac - b * b > 1e-4f * ac;
 }
 
 // ---------------------------------------------------------------- per tile
@@ -143,7 +190,7 @@ __device__ __forceinline__ TileBox warp_box(const RasterArgs& a, const TileRange
 // rectangle, which for a positive-definite form is 0 inside and otherwise
 // the smallest of the four edge minima (a 1-D quadratic each).  The margin
 // (1e-3 + 1e-5 of the form's magnitude over the rectangle) is far above the
-// rounding of the per-pixel float evaluation and of __expf, so an entry
+// rounding of the per-pixel float evaluation and of exp_neg, so an entry
 // dropped here fails the per-pixel alpha test at every pixel.
 __device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float my, float a,
                                              float b, float c, float op) {
@@ -187,8 +234,9 @@ constexpr int kTraceWords = kWarps * kPPT;  // 8 -> 256 pixels
 template <int BATCH, bool TRACE_IN>
 struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
-    float4 mo[BATCH];   // mx, my, opacity, -
+    float4 mo[BATCH];   // mx, my, opacity, 1 if the fast form applies else 0
     float4 q[BATCH];    // a, b, c, -
+    float4 qf[BATCH];   // fast form: a/2, b, c/2, -
     float4 col[BATCH];  // up to 4 channels of the launch's chunk
     int32_t gid[BATCH];
     int32_t j[BATCH];   // list position
@@ -281,10 +329,16 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
         if ((ball[r][0] >> lane) & 1u) {
             const int pos = base[0] + __popc(ball[r][0] & lt);
             const float* cc = a.colors + (int64_t)gid[r] * a.channels + a.ch_off;
-            st.mo[pos] = mo[r];
+            const float4 col = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
+                                           CH > 3 ? cc[3] : 0.0f);
+            float4 f;
+            bool fast = fast_terms(mo[r].x, mo[r].y, q[r].x, q[r].y, q[r].z, mo[r].z, f);
+            fast = fast && fabsf(col.x) < 3.0e38f && fabsf(col.y) < 3.0e38f &&
+                   fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
+            st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z, fast ? 1.0f : 0.0f);
             st.q[pos] = q[r];
-            st.col[pos] = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
-                                      CH > 3 ? cc[3] : 0.0f);
+            st.qf[pos] = f;
+            st.col[pos] = col;
             st.gid[pos] = gid[r];
             st.j[pos] = (int32_t)jj[r];
             if (TRACE_IN) {
@@ -317,13 +371,23 @@ __device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
 
 // ------------------------------------------------------------------ forward
 
+// Component i (0 or 1, a compile-time constant after unrolling) of a pair.
+__device__ __forceinline__ float& comp(float2& v, int i) { return i ? v.y : v.x; }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
 // At most 85 registers, so 12 blocks (24 warps) fit on an SM.
+//
+// A thread's 4 pixels are handled as two pairs (rows 0-1 and 2-3 of its
+// strip) with the packed f32x2 operations, whose per-component rounding is
+// that of the scalar operation, so results are bit for bit those of the
+// scalar code.
 template <int CH, bool COUNT, bool TRACE>
 __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
                  int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts,
                  uint32_t* __restrict__ trace) {
     constexpr int kBatch = kBatchFwd;
+    constexpr int kPairs = kPPT / 2;
     __shared__ StageSmem<kBatch, false> st;
     __shared__ uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
     const TileRange tr = tile_range(a);
@@ -333,24 +397,32 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     const PixelSlot ps = pixel_slot(tr);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float px = (float)ps.x + 0.5f;
-    float T[kPPT], acc[kPPT][4], py[kPPT];
+    float2 T[kPairs], acc[kPairs][4], npy[kPairs];
+    float py[kPPT];
     int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT], n_last[kPPT];
     bool done[kPPT];
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
-        T[k] = 1.0f;
-        acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.0f;
         last[k] = -1;
         n_eval[k] = n_comp[k] = n_last[k] = 0;
         done[k] = !(ps.x < a.width && ps.y0 + k < a.height);
         py[k] = (float)(ps.y0 + k) + 0.5f;
     }
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) {
+        T[p] = splat2(1.0f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[p][c] = splat2(0.0f);
+        npy[p] = make_float2(-py[2 * p], -py[2 * p + 1]);
+    }
+    const float2 one = splat2(1.0f), minus_one = splat2(-1.0f);
     for (int64_t b0 = tr.start; b0 < tr.end; b0 += kBatch) {
         bool all_done = true;
 #pragma unroll
         for (int k = 0; k < kPPT; ++k) all_done &= done[k];
         if (__syncthreads_count(all_done) == kThreads) break;
         const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
+        const int32_t b0_32 = (int32_t)b0;  // list positions are below 2^31
         if (TRACE)
             for (int i = tid; i < kBatch * kTraceWords; i += kThreads) (&s_trace[0][0])[i] = 0u;
         stage_batch<false, false, kBatch, CH>(a, box, b0, b0 + n_raw, nullptr, st);
@@ -359,43 +431,91 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
             for (int ii = 0; ii < nw; ++ii) {
                 const int i = st.idx[warp][ii];
                 const float4 mo = st.mo[i];
-                const float4 q = st.q[i];
-                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
                 const int32_t j = st.j[i];
-                // the 4 evaluations are independent and branch-free, so they
-                // interleave; only compositing branches
-                float alpha[kPPT];
+                const float4 col = st.col[i];
+                const float colv[4] = {col.x, col.y, col.z, col.w};
                 bool took[kPPT];
+                if (mo.w != 0.0f) {  // fast form (warp-uniform): branch-free compositing
+                    const float4 h = st.qf[i];
+                    const FastColumn fc = fast_column(mo.x, h, px);
+                    const float2 qa2 = splat2(fc.qa2), bdx = splat2(fc.bdx), c2 = splat2(h.z);
+                    const float2 my = splat2(mo.y), op = splat2(mo.z);
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                    alpha[k] = e.alpha;
-                    took[k] = !done[k] && e.s >= 0.0f && e.alpha >= a.alpha_cutoff;
-                    if (COUNT) n_eval[k] += done[k] ? 0 : 1;
-                }
+                    for (int p = 0; p < kPairs; ++p) {
+                        // s = (a/2 dx) dx + (c/2 dy) dy + (b dx) dy, per pixel.  The
+                        // sums stay scalar: a packed product feeding a packed sum is
+                        // fused into one packed FMA by the code generator despite
+                        // the explicit rounding, which would round s differently.
+                        const float2 dy = __fadd2_rn(my, npy[p]);
+                        const float2 qc2 = __fmul2_rn(__fmul2_rn(c2, dy), dy);
+                        const float2 qb = __fmul2_rn(bdx, dy);
+                        const float2 sv = make_float2(__fadd_rn(__fadd_rn(qa2.x, qc2.x), qb.x),
+                                                      __fadd_rn(__fadd_rn(qa2.y, qc2.y), qb.y));
+                        const float2 raw =
+                            __fmul2_rn(op, make_float2(exp_neg(sv.x), exp_neg(sv.y)));
+                        float2 aw;
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    if (!took[k]) continue;
-                    const float4 col = st.col[i];
-                    const PairEval e{0.0f, 0.0f, 0.0f, 0.0f, alpha[k]};
-                    const float w = T[k] * e.alpha;
-                    acc[k][0] += w * col.x;
-                    if (CH > 1) acc[k][1] += w * col.y;
-                    if (CH > 2) acc[k][2] += w * col.z;
-                    if (CH > 3) acc[k][3] += w * col.w;
-                    T[k] = T[k] * (1.0f - e.alpha);
-                    last[k] = j;
-                    if (COUNT) {
-                        ++n_comp[k];
-                        n_last[k] = n_eval[k];
+                        for (int e = 0; e < 2; ++e) {
+                            const int k = 2 * p + e;
+                            const float alpha = fminf(comp(const_cast<float2&>(raw), e),
+                                                      kAlphaClamp);
+                            took[k] = !done[k] && alpha >= a.alpha_cutoff;
+                            if (COUNT) n_eval[k] += done[k] ? 0 : 1;
+                            // a pair not taken adds exactly 0 (finite colours, T)
+                            comp(aw, e) = took[k] ? alpha : 0.0f;
+                        }
+                        const float2 w = __fmul2_rn(T[p], aw);
+#pragma unroll
+                        for (int c = 0; c < CH; ++c)
+                            acc[p][c] = __ffma2_rn(w, splat2(colv[c]), acc[p][c]);
+                        T[p] = __fmul2_rn(T[p], __ffma2_rn(aw, minus_one, one));
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int k = 2 * p + e;
+                            last[k] = took[k] ? j : last[k];
+                            if (COUNT && took[k]) {
+                                ++n_comp[k];
+                                n_last[k] = n_eval[k];
+                            }
+                            done[k] = done[k] ||
+                                      (took[k] && comp(T[p], e) < a.transmittance_threshold);
+                        }
                     }
-                    if (T[k] < a.transmittance_threshold) done[k] = true;
+                } else {  // exact-order form, with the s >= 0 test
+                    const float4 q = st.q[i];
+                    const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+                    float alpha[kPPT];
+#pragma unroll
+                    for (int k = 0; k < kPPT; ++k) {
+                        const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                        alpha[k] = e.alpha;
+                        took[k] = !done[k] && e.s >= 0.0f && e.alpha >= a.alpha_cutoff;
+                        if (COUNT) n_eval[k] += done[k] ? 0 : 1;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kPPT; ++k) {
+                        if (!took[k]) continue;
+                        float& Tk = comp(T[k >> 1], k & 1);
+                        const float w = Tk * alpha[k];
+#pragma unroll
+                        for (int c = 0; c < CH; ++c) {
+                            float& ak = comp(acc[k >> 1][c], k & 1);
+                            ak = __fmaf_rn(w, colv[c], ak);
+                        }
+                        Tk = Tk * (1.0f - alpha[k]);
+                        last[k] = j;
+                        if (COUNT) {
+                            ++n_comp[k];
+                            n_last[k] = n_eval[k];
+                        }
+                        if (Tk < a.transmittance_threshold) done[k] = true;
+                    }
                 }
                 if (TRACE) {
 #pragma unroll
                     for (int k = 0; k < kPPT; ++k) {
                         const unsigned m = __ballot_sync(0xffffffffu, took[k]);
-                        if (lane == k) s_trace[j - b0][warp * kPPT + k] = m;
+                        if (lane == k) s_trace[j - b0_32][warp * kPPT + k] = m;
                     }
                 }
                 // leave the batch early once every pixel of the warp has stopped
@@ -424,11 +544,12 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
         const int y = ps.y0 + k;
         if (ps.x < a.width && y < a.height) {
             const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
+            const float Tk = comp(T[k >> 1], k & 1);
             float* o = out_rgb + p * a.channels + a.ch_off;
 #pragma unroll
-            for (int c = 0; c < CH; ++c) o[c] = acc[k][c] + T[k] * bg[c];
+            for (int c = 0; c < CH; ++c) o[c] = comp(acc[k >> 1][c], k & 1) + Tk * bg[c];
             if (!a.first_chunk) continue;
-            out_alpha[p] = 1.0f - T[k];
+            out_alpha[p] = 1.0f - Tk;
             out_last[p] = last[k];
             if (COUNT) {
                 out_counts[3 * p] = n_eval[k];
@@ -639,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 const ColumnTerms ct =
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
                 const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
+                const float dx = ct.dx;
                 const float Tc = w.state[S::kTc][si];
                 // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
                 // cutoff and last_id >= j (from the trace, or tested while
@@ -663,12 +785,12 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
                 v[G::kOp] += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
-                const float gmx = g_s * (q.x * ct.dx + q.y * e.dy);
-                const float gmy = g_s * (q.z * e.dy + q.y * ct.dx);
+                const float gmx = g_s * (q.x * dx + q.y * e.dy);
+                const float gmy = g_s * (q.z * e.dy + q.y * dx);
                 v[G::kMx] += gmx;
                 v[G::kMy] += gmy;
-                v[G::kQa] += g_s * (0.5f * ct.dx * ct.dx);
-                v[G::kQb] += g_s * (ct.dx * e.dy);
+                v[G::kQa] += g_s * (0.5f * dx * dx);
+                v[G::kQb] += g_s * (dx * e.dy);
                 v[G::kQc] += g_s * (0.5f * e.dy * e.dy);
                 if (ABS) {
                     v[G::kAx] += fabsf(gmx);
