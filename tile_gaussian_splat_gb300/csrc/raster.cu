@@ -52,7 +52,6 @@ constexpr int kWarps = kThreads / kWarp;         // 2
 constexpr int kBatchFwd = 2 * kThreads;          // records staged per batch (forward)
 constexpr int kBatchBwd = kThreads;              // records staged per batch (backward)
 constexpr int kWarpPix = kWarp * kPPT;           // pixels per warp (128)
-constexpr int kRedEntries = 2;                   // entries buffered per reduction
 constexpr float kAlphaClamp = 0.99f;
 
 // ---------------------------------------------------------------- per pair
@@ -231,12 +230,12 @@ __device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float m
 // the threads of warp `warp`.
 constexpr int kTraceWords = kWarps * kPPT;  // 8 -> 256 pixels
 
-template <int BATCH, bool TRACE_IN>
+template <int BATCH, bool TRACE_IN, bool FAST>
 struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
     float4 mo[BATCH];   // mx, my, opacity, 1 if the fast form applies else 0
     float4 q[BATCH];    // a, b, c, -
-    float4 qf[BATCH];   // fast form: a/2, b, c/2, -
+    float4 qf[FAST ? BATCH : 1];  // fast form: a/2, b, c/2, - (forward only)
     float4 col[BATCH];  // up to 4 channels of the launch's chunk
     int32_t gid[BATCH];
     int32_t j[BATCH];   // list position
@@ -258,8 +257,8 @@ template <bool REVERSE, bool TRACE_IN, int BATCH, int CH>
 __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&box)[kWarps],
                                            int64_t lo, int64_t hi,
                                            const uint32_t* __restrict__ trace,
-                                           StageSmem<BATCH, TRACE_IN>& st) {
-    constexpr int kPerThread = StageSmem<BATCH, TRACE_IN>::kPerThread;
+                                           StageSmem<BATCH, TRACE_IN, !REVERSE>& st) {
+    constexpr int kPerThread = StageSmem<BATCH, TRACE_IN, !REVERSE>::kPerThread;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = (int)(hi - lo);
     const int64_t CN = (int64_t)a.C * a.N;
@@ -337,7 +336,7 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
                    fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
             st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z, fast ? 1.0f : 0.0f);
             st.q[pos] = q[r];
-            st.qf[pos] = f;
+            if (!REVERSE) st.qf[pos] = f;
             st.col[pos] = col;
             st.gid[pos] = gid[r];
             st.j[pos] = (int32_t)jj[r];
@@ -388,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                  uint32_t* __restrict__ trace) {
     constexpr int kBatch = kBatchFwd;
     constexpr int kPairs = kPPT / 2;
-    __shared__ StageSmem<kBatch, false> st;
+    __shared__ StageSmem<kBatch, false, true> st;
     __shared__ uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
     const TileRange tr = tile_range(a);
     TileBox box[kWarps];
@@ -588,9 +587,11 @@ template <int CH, int F>
 struct BwdWarpSmem {
     float state[StateLayout<CH>::kFields][kWarpPix];
     int16_t list[2][kWarpPix];    // packed valid pairs: k * 32 + owner lane (double buffer)
-    float red[kRedEntries][F][kWarp + 1];
-    int32_t red_gid[kRedEntries];
-    int32_t red_n[kRedEntries];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
+    // entries buffered per reduction: one (entry, field) sum per lane
+    static constexpr int kRed = kWarp / F;
+    float4 red[kRed][F][kWarp / 4];  // per (entry, field): the lanes' terms
+    int32_t red_gid[kRed];
+    int32_t red_n[kRed];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
 };
 
 template <int CH, int F>
@@ -598,22 +599,35 @@ __device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslot
                                                 const RasterArgs& a, const RasterGrads& gr,
                                                 int lane) {
     using G = GradLayout<CH>;
+    static_assert(BwdWarpSmem<CH, F>::kRed >= 1, "one reduction task per lane");
     __syncwarp();
-    for (int t = lane; t < nslots * F; t += kWarp) {
+    const int t = lane;
+    if (t < nslots * F) {
         const int e = t / F, f = t - (t / F) * F;
-        const float* row = w.red[e][f];
-        const int n = w.red_n[e];
-        float sum = 0.0f;
-        for (int l = 0; l < n; ++l) sum += row[l];
-        if (sum == 0.0f) continue;
-        const int64_t g = w.red_gid[e];
-        float* dst;
-        if (f < CH) dst = gr.grad_colors + g * a.channels + a.ch_off + f;
-        else if (f == G::kOp) dst = gr.grad_opacities + g;
-        else if (f <= G::kMy) dst = gr.grad_means2d + 2 * g + (f - G::kMx);
-        else if (f <= G::kQc) dst = gr.grad_conics + 3 * g + (f - G::kQa);
-        else dst = gr.grad_means2d_abs + 2 * g + (f - G::kAx);
-        atomicAdd(dst, sum);
+        const int nch = (w.red_n[e] + 3) >> 2;  // 16-byte chunks holding terms
+        // chunk (i + t) mod 8 at step i: the 8 lanes of a quarter warp read 8
+        // different chunks, so the rows (all starting at bank 0) do not clash
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < kWarp / 4; ++i) {
+            const int c = (i + t) & (kWarp / 4 - 1);
+            if (c < nch) {
+                const float4 q = w.red[e][f][c];
+                acc = __fadd2_rn(acc, make_float2(q.x, q.y));
+                acc = __fadd2_rn(acc, make_float2(q.z, q.w));
+            }
+        }
+        const float sum = acc.x + acc.y;
+        if (sum != 0.0f) {
+            const int64_t g = w.red_gid[e];
+            float* dst;
+            if (f < CH) dst = gr.grad_colors + g * a.channels + a.ch_off + f;
+            else if (f == G::kOp) dst = gr.grad_opacities + g;
+            else if (f <= G::kMy) dst = gr.grad_means2d + 2 * g + (f - G::kMx);
+            else if (f <= G::kQc) dst = gr.grad_conics + 3 * g + (f - G::kQa);
+            else dst = gr.grad_means2d_abs + 2 * g + (f - G::kAx);
+            atomicAdd(dst, sum);
+        }
     }
     __syncwarp();
 }
@@ -631,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     using G = GradLayout<CH>;
     constexpr int F = CH + (ABS ? 8 : 6);
     constexpr int kBatch = kBatchBwd;
-    __shared__ StageSmem<kBatch, TRACE> st;
+    __shared__ StageSmem<kBatch, TRACE, false> st;
     __shared__ BwdWarpSmem<CH, F> ws[kWarps];
     __shared__ float s_bg[kWarps][4];
     __shared__ int s_jmax;
@@ -801,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             }
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
-            for (int f = 0; f < F; ++f) w.red[nslots][f][lane] = v[f];
+            for (int f = 0; f < F; ++f) reinterpret_cast<float*>(w.red[nslots][f])[lane] = v[f];
             if (lane == 0) {
                 w.red_gid[nslots] = st.gid[i];
                 w.red_n[nslots] = min(count, kWarp);
@@ -809,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             // the next entry packs into the other list buffer; the warp sync
             // after that packing orders this entry's reads before its reuse
             lb ^= 1;
-            if (++nslots == kRedEntries) {
+            if (++nslots == BwdWarpSmem<CH, F>::kRed) {
                 flush_reduction<CH, F>(w, nslots, a, gr, lane);
                 nslots = 0;
             }
