@@ -565,12 +565,18 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 // k * 32 + ((l + 8 k) & 31): an owner's accesses for one slot hit 32
 // distinct banks, and the 4 pixels of one column (same lane, slots 0..3)
 // fall in 4 different banks when other lanes gather them.
-// Fields: T, T_after, rem[CH], upstream colour gradient[CH], upstream alpha
-// gradient.
+// Fields: T, Q and the upstream colour gradient g[CH].
+//
+// The walk's remainder rem[CH] and running product T_after enter the alpha
+// gradient only as  sum_c g_c (color_c - rem_c) + g_a T_after
+//   = g . color - Q,   with  Q = g . rem - g_a T_after.
+// Both rem_c and T_after follow  x <- alpha y + (1 - alpha) x  (with y =
+// color_c and y = 0), so Q follows  Q <- alpha (g . color) + (1 - alpha) Q
+// from  Q = g . background - g_a.  One scalar replaces CH + 1 of them.
 template <int CH>
 struct StateLayout {
-    static constexpr int kTc = 0, kTa = 1, kR = 2, kG = 2 + CH, kGA = 2 + 2 * CH;
-    static constexpr int kFields = 3 + 2 * CH;
+    static constexpr int kTc = 0, kQ = 1, kG = 2;
+    static constexpr int kFields = 2 + CH;
 };
 // Gradient fields in the reduction buffer: colours[CH], then these.
 template <int CH>
@@ -688,15 +694,15 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             ga = a.first_chunk ? gr.grad_render_alphas[p] : 0.0f;
         }
         const float Tc = 1.0f - ra[k];
-        w.state[S::kTc][si] = Tc;
-        w.state[S::kTa][si] = 1.0f;
+        float Q = -ga;
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
-            w.state[S::kR + c][si] = bgv[c];
+            Q += gc[c] * bgv[c];
             w.state[S::kG + c][si] = gc[c];
             sb[c] += gc[c] * Tc;
         }
-        w.state[S::kGA][si] = ga;
+        w.state[S::kTc][si] = Tc;
+        w.state[S::kQ][si] = Q;
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
     if (tid == 0) s_jmax = -1;
@@ -780,22 +786,19 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 // cutoff and last_id >= j (from the trace, or tested while
                 // packing); the T < 1 guard depends on the walk and is tested here
                 if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
-                const float Ta = w.state[S::kTa][si];
-                const float ga = w.state[S::kGA][si];
+                const float Q = w.state[S::kQ][si];
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 const float one_m = 1.0f - e.alpha;
                 const float Tb = __fdividef(Tc, one_m);
                 const float vis = Tb * e.alpha;
-                float dot = 0.0f;
+                float gcol = 0.0f;  // g . color
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
                     const float gcc = w.state[S::kG + c][si];
-                    const float rc = w.state[S::kR + c][si];
                     v[c] += gcc * vis;
-                    dot += gcc * (colv[c] - rc);
-                    w.state[S::kR + c][si] = e.alpha * colv[c] + one_m * rc;
+                    gcol += gcc * colv[c];
                 }
-                const float g_alpha = Tb * (dot + ga * Ta);
+                const float g_alpha = Tb * (gcol - Q);
                 const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
                 v[G::kOp] += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
@@ -810,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     v[G::kAx] += fabsf(gmx);
                     v[G::kAy] += fabsf(gmy);
                 }
-                w.state[S::kTa][si] = Ta * one_m;
+                w.state[S::kQ][si] = e.alpha * gcol + one_m * Q;
                 w.state[S::kTc][si] = Tb;
             }
             // 3. this entry's terms into the warp's reduction buffer
