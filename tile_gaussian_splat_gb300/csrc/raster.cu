@@ -42,7 +42,7 @@ namespace {
 #define GS_FWD_MIN_BLOCKS 12
 #endif
 #ifndef GS_BWD_MIN_BLOCKS
-#define GS_BWD_MIN_BLOCKS 10
+#define GS_BWD_MIN_BLOCKS 12
 #endif
 
 constexpr int kTile = 16;
