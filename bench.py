@@ -403,10 +403,15 @@ def run_ours(args, rank, world, scene):
     key_bits = gsb.gs_tile_bits(s.tile_width, s.tile_height) + max(0, (s.C - 1).bit_length())
     up_passes = (key_bits + 7) // 8
     # algorithmic bytes (stated in the design doc): what each stage must read and write
+    # emit+sort: rects + depth histograms (read mean, radii, depth; write a
+    # 16-byte rect) 36 B/splat; depth sort 12 + 3 x 16 B/splat; emission
+    # (order + rect gather) 20 B/splat and an 8-byte key+id per intersection;
+    # camera|tile passes 16 B per intersection each, the last one 24 B (read
+    # 8, write the 12-byte output, gather 4 bytes of depth)
+    tile_pass_bytes = (16 * (up_passes - 1) + 24) if up_passes else 24
     bytes_ = {
         "isect_query": CN * (8 + 8 + 4),
-        "isect_emit_sort": CN * 4 + 4 * CN * 16 + CN * (4 + 8 + 8 + 4) + I * 12
-        + up_passes * I * 24,
+        "isect_emit_sort": CN * (36 + 60 + 20) + I * (8 + tile_pass_bytes),
         "tile_ranges": I * 8 + tiles * 4,
     }
     clk = clocks.summary()

@@ -6,13 +6,19 @@
 // fewer bytes moved:
 //   1. the splats are sorted by the bits of their depth (four 8-bit passes
 //      over C*N 32-bit keys, stable, so equal depths stay in index order);
+//      the pass that histograms their digits also caches every splat's tile
+//      rect, so step 2 gathers 16 bytes per splat in depth order;
 //   2. the intersections are emitted splat by splat in that order, so in
-//      every tile they already appear by (depth bits, splat index);
-//   3. a stable LSD sort on the camera|tile digits of the key's upper word
-//      (ceil((tile_bits + camera bits) / 8) passes over the I keys) then
-//      yields exactly the order of a stable sort of the full keys.
+//      every tile they already appear by (depth bits, splat index); only the
+//      32-bit camera|tile word is written;
+//   3. a stable LSD sort on the camera|tile digits (ceil((tile_bits +
+//      camera bits) / 8) passes over the I 32-bit keys with their ids) then
+//      yields exactly the order of a stable sort of the full keys; the last
+//      pass writes the 64-bit keys, taking each key's low word (the splat's
+//      depth bits) from the depths array.
 // Every key of a splat carries the same depth bits, so its low 32 bits are
-// sorted once per splat instead of once per intersection.
+// sorted once per splat instead of once per intersection, and the radix
+// passes move 8 bytes per intersection instead of 12.
 #include <cstdint>
 #include <cstring>
 
@@ -63,19 +69,20 @@ struct IsectLayout {
     uint32_t* hist_up;       // [4][256]
     uint64_t* lb_emit;       // [chunks]
     uint64_t* lb_depth[4];   // [blocks32 * 256] each
-    uint64_t* lb_up[4];      // [blocks64 * 256] each
+    uint64_t* lb_up[4];      // [blocks32 * 256] each
     size_t zero_end;
     uint32_t* dkeys[2];      // [C*N]
     int32_t* dvals[2];       // [C*N]
-    uint64_t* alt_keys;      // [I]
-    int32_t* alt_ids;        // [I]
+    int4* rects;             // [C*N] tile rects (x0, y0, x1, y1), presort only
+    uint32_t* k32;           // [I] camera|tile keys (sorted path)
+    int32_t* v32;            // [I] their flatten ids
     size_t bytes;
 };
 
 struct IsectPlan {
     int64_t CN;
     int tile_bits, cam_bits, up_passes;
-    bool presort;
+    bool sort, presort;
 };
 
 IsectPlan make_plan(int C, int N, int tw, int th, int64_t n_isects, int sort) {
@@ -84,6 +91,7 @@ IsectPlan make_plan(int C, int N, int tw, int th, int64_t n_isects, int sort) {
     p.tile_bits = gs_tile_bits(tw, th);
     p.cam_bits = bitlen((uint64_t)(C > 0 ? C - 1 : 0));
     p.up_passes = sort ? (p.tile_bits + p.cam_bits + 7) / 8 : 0;
+    p.sort = sort != 0;
     p.presort = sort && n_isects > 1 && p.CN > 1;
     if (n_isects <= 1) p.up_passes = 0;
     return p;
@@ -103,7 +111,7 @@ IsectLayout carve_isect(void* ws, const IsectPlan& p, int64_t n_isects, bool que
             for (int i = 0; i < 4; ++i)
                 L.lb_depth[i] = cv.take<uint64_t>((size_t)sort_blocks(p.CN, kTile32) * 256);
         for (int i = 0; i < p.up_passes; ++i)
-            L.lb_up[i] = cv.take<uint64_t>((size_t)sort_blocks(n_isects, kTile64) * 256);
+            L.lb_up[i] = cv.take<uint64_t>((size_t)sort_blocks(n_isects, kTile32) * 256);
     }
     L.zero_end = cv.used;
     if (!query) {
@@ -112,10 +120,11 @@ IsectLayout carve_isect(void* ws, const IsectPlan& p, int64_t n_isects, bool que
                 L.dkeys[i] = cv.take<uint32_t>((size_t)p.CN);
                 L.dvals[i] = cv.take<int32_t>((size_t)p.CN);
             }
+            L.rects = cv.take<int4>((size_t)p.CN);
         }
-        if (p.up_passes > 0) {
-            L.alt_keys = cv.take<uint64_t>((size_t)n_isects);
-            L.alt_ids = cv.take<int32_t>((size_t)n_isects);
+        if (p.sort) {
+            L.k32 = cv.take<uint32_t>((size_t)n_isects);
+            L.v32 = cv.take<int32_t>((size_t)n_isects);
         }
     }
     L.bytes = cv.used;
@@ -227,11 +236,22 @@ int gs_isect_tiles(const float* means2d, const float* radii, int elliptical, con
         }
         return GS_OK;
     }
+    const uint32_t* dbits = reinterpret_cast<const uint32_t*>(depths);
+    if (!p.sort) {
+        // emission order, 64-bit keys straight into the outputs
+        launch_isect_emit(means2d, radii, elliptical, depths, nullptr, nullptr, p.CN, tile_size,
+                          tile_width, tile_height, N, p.tile_bits, keys, nullptr, flatten_ids,
+                          n_isects, tiles_per_gauss,
+                          LookbackScratch{L.lb_emit, L.tickets + 2 * kMaxPasses}, nullptr, 0,
+                          L.abort_flag, d_status, s);
+        return check_launch();
+    }
     const int32_t* order = nullptr;
     if (p.presort) {
-        // 1. splats by depth bits, four stable passes (values start as indices)
-        const uint32_t* dbits = reinterpret_cast<const uint32_t*>(depths);
-        launch_digit_hist_u32(dbits, p.CN, 0, 32, L.hist_depth, s);
+        // 1. tile rects and depth-digit histograms, then the splats by depth
+        //    bits in four stable passes (values start as indices)
+        launch_rect_hist(means2d, radii, elliptical, dbits, p.CN, tile_size, tile_width,
+                         tile_height, L.rects, L.hist_depth, s);
         const uint32_t* kin = dbits;
         const int32_t* vin = nullptr;
         for (int pass = 0; pass < 4; ++pass) {
@@ -246,28 +266,39 @@ int gs_isect_tiles(const float* means2d, const float* radii, int elliptical, con
         }
         order = vin;
     }
-    // 2. emission (into the buffer that makes the last radix pass land in keys)
-    const bool odd = (p.up_passes & 1) != 0;
-    uint64_t* ek = odd ? L.alt_keys : keys;
-    int32_t* ei = odd ? L.alt_ids : flatten_ids;
-    launch_isect_emit(means2d, radii, elliptical, depths, order, p.CN, tile_size, tile_width,
-                      tile_height, N, p.tile_bits, ek, ei, n_isects, tiles_per_gauss,
+    // 2. emission of 32-bit camera|tile keys.  The passes alternate between
+    //    the workspace pair (k32, v32) and the caller's keys buffer (8 bytes
+    //    per key: 32-bit keys in its first half, ids in its second); the
+    //    start is chosen so that the last pass reads the workspace pair and
+    //    writes the 64-bit keys and the ids.
+    uint32_t* ak = reinterpret_cast<uint32_t*>(keys);
+    int32_t* av = reinterpret_cast<int32_t*>(keys) + n_isects;
+    const bool start_a = p.up_passes > 0 && (p.up_passes & 1) == 0;
+    uint32_t* ck = start_a ? ak : L.k32;
+    int32_t* cv = start_a ? av : L.v32;
+    launch_isect_emit(means2d, radii, elliptical, depths, p.presort ? L.rects : nullptr, order,
+                      p.CN, tile_size, tile_width, tile_height, N, p.tile_bits, nullptr, ck, cv,
+                      n_isects, tiles_per_gauss,
                       LookbackScratch{L.lb_emit, L.tickets + 2 * kMaxPasses},
                       p.up_passes ? L.hist_up : nullptr, p.up_passes, L.abort_flag, d_status, s);
-    // 3. stable passes over the camera|tile digits of the upper word
-    const int end_bit = 32 + p.tile_bits + p.cam_bits;
-    uint64_t* src_k = ek;
-    int32_t* src_i = ei;
+    // 3. stable passes over the camera|tile digits; the last one widens
+    const int end_bit = p.tile_bits + p.cam_bits;
     for (int pass = 0; pass < p.up_passes; ++pass) {
-        uint64_t* dst_k = src_k == keys ? L.alt_keys : keys;
-        int32_t* dst_i = src_i == flatten_ids ? L.alt_ids : flatten_ids;
-        launch_onesweep_u64(src_k, src_i, dst_k, dst_i, n_isects, 32 + 8 * pass, end_bit,
-                            L.hist_up + 256 * pass,
-                            LookbackScratch{L.lb_up[pass], L.tickets + 4 + pass}, L.abort_flag,
-                            d_status, s);
-        src_k = dst_k;
-        src_i = dst_i;
+        const LookbackScratch lb{L.lb_up[pass], L.tickets + 4 + pass};
+        if (pass == p.up_passes - 1) {
+            launch_onesweep_u32_widen(ck, cv, keys, flatten_ids, n_isects, 8 * pass, end_bit,
+                                      L.hist_up + 256 * pass, dbits, lb, L.abort_flag, d_status,
+                                      s);
+        } else {
+            uint32_t* nk = ck == ak ? L.k32 : ak;
+            int32_t* nv = cv == av ? L.v32 : av;
+            launch_onesweep_u32(ck, cv, nk, nv, n_isects, 8 * pass, end_bit,
+                                L.hist_up + 256 * pass, lb, L.abort_flag, d_status, s);
+            ck = nk;
+            cv = nv;
+        }
     }
+    if (p.up_passes == 0) launch_widen(ck, cv, dbits, n_isects, keys, flatten_ids, s);
     return check_launch();
 }
 

@@ -45,6 +45,14 @@ void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32
                          LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
                          cudaStream_t s);
 
+// The same pass over 32-bit keys (with values) whose output keys are the
+// 64-bit key << 32 | wide_low[value].
+void launch_onesweep_u32_widen(const uint32_t* keys_in, const int32_t* vals_in,
+                               uint64_t* keys_out, int32_t* vals_out, int64_t n, int shift,
+                               int end_bit, const uint32_t* hist, const uint32_t* wide_low,
+                               LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                               cudaStream_t s);
+
 // ---- isect.cu
 constexpr int kIsectThreads = 256;
 constexpr int kEmitChunk = 2 * kIsectThreads;  // splats per emit block
@@ -56,12 +64,22 @@ void launch_isect_count(const float* means2d, const float* radii, int elliptical
 // Emits keys/ids for splats in `order` (nullptr = index order) with a
 // decoupled look-back scan of their counts.  up_hist (may be null) receives
 // histograms of the up_passes 8-bit digits of the key's upper word.
+// Tile rects (x0, y0, x1, y1) of every splat, in index order, plus the
+// histograms of the four 8-bit digits of the depth bits (hist [4][256]).
+void launch_rect_hist(const float* means2d, const float* radii, int elliptical,
+                      const uint32_t* dbits, int64_t CN, int tile_size, int tile_width,
+                      int tile_height, int4* rects, uint32_t* hist, cudaStream_t s);
+// keys != null: 64-bit keys; else 32-bit camera|tile keys into keys32.
+// rects may be null (then computed from means2d and radii).
 void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
-                       const float* depths, const int32_t* order, int64_t CN, int tile_size,
-                       int tile_width, int tile_height, int N, int tile_bits, uint64_t* keys,
-                       int32_t* ids, int64_t capacity, int32_t* tiles_per_gauss,
-                       LookbackScratch lb, uint32_t* up_hist, int up_passes,
-                       int32_t* abort_flag, int32_t* d_status, cudaStream_t s);
+                       const float* depths, const int4* rects, const int32_t* order, int64_t CN,
+                       int tile_size, int tile_width, int tile_height, int N, int tile_bits,
+                       uint64_t* keys, uint32_t* keys32, int32_t* ids, int64_t capacity,
+                       int32_t* tiles_per_gauss, LookbackScratch lb, uint32_t* up_hist,
+                       int up_passes, int32_t* abort_flag, int32_t* d_status, cudaStream_t s);
+// keys[i] = k32[i] << 32 | dbits[v32[i]], ids[i] = v32[i].
+void launch_widen(const uint32_t* k32, const int32_t* v32, const uint32_t* dbits, int64_t n,
+                  uint64_t* keys, int32_t* ids, cudaStream_t s);
 
 void launch_tile_ranges(const uint64_t* keys, int64_t n, int C, int tile_width, int tile_height,
                         int tile_bits, int32_t* offsets, int32_t* d_status, cudaStream_t s);

@@ -3,6 +3,11 @@
 //
 //   k_isect_count  one thread per splat: rect, tiles_per_gauss, block sum
 //                  added to the total (size query).
+//   k_rect_hist    one pass over the splats in index order: each splat's
+//                  tile rect into a 16-byte record (so the emission, which
+//                  visits splats in depth order, gathers one sector per splat)
+//                  and the histograms of the four 8-bit digits of the depth
+//                  bits for the depth sort.
 //   k_isect_emit   one thread per splat of a 256-splat chunk taken in ticket
 //                  order; a block scan of the counts plus a decoupled
 //                  look-back over earlier chunks gives each splat's first
@@ -12,6 +17,10 @@
 //                  coalesced whatever the per-splat counts are.  Optionally
 //                  also histograms the 8-bit digits of the key's upper word
 //                  for the radix passes that follow.
+//                  With 32-bit keys (sorted path) it writes only the camera |
+//                  tile word; the depth bits are attached by the last radix
+//                  pass (or k_widen), which reads them from the depths array
+//                  through L2.
 //   k_tile_ranges  one thread per sorted key: where the tile id changes, the
 //                  tiles in between get this key's position.
 #include <cstdint>
@@ -52,11 +61,80 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0 && sum) atomicAdd(total, (unsigned long long)sum);
 }
 
+__global__ void __launch_bounds__(kThreads)
+    k_rect_hist(const float* __restrict__ means2d, const float* __restrict__ radii,
+                int elliptical, const uint32_t* __restrict__ dbits, int64_t CN, float ts,
+                int tile_width, int tile_height, int4* __restrict__ rects,
+                uint32_t* __restrict__ hist) {
+    constexpr int kW = kThreads / kWarp;
+    // one private histogram per warp and digit; a digit shared by the whole
+    // warp (common in the high bits) is added once by lane 0
+    __shared__ uint32_t sh[kW][4][256];
+    for (int i = threadIdx.x; i < kW * 4 * 256; i += kThreads) (&sh[0][0][0])[i] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const int64_t begin = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t rounds = (CN + stride - 1) / stride;  // same trip count in every lane
+    for (int64_t r = 0; r < rounds; ++r) {
+        const int64_t i = begin + r * stride;
+        const bool valid = i < CN;
+        uint32_t key = 0;
+        if (valid) {
+            const float2 m = reinterpret_cast<const float2*>(means2d)[i];
+            float rx, ry;
+            if (elliptical) {
+                const float2 rr = reinterpret_cast<const float2*>(radii)[i];
+                rx = rr.x;
+                ry = rr.y;
+            } else {
+                rx = ry = radii[i];
+            }
+            const Rect rc = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+            rects[i] = make_int4(rc.x0, rc.y0, rc.x1, rc.y1);
+            key = dbits[i];
+        }
+        const bool full = __all_sync(0xffffffffu, valid);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t d = (key >> (8 * p)) & 0xffu;
+            const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+            if (full && __all_sync(0xffffffffu, d == d0)) {
+                if (lane == 0) sh[warp][p][d] += 32u;
+            } else if (valid) {
+                atomicAdd(&sh[warp][p][d], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 256; i += kThreads) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) v += (&sh[w][0][0])[i];
+        if (v) atomicAdd(&hist[i], v);
+    }
+}
+
+// Widens sorted 32-bit camera|tile keys to the 64-bit keys (depth bits from
+// the splat's depth) when no radix pass over them is needed.
+__global__ void __launch_bounds__(kThreads)
+    k_widen(const uint32_t* __restrict__ k32, const int32_t* __restrict__ v32,
+            const uint32_t* __restrict__ dbits, int64_t n, uint64_t* __restrict__ keys,
+            int32_t* __restrict__ ids) {
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        const int32_t v = v32[i];
+        keys[i] = ((uint64_t)k32[i] << 32) | dbits[v];
+        ids[i] = v;
+    }
+}
+
 constexpr int kEmitSplats = kEmitChunk;  // splats per emit block (2 per thread)
 
 struct EmitSmem {
     int32_t incl[kEmitSplats];  // inclusive prefix of counts in the chunk
-    int32_t rect[kEmitSplats];  // x0 | y0 << 16
+    int32_t x0[kEmitSplats];    // rect origin in tiles
+    int32_t y0[kEmitSplats];
     int32_t w[kEmitSplats];     // rect width in tiles
     uint32_t upper[kEmitSplats];  // camera << tile_bits
     uint32_t dbits[kEmitSplats];
@@ -103,11 +181,17 @@ __device__ __forceinline__ int64_t chunk_lookback(uint64_t* lookback, int64_t bl
     return prefix;
 }
 
+// WIDE: 64-bit keys (camera | tile) << 32 | depth bits; else the 32-bit
+// camera | tile word alone (keys32).  rects (may be null): the splats' rects
+// from k_rect_hist, else computed here from means2d and radii.
+template <bool WIDE>
 __global__ void __launch_bounds__(kThreads)
     k_isect_emit(const float* __restrict__ means2d, const float* __restrict__ radii, int elliptical,
-                 const float* __restrict__ depths, const int32_t* __restrict__ order, int64_t CN,
+                 const float* __restrict__ depths, const int4* __restrict__ rects,
+                 const int32_t* __restrict__ order, int64_t CN,
                  float ts, int tile_width, int tile_height, int N, int tile_bits,
-                 uint64_t* __restrict__ keys, int32_t* __restrict__ ids, int64_t capacity,
+                 uint64_t* __restrict__ keys, uint32_t* __restrict__ keys32,
+                 int32_t* __restrict__ ids, int64_t capacity,
                  int32_t* __restrict__ tiles_per_gauss, uint64_t* __restrict__ lookback,
                  uint32_t* __restrict__ ticket, uint32_t* __restrict__ up_hist, int up_passes,
                  ErrorSink err) {
@@ -128,21 +212,28 @@ __global__ void __launch_bounds__(kThreads)
         cnt[u] = 0;
         if (k < CN) {
             const int64_t s = order ? (int64_t)order[k] : k;
-            const float2 m = reinterpret_cast<const float2*>(means2d)[s];
-            float rx, ry;
-            if (elliptical) {
-                const float2 r = reinterpret_cast<const float2*>(radii)[s];
-                rx = r.x;
-                ry = r.y;
+            Rect r;
+            if (rects) {
+                const int4 rc = rects[s];
+                r = Rect{rc.x, rc.y, rc.z, rc.w};
             } else {
-                rx = ry = radii[s];
+                const float2 m = reinterpret_cast<const float2*>(means2d)[s];
+                float rx, ry;
+                if (elliptical) {
+                    const float2 rr = reinterpret_cast<const float2*>(radii)[s];
+                    rx = rr.x;
+                    ry = rr.y;
+                } else {
+                    rx = ry = radii[s];
+                }
+                r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
             }
-            const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
             cnt[u] = (r.x1 - r.x0) * (r.y1 - r.y0);
-            sm.rect[slot] = r.x0 | (r.y0 << 16);
+            sm.x0[slot] = r.x0;
+            sm.y0[slot] = r.y0;
             sm.w[slot] = r.x1 - r.x0;
             sm.upper[slot] = (uint32_t)((uint64_t)(s / N) << tile_bits);
-            sm.dbits[slot] = __float_as_uint(depths[s]);
+            if (WIDE) sm.dbits[slot] = __float_as_uint(depths[s]);
             sm.sid[slot] = (int32_t)s;
             if (tiles_per_gauss) tiles_per_gauss[s] = cnt[u];
         }
@@ -182,13 +273,13 @@ __global__ void __launch_bounds__(kThreads)
             const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
             const int w = sm.w[o];
             const int dy = li / w;
-            const int rc = sm.rect[o];
-            const int ty = (rc >> 16) + dy;
-            const int tx = (rc & 0xffff) + (li - dy * w);
+            const int ty = sm.y0[o] + dy;
+            const int tx = sm.x0[o] + (li - dy * w);
             upper = sm.upper[o] | (uint32_t)(ty * tile_width + tx);
             const int64_t pos = base + q;
             if (pos < capacity) {
-                keys[pos] = ((uint64_t)upper << 32) | sm.dbits[o];
+                if (WIDE) keys[pos] = ((uint64_t)upper << 32) | sm.dbits[o];
+                else keys32[pos] = upper;
                 ids[pos] = sm.sid[o];
             }
         }
@@ -256,18 +347,40 @@ void launch_isect_count(const float* means2d, const float* radii, int elliptical
                                                        tiles_per_gauss, total);
 }
 
+void launch_rect_hist(const float* means2d, const float* radii, int elliptical,
+                      const uint32_t* dbits, int64_t CN, int tile_size, int tile_width,
+                      int tile_height, int4* rects, uint32_t* hist, cudaStream_t s) {
+    if (CN <= 0) return;
+    k_rect_hist<<<grid_for(CN, 4), kThreads, 0, s>>>(means2d, radii, elliptical, dbits, CN,
+                                                     (float)tile_size, tile_width, tile_height,
+                                                     rects, hist);
+}
+
 void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
-                       const float* depths, const int32_t* order, int64_t CN, int tile_size,
-                       int tile_width, int tile_height, int N, int tile_bits, uint64_t* keys,
-                       int32_t* ids, int64_t capacity, int32_t* tiles_per_gauss,
-                       LookbackScratch lb, uint32_t* up_hist, int up_passes,
-                       int32_t* abort_flag, int32_t* d_status, cudaStream_t s) {
+                       const float* depths, const int4* rects, const int32_t* order, int64_t CN,
+                       int tile_size, int tile_width, int tile_height, int N, int tile_bits,
+                       uint64_t* keys, uint32_t* keys32, int32_t* ids, int64_t capacity,
+                       int32_t* tiles_per_gauss, LookbackScratch lb, uint32_t* up_hist,
+                       int up_passes, int32_t* abort_flag, int32_t* d_status, cudaStream_t s) {
     if (CN <= 0) return;
     const int64_t chunks = (CN + kEmitSplats - 1) / kEmitSplats;
-    k_isect_emit<<<(unsigned)chunks, kThreads, 0, s>>>(
-        means2d, radii, elliptical, depths, order, CN, (float)tile_size, tile_width, tile_height,
-        N, tile_bits, keys, ids, capacity, tiles_per_gauss, lb.words, lb.ticket, up_hist,
-        up_passes, ErrorSink{abort_flag, d_status});
+    const ErrorSink err{abort_flag, d_status};
+    if (keys)
+        k_isect_emit<true><<<(unsigned)chunks, kThreads, 0, s>>>(
+            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size, tile_width,
+            tile_height, N, tile_bits, keys, nullptr, ids, capacity, tiles_per_gauss, lb.words,
+            lb.ticket, up_hist, up_passes, err);
+    else
+        k_isect_emit<false><<<(unsigned)chunks, kThreads, 0, s>>>(
+            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size, tile_width,
+            tile_height, N, tile_bits, nullptr, keys32, ids, capacity, tiles_per_gauss,
+            lb.words, lb.ticket, up_hist, up_passes, err);
+}
+
+void launch_widen(const uint32_t* k32, const int32_t* v32, const uint32_t* dbits, int64_t n,
+                  uint64_t* keys, int32_t* ids, cudaStream_t s) {
+    if (n <= 0) return;
+    k_widen<<<grid_for(n, 4), kThreads, 0, s>>>(k32, v32, dbits, n, keys, ids);
 }
 
 void launch_tile_ranges(const uint64_t* keys, int64_t n, int C, int tile_width, int tile_height,

@@ -94,12 +94,16 @@ struct OnesweepSmem {
     uint32_t blk;
 };
 
-template <typename K, int ITEMS, bool IOTA>
+// WIDEN (32-bit keys only): the output key is the 64-bit key_in << 32 |
+// wide_low[value] (into keys_wide instead of keys_out).
+template <typename K, int ITEMS, bool IOTA, bool WIDEN = false>
 __global__ void __launch_bounds__(kThreads, 4)
     k_onesweep(const K* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
                K* __restrict__ keys_out, int32_t* __restrict__ vals_out, int64_t n, int shift,
                uint32_t dmask, const uint32_t* __restrict__ hist, uint64_t* __restrict__ lookback,
-               uint32_t* __restrict__ ticket, ErrorSink err) {
+               uint32_t* __restrict__ ticket, ErrorSink err,
+               uint64_t* __restrict__ keys_wide = nullptr,
+               const uint32_t* __restrict__ wide_low = nullptr) {
     __shared__ OnesweepSmem<K, ITEMS> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) sm.blk = atomicAdd(ticket, 1u);
@@ -124,18 +128,31 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
     }
 
-    // 3. rank within the warp, in element order (i, then lane)
+    // 3. rank within the warp, in element order (i, then lane): for each
+    //    item the lowest lane of every group of equal digits adds the group
+    //    size to the warp's count with one shared atomic, whose old value
+    //    (broadcast to the group) is the group's base.  A warp's atomics on
+    //    one address take effect in issue order, so an item need not wait for
+    //    the previous one: each atomic's result is collected two items later.
     const unsigned lt = lanemask_lt();
+    constexpr int kLag = 2;
+    unsigned peers[ITEMS];
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-        const bool valid = warp_base + i * kWarp + lane < n;
-        const uint32_t d = valid ? digit_of(key[i], shift, dmask) : 0x100u + lane;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        uint32_t before = valid ? sm.warp_count[warp][d] : 0u;
-        __syncwarp();
-        if (valid && (peers & lt) == 0) sm.warp_count[warp][d] = before + __popc(peers);
-        __syncwarp();
-        rank[i] = before + __popc(peers & lt);
+    for (int i = 0; i < ITEMS + kLag; ++i) {
+        if (i < ITEMS) {
+            const bool valid = warp_base + i * kWarp + lane < n;
+            const uint32_t d = valid ? digit_of(key[i], shift, dmask) : 0x100u + lane;
+            peers[i] = __match_any_sync(0xffffffffu, d);
+            uint32_t old = 0;
+            if (valid && (peers[i] & lt) == 0)
+                old = atomicAdd(&sm.warp_count[warp][d], (uint32_t)__popc(peers[i]));
+            rank[i] = old;
+        }
+        if (i >= kLag) {
+            const int j = i - kLag;
+            rank[j] = __shfl_sync(0xffffffffu, rank[j], __ffs(peers[j]) - 1) +
+                      __popc(peers[j] & lt);
+        }
     }
     __syncthreads();
 
@@ -154,14 +171,26 @@ __global__ void __launch_bounds__(kThreads, 4)
     int64_t all;
     const int64_t bucket_start = block_exclusive_scan<kThreads>(hist[d], sm.scratch_a, &all);
 
+    // look back over the predecessors' words for this digit, four per round
+    // trip (nearest first); a word not yet published is waited for
     int64_t excl = 0;
     if (blk > 0) {
-        int64_t p = blk - 1;
-        for (;;) {
-            const uint64_t v = wait_published(lookback + p * 256 + d, err);
-            excl += (int64_t)(v >> 2);
-            if ((v & kFlagMask) == kFlagPrefix || p == 0) break;
-            --p;
+        constexpr int kWin = 4;
+        bool found = false;
+        for (int64_t top = blk - 1; !found; top -= kWin) {
+            uint64_t wv[kWin];
+#pragma unroll
+            for (int u = 0; u < kWin; ++u)
+                wv[u] = top - u >= 0 ? ld_relaxed_u64(lookback + (top - u) * 256 + d) : 0;
+#pragma unroll
+            for (int u = 0; u < kWin; ++u) {
+                if (found) break;
+                const int64_t p = top - u;
+                uint64_t v = wv[u];
+                if ((v & kFlagMask) == 0) v = wait_published(lookback + p * 256 + d, err);
+                excl += (int64_t)(v >> 2);
+                found = (v & kFlagMask) == kFlagPrefix || p == 0;
+            }
         }
         st_relaxed_u64(mine, ((uint64_t)(excl + total) << 2) | kFlagPrefix);
     }
@@ -189,8 +218,10 @@ __global__ void __launch_bounds__(kThreads, 4)
         // in range by construction when the histogram matches the keys; the
         // test only matters after a timed-out wait or an inconsistent input
         if ((uint64_t)o < (uint64_t)n) {
-            keys_out[o] = k;
-            vals_out[o] = sm.vals[j];
+            const int32_t v = sm.vals[j];
+            if (WIDEN) keys_wide[o] = ((uint64_t)k << 32) | wide_low[v];
+            else keys_out[o] = k;
+            vals_out[o] = v;
         } else {
             err.raise(GS_ERR_COUNT_MISMATCH);
         }
@@ -260,6 +291,20 @@ void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32
     else
         k_onesweep<uint32_t, kItems32, true><<<(unsigned)blocks, kThreads, 0, s>>>(
             keys_in, vals_in, keys_out, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err);
+}
+
+void launch_onesweep_u32_widen(const uint32_t* keys_in, const int32_t* vals_in,
+                               uint64_t* keys_out, int32_t* vals_out, int64_t n, int shift,
+                               int end_bit, const uint32_t* hist, const uint32_t* wide_low,
+                               LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
+                               cudaStream_t s) {
+    if (n <= 0) return;
+    const int64_t blocks = sort_blocks(n, kTile32);
+    ErrorSink err{abort_flag, d_status};
+    const uint32_t dm = digit_mask(shift, end_bit);
+    k_onesweep<uint32_t, kItems32, false, true><<<(unsigned)blocks, kThreads, 0, s>>>(
+        keys_in, vals_in, nullptr, vals_out, n, shift, dm, hist, lb.words, lb.ticket, err,
+        keys_out, wide_low);
 }
 
 }  // namespace gs
