@@ -211,15 +211,28 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
     }
     __syncthreads();
+    // unrolled over the thread's (at most ITEMS) slots, so the loads (and the
+    // gathers of the widening pass) of all of them are in flight together
     const int cnt = (int)tile_count;
-    for (int j = tid; j < cnt; j += kThreads) {
+    uint32_t low[ITEMS];
+    if (WIDEN) {
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int j = it * kThreads + tid;
+            low[it] = j < cnt ? wide_low[sm.vals[j]] : 0u;
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * kThreads + tid;
+        if (j >= cnt) break;
         const K k = sm.keys[j];
         const int64_t o = sm.out_base[digit_of(k, shift, dmask)] + j;
         // in range by construction when the histogram matches the keys; the
         // test only matters after a timed-out wait or an inconsistent input
         if ((uint64_t)o < (uint64_t)n) {
             const int32_t v = sm.vals[j];
-            if (WIDEN) keys_wide[o] = ((uint64_t)k << 32) | wide_low[v];
+            if (WIDEN) keys_wide[o] = ((uint64_t)k << 32) | low[it];
             else keys_out[o] = k;
             vals_out[o] = v;
         } else {
