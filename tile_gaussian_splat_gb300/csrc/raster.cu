@@ -29,6 +29,7 @@
 // warp sums the buffer column-wise (one lane per (entry, field)) and adds
 // the sums to the gradients with one atomic each.
 #include <cstdint>
+#include <type_traits>
 
 #include "gs_device.cuh"
 #include "gs_internal.h"
@@ -229,11 +230,12 @@ __device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float m
 // tile, bit = lane.  Word w = warp * kPPT + k covers the pixels of slot k of
 // the threads of warp `warp`.
 constexpr int kTraceWords = kWarps * kPPT;  // 8 -> 256 pixels
+static_assert(kPPT == 4, "a warp's trace words of one entry are one uint4");
 
 template <int BATCH, bool TRACE_IN, bool FAST>
 struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
-    float4 mo[BATCH];   // mx, my, opacity, 1 if the fast form applies else 0
+    float4 mo[BATCH];   // mx, my, opacity, fast form: 0 no, 1 yes, 2 yes without clamp
     float4 q[BATCH];    // a, b, c, -
     float4 qf[FAST ? BATCH : 1];  // fast form: a/2, b, c/2, - (forward only)
     float4 col[BATCH];  // up to 4 channels of the launch's chunk
@@ -334,7 +336,10 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
             bool fast = fast_terms(mo[r].x, mo[r].y, q[r].x, q[r].y, q[r].z, mo[r].z, f);
             fast = fast && fabsf(col.x) < 3.0e38f && fabsf(col.y) < 3.0e38f &&
                    fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
-            st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z, fast ? 1.0f : 0.0f);
+            // 2: fast form, and o <= 0.98 so o exp(-s) (s >= 0) never reaches the
+            // 0.99 clamp, whatever the exponential's 2^-22 rounding
+            st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
+                                     fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f);
             st.q[pos] = q[r];
             if (!REVERSE) st.qf[pos] = f;
             st.col[pos] = col;
@@ -388,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     constexpr int kBatch = kBatchFwd;
     constexpr int kPairs = kPPT / 2;
     __shared__ StageSmem<kBatch, false, true> st;
-    __shared__ uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
+    __shared__ __align__(16) uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
     const TileRange tr = tile_range(a);
     TileBox box[kWarps];
 #pragma unroll
@@ -434,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                 const float4 col = st.col[i];
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 bool took[kPPT];
-                if (mo.w != 0.0f) {  // fast form (warp-uniform): branch-free compositing
+                // fast form (warp-uniform): branch-free compositing
+                auto fast_pairs = [&](auto clamp_tag) {
+                    constexpr bool kClamp = decltype(clamp_tag)::value;
                     const float4 h = st.qf[i];
                     const FastColumn fc = fast_column(mo.x, h, px);
                     const float2 qa2 = splat2(fc.qa2), bdx = splat2(fc.bdx), c2 = splat2(h.z);
@@ -456,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int k = 2 * p + e;
-                            const float alpha = fminf(comp(const_cast<float2&>(raw), e),
-                                                      kAlphaClamp);
+                            const float r_e = comp(const_cast<float2&>(raw), e);
+                            const float alpha = kClamp ? fminf(r_e, kAlphaClamp) : r_e;
                             took[k] = !done[k] && alpha >= a.alpha_cutoff;
                             if (COUNT) n_eval[k] += done[k] ? 0 : 1;
                             // a pair not taken adds exactly 0 (finite colours, T)
@@ -480,6 +487,11 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                                       (took[k] && comp(T[p], e) < a.transmittance_threshold);
                         }
                     }
+                };
+                if (mo.w > 1.5f) {
+                    fast_pairs(std::integral_constant<bool, false>{});
+                } else if (mo.w != 0.0f) {
+                    fast_pairs(std::integral_constant<bool, true>{});
                 } else {  // exact-order form, with the s >= 0 test
                     const float4 q = st.q[i];
                     const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
@@ -511,11 +523,13 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                     }
                 }
                 if (TRACE) {
-#pragma unroll
-                    for (int k = 0; k < kPPT; ++k) {
-                        const unsigned m = __ballot_sync(0xffffffffu, took[k]);
-                        if (lane == k) s_trace[j - b0_32][warp * kPPT + k] = m;
-                    }
+                    // the warp's 4 slot masks, one 16-byte store
+                    const uint4 m4 = make_uint4(__ballot_sync(0xffffffffu, took[0]),
+                                                __ballot_sync(0xffffffffu, took[1]),
+                                                __ballot_sync(0xffffffffu, took[2]),
+                                                __ballot_sync(0xffffffffu, took[3]));
+                    if (lane == 0)
+                        *reinterpret_cast<uint4*>(&s_trace[j - b0_32][warp * kPPT]) = m4;
                 }
                 // leave the batch early once every pixel of the warp has stopped
                 if ((ii & 15) == 15) {
