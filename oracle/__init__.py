@@ -55,6 +55,8 @@ def lib():
                                         P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
                                         F32, P, P]
         L.orc_rasterize_bwd.restype = I32
+        L.orc_bin_splats.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, I64, P, P]
+        L.orc_bin_splats.restype = I64
         L.orc_project.argtypes = [P, P, P, P, I64, I64, I32, I32, F32, F32, F32, F32, I32, P, P,
                                   P, P, P]
         L.orc_project.restype = I32
@@ -264,6 +266,21 @@ def render(scene, sort=True, pixels=None, tie_rel=0.0, tie_rel_T=None):
                         offsets, ids, scene.alpha_cutoff, scene.transmittance_threshold,
                         pixels=pixels, tie_rel=tie_rel, tie_rel_T=tie_rel_T)
     return dict(tiles_per_gauss=tpg, keys=keys, flatten_ids=ids, offsets=offsets), fwd
+
+
+def bin_splats(means2d, radii, depths, tile_size, tile_width, tile_height, capacity):
+    """Fixed-capacity bin lists: (bins int32 (C, TH, TW, M) with -1 after each
+    bin's splats, counts int32 (C, TH, TW), the largest count)."""
+    means2d = _c(means2d, np.float32)
+    radii = _c(radii, np.float32)
+    depths = _c(depths, np.float32)
+    C, N = means2d.shape[:2]
+    bins = np.empty((C, tile_height, tile_width, capacity), np.int32)
+    counts = np.empty((C, tile_height, tile_width), np.int32)
+    largest = lib().orc_bin_splats(_ptr(means2d), _ptr(radii), int(radii.ndim == 3),
+                                   _ptr(depths), C, N, tile_size, tile_width, tile_height,
+                                   capacity, _ptr(bins), _ptr(counts))
+    return bins, counts, int(largest)
 
 
 def project(means, covars, viewmats, intrinsics, width, height, eps2d=0.3, near_plane=0.01,

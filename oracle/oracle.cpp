@@ -19,6 +19,8 @@
 //              gs_raster_backward_pixel, gs_raster_backward_without_gvl.
 //   [G-bridge] gsplat 1.0.0, data/ext/gsplat_native/raster_backward_bridge.c:
 //              gs_raster_backward (argument set, zeroed outputs).
+//   [P3D-fine] pytorch3d rasterize_meshes.cu, RasterizeMeshesFineCudaKernel:
+//              fixed-capacity bin lists with a -1 sentinel (layout only).
 //   [R-train]  rlx-metal 0.2.9, src/splat_training.rs:
 //              training_forward_metal_traced (alpha_cutoff,
 //              transmittance_threshold), alpha_cutoff = 1/255.
@@ -240,6 +242,46 @@ int orc_tile_offsets(const uint64_t* keys, int64_t n, int C, int tile_width, int
         run += counts[t];
     }
     return 0;
+}
+
+// Fixed-capacity bin lists (the bin_faces layout of the pytorch3d fine
+// rasterizer, "pytorch3d rasterize_meshes.cu", RasterizeMeshesFineCudaKernel:
+// (N, BH, BW, M) int32 with -1 as sentinel) holding, per tile, the splats
+// whose rect covers it in compositing order: ascending depth bits, ties by
+// splat index (the order of the stable sort of the 64-bit keys restricted
+// to the tile).  counts[t] = number of covering splats (may exceed M);
+// bins[t][k] for k < min(count, M), -1 after.  Reading: on overflow the bin
+// keeps the first M in that order.  Returns the largest count.
+int64_t orc_bin_splats(const float* means2d, const float* radii, int elliptical,
+                       const float* depths, int64_t C, int64_t N, int tile_size,
+                       int tile_width, int tile_height, int64_t M, int32_t* bins,
+                       int32_t* counts) {
+    const int64_t per_camera = (int64_t)tile_width * tile_height;
+    std::vector<std::vector<int32_t>> lists((size_t)(C * per_camera));
+    for (int64_t c = 0; c < C; ++c)
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t i = c * N + n;
+            Rect r = bounds_of(means2d + 2 * i, radii + (elliptical ? 2 : 1) * i, elliptical,
+                               tile_size, tile_width, tile_height);
+            for (int ty = r.y0; ty < r.y1; ++ty)
+                for (int tx = r.x0; tx < r.x1; ++tx)
+                    lists[(size_t)(c * per_camera + (int64_t)ty * tile_width + tx)].push_back(
+                        (int32_t)i);
+        }
+    int64_t largest = 0;
+    for (size_t t = 0; t < lists.size(); ++t) {
+        std::vector<int32_t>& v = lists[t];
+        // splats were appended in index order; a stable sort by depth bits
+        // keeps equal depths in that order
+        std::stable_sort(v.begin(), v.end(), [&](int32_t x, int32_t y) {
+            return float_bits(depths[x]) < float_bits(depths[y]);
+        });
+        counts[t] = (int32_t)v.size();
+        largest = std::max<int64_t>(largest, (int64_t)v.size());
+        for (int64_t k = 0; k < M; ++k)
+            bins[(int64_t)t * M + k] = k < (int64_t)v.size() ? v[(size_t)k] : -1;
+    }
+    return largest;
 }
 
 // Forward compositing of one pixel (float, as the listings).
