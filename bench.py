@@ -388,6 +388,7 @@ def run_ours(args, rank, world, scene):
         e2e = float(t.item())
 
     proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
+    bins = time_bins(path, max_list, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
 
     if rank != 0:
         return None
@@ -395,6 +396,8 @@ def run_ours(args, rank, world, scene):
     hbm_peak, peak_kind = _peaks()
     proj.update(achieved_gbs=round(proj["bytes"] / (proj["ms"] * 1e-3) / 1e9, 1))
     proj["frac"] = round(proj["achieved_gbs"] / hbm_peak, 4)
+    bins.update(achieved_gbs=round(bins["bytes"] / (bins["ms"] * 1e-3) / 1e9, 1))
+    bins["frac"] = round(bins["achieved_gbs"] / hbm_peak, 4)
     st = stage_ms.mean(axis=0)
     names = ["isect_query", "isect_emit_sort", "tile_ranges", "raster_fwd", "raster_bwd"]
     CN, I = s.C * s.N, path.I
@@ -477,6 +480,7 @@ def run_ours(args, rank, world, scene):
                  "pairs_evaluated_bwd": bwd_eval},
         "roofline": roof,
         "project": proj,
+        "bins": bins,
         "e2e": {"value": round(pixels / (e2e * 1e-3) / 1e6 * world, 2),
                 "unit": "Mpixel/s (pinned host inputs -> image + gradients on host, "
                         "uploads/downloads overlapped with the previous/next step)",
@@ -525,6 +529,41 @@ def time_projection(dev, flush, warmup, steps):
                        "height": s.height, "visible_pairs": visible,
                        "outputs": "radii, means2d, depths, conics, compensations, radii_float",
                        "l2": "flushed between launches"}}
+
+
+def time_bins(path, max_list, flush, warmup, steps):
+    """gs_bin_splats on the step's scene: the fixed-capacity bin lists that
+    can replace emit + sort + ranges (capacity = the longest tile list
+    rounded up to 32), timed alone."""
+    import torch
+
+    s, d, gsb = path.s, path.d, path.gs
+    M = (max_list + 31) // 32 * 32
+    out = (torch.empty((s.C, s.tile_height, s.tile_width, M), dtype=torch.int32, device=path.dev),
+           torch.empty((s.C, s.tile_height, s.tile_width), dtype=torch.int32, device=path.dev))
+    call = lambda: gsb.gs_bin_splats(d["means2d"], d["radii"], d["depths"], s.tile_size,
+                                     s.tile_width, s.tile_height, M, d_status=path.status,
+                                     out=out)
+    for _ in range(warmup):
+        call()
+        flush.zero_()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        call()
+        b.record()
+        flush.zero_()
+    torch.cuda.synchronize()
+    gsb.check_status(path.status, "bins")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    nb = s.C * s.tile_width * s.tile_height
+    # fill: mean + radii per splat, one 4-byte id per intersection; sort: read
+    # the id, gather 4 bytes of depth, write every slot (ids and -1s)
+    return {"kernels": "k_bin_fill, k_bin_sort", "ms": round(ms, 4), "capacity": M,
+            "bytes": s.C * s.N * 16 + path.I * (4 + 4 + 4) + nb * M * 4,
+            "note": "alternative to emit + sort + ranges; not part of the step"}
 
 
 # -------------------------------------------------------- oracle arm

@@ -16,6 +16,8 @@
  *       gs_offset_encode
  *   gsplat 1.0.0, data/ext/gsplat_native/projection.c: gs_project_one,
  *       gs_projection_forward
+ *   pytorch3d rasterize_meshes.cu, RasterizeMeshesFineCudaKernel: the
+ *       fixed-capacity bin layout of gs_bin_splats
  *   gsplat 1.0.0, data/ext/gsplat_native/raster_backward.c and
  *       raster_backward_bridge.c: gs_raster_backward_pixel,
  *       gs_raster_backward_without_gvl, gs_raster_backward
@@ -171,6 +173,66 @@ int gs_project(const float* means, const float* covars, const float* viewmats,
                int orthographic, int32_t* radii, float* means2d, float* depths,
                float* conics, float* compensations, float* radii_float,
                int32_t* d_status, void* stream);
+
+/* Largest capacity (slots per bin) of the bin-list calls. */
+#define GS_BIN_MAX_CAPACITY 16384
+
+/*
+ * gs_bin_splats -- fixed-capacity per-tile bin lists, the bin_faces layout
+ * of the pytorch3d fine rasterizer (rasterize_meshes.cu,
+ * RasterizeMeshesFineCudaKernel: (N, BH, BW, M) int32, -1 as sentinel),
+ * holding for every tile the splats whose rect covers it (the rect of
+ * gs_isect_tiles) in compositing order: ascending depth bits, ties by splat
+ * index -- exactly the tile's slice of gs_isect_tiles' sorted flatten_ids,
+ * without a global sort.
+ * Inputs: as gs_isect_tiles (means2d, radii, elliptical, depths, C, N,
+ *   tile_size, tile grid); capacity M in [1, GS_BIN_MAX_CAPACITY] with
+ *   C * TH * TW * M < 2^31.
+ * Outputs (device): bins int32 (C, TH, TW, M): bin t's splats (flatten ids
+ *   c*N + n) in slots [0, min(count, M)), -1 after; bin_counts int32
+ *   (C, TH, TW): the number of splats covering each tile (zeroed by this
+ *   call; may exceed M).  A bin with more than M splats reports
+ *   GS_ERR_CAPACITY to d_status and then holds M of them, which ones being
+ *   unspecified; retry with M >= the largest count.
+ * Asynchronous; needs no workspace.
+ */
+int gs_bin_splats(const float* means2d, const float* radii, int elliptical,
+                  const float* depths, int C, int N, int tile_size,
+                  int tile_width, int tile_height, int capacity, int32_t* bins,
+                  int32_t* bin_counts, int32_t* d_status, void* stream);
+
+/*
+ * gs_rasterize_fwd_bins / gs_rasterize_bwd_bins -- gs_rasterize_fwd and
+ * gs_rasterize_bwd over bin lists instead of (offsets, flatten_ids): tile
+ * t's list is bins[t, 0 .. min(bin_counts[t], capacity)).  List positions
+ * (last_ids, trace rows) are positions in the bins array, t * capacity + k;
+ * the optional trace has C * TH * TW * capacity rows of 8 words.  Everything
+ * else (arguments, outputs, errors) as the sorted-list calls.
+ */
+int gs_rasterize_fwd_bins(const float* means2d, const float* conics,
+                          const float* colors, const float* opacities,
+                          const float* backgrounds, const int32_t* masks,
+                          int C, int N, int channels, int width, int height,
+                          int tile_size, const int32_t* bins,
+                          const int32_t* bin_counts, int capacity,
+                          float alpha_cutoff, float transmittance_threshold,
+                          float* render_colors, float* render_alphas,
+                          int32_t* last_ids, int32_t* pair_counts,
+                          uint32_t* trace, int32_t* d_status, void* stream);
+int gs_rasterize_bwd_bins(const float* means2d, const float* conics,
+                          const float* colors, const float* opacities,
+                          const float* backgrounds, const int32_t* masks,
+                          int C, int N, int channels, int width, int height,
+                          int tile_size, const int32_t* bins,
+                          const int32_t* bin_counts, int capacity,
+                          float alpha_cutoff, const float* render_alphas,
+                          const int32_t* last_ids,
+                          const float* grad_render_colors,
+                          const float* grad_render_alphas, float* grad_means2d,
+                          float* grad_conics, float* grad_colors,
+                          float* grad_opacities, float* grad_backgrounds,
+                          float* grad_means2d_abs, const uint32_t* trace,
+                          int32_t* d_status, void* stream);
 
 /* Largest channel count the rasterizer accepts. */
 #define GS_MAX_CHANNELS 1024

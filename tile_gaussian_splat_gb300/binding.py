@@ -40,6 +40,11 @@ SIGNATURES = {
                                P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "gs_project": (I32, [P, P, P, P, I32, I32, I32, I32, F32, F32, F32, F32, I32, P, P, P, P, P,
                          P, P, P]),
+    "gs_bin_splats": (I32, [P, P, I32, P, I32, I32, I32, I32, I32, I32, P, P, P, P]),
+    "gs_rasterize_fwd_bins": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I32,
+                                    F32, F32, P, P, P, P, P, P, P]),
+    "gs_rasterize_bwd_bins": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I32,
+                                    F32, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "gs_sort_workspace_size": (SZ, [I64]),
     "gs_sort_pairs": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
     "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
@@ -191,6 +196,23 @@ def gs_project(means, covars, viewmats, intrinsics, width, height, eps2d=0.3, ne
     return out
 
 
+def gs_bin_splats(means2d, radii, depths, tile_size, tile_width, tile_height, capacity,
+                  d_status=None, out=None, stream=None):
+    """Returns (bins int32 (C, TH, TW, capacity) with -1 after each bin's
+    splats, bin_counts int32 (C, TH, TW))."""
+    C, N = means2d.shape[:2]
+    dev = means2d.device
+    if out is None:
+        out = (_empty((C, tile_height, tile_width, capacity), torch.int32, dev),
+               _empty((C, tile_height, tile_width), torch.int32, dev))
+    bins, counts = out
+    _check(lib().gs_bin_splats(
+        _ptr(means2d), _ptr(radii), int(radii.dim() == 3), _ptr(depths), C, N, tile_size,
+        tile_width, tile_height, int(capacity), _ptr(bins), _ptr(counts), _ptr(d_status),
+        _stream(stream)), "gs_bin_splats")
+    return bins, counts
+
+
 def gs_rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                      tile_size, offsets, flatten_ids, alpha_cutoff, transmittance_threshold,
                      d_status=None, out=None, pair_counts=None, trace=None, stream=None):
@@ -271,3 +293,54 @@ def gs_sort_pairs_noalloc(keys, values, begin_bit=0, end_bit=64, d_status=None, 
                                        end_bit, _ptr(d_status), _stream(stream)),
            "gs_sort_pairs_noalloc")
     return keys, values
+
+
+def gs_rasterize_fwd_bins(means2d, conics, colors, opacities, backgrounds, masks, width, height,
+                          tile_size, bins, bin_counts, alpha_cutoff, transmittance_threshold,
+                          d_status=None, out=None, pair_counts=None, trace=None, stream=None):
+    """gs_rasterize_fwd over bin lists (bins (C, TH, TW, M), bin_counts).
+    last_ids and trace rows are positions in bins."""
+    C, N = means2d.shape[:2]
+    ch = colors.shape[-1]
+    dev = means2d.device
+    if out is None:
+        out = (_empty((C, height, width, ch), torch.float32, dev),
+               _empty((C, height, width, 1), torch.float32, dev),
+               _empty((C, height, width), torch.int32, dev))
+    rgb, alpha, last = out
+    _check(lib().gs_rasterize_fwd_bins(
+        _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
+        _ptr(masks), C, N, ch, width, height, tile_size, _ptr(bins), _ptr(bin_counts),
+        bins.shape[-1], float(alpha_cutoff), float(transmittance_threshold), _ptr(rgb),
+        _ptr(alpha), _ptr(last), _ptr(pair_counts), _ptr(trace), _ptr(d_status),
+        _stream(stream)), "gs_rasterize_fwd_bins")
+    return rgb, alpha, last
+
+
+def gs_rasterize_bwd_bins(means2d, conics, colors, opacities, backgrounds, masks, width, height,
+                          tile_size, bins, bin_counts, alpha_cutoff, render_alphas, last_ids,
+                          grad_render_colors, grad_render_alphas, want_grad_backgrounds=None,
+                          absgrad=False, d_status=None, out=None, trace=None, stream=None):
+    """gs_rasterize_bwd over bin lists; same outputs as gs_rasterize_bwd."""
+    C, N = means2d.shape[:2]
+    ch = colors.shape[-1]
+    dev = means2d.device
+    if want_grad_backgrounds is None:
+        want_grad_backgrounds = backgrounds is not None
+    if out is None:
+        out = dict(grad_means2d=_empty((C, N, 2), torch.float32, dev),
+                   grad_conics=_empty((C, N, 3), torch.float32, dev),
+                   grad_colors=_empty((C, N, ch), torch.float32, dev),
+                   grad_opacities=_empty((C, N), torch.float32, dev),
+                   grad_backgrounds=_empty((C, ch), torch.float32, dev)
+                   if want_grad_backgrounds else None,
+                   grad_means2d_abs=_empty((C, N, 2), torch.float32, dev) if absgrad else None)
+    _check(lib().gs_rasterize_bwd_bins(
+        _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
+        _ptr(masks), C, N, ch, width, height, tile_size, _ptr(bins), _ptr(bin_counts),
+        bins.shape[-1], float(alpha_cutoff), _ptr(render_alphas), _ptr(last_ids),
+        _ptr(grad_render_colors), _ptr(grad_render_alphas), _ptr(out["grad_means2d"]),
+        _ptr(out["grad_conics"]), _ptr(out["grad_colors"]), _ptr(out["grad_opacities"]),
+        _ptr(out["grad_backgrounds"]), _ptr(out["grad_means2d_abs"]), _ptr(trace),
+        _ptr(d_status), _stream(stream)), "gs_rasterize_bwd_bins")
+    return out

@@ -319,41 +319,40 @@ int gs_tile_offsets(const uint64_t* keys, int64_t n_isects, int C, int tile_widt
     return check_launch();
 }
 
-int gs_rasterize_fwd(const float* means2d, const float* conics, const float* colors,
-                     const float* opacities, const float* backgrounds, const int32_t* masks,
-                     int C, int N, int channels, int width, int height, int tile_size,
-                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
-                     float alpha_cutoff, float transmittance_threshold, float* render_colors,
-                     float* render_alphas, int32_t* last_ids, int32_t* pair_counts,
-                     uint32_t* trace, int32_t* d_status, void* stream) {
-    (void)d_status;
-    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
-                        tile_size, offsets, flatten_ids, n_isects))
-        return GS_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// The raster calls over either list form: sorted lists (offsets != null,
+// flatten_ids of length n_isects) or bin lists (bin_counts != null,
+// flatten_ids = the bins, n_isects = tiles * bin_capacity).
+int raster_fwd(const float* means2d, const float* conics, const float* colors,
+               const float* opacities, const float* backgrounds, const int32_t* masks, int C,
+               int N, int channels, int width, int height, const int32_t* offsets,
+               const int32_t* bin_counts, int bin_capacity, const int32_t* flatten_ids,
+               int64_t n_isects, float alpha_cutoff, float transmittance_threshold,
+               float* render_colors, float* render_alphas, int32_t* last_ids,
+               int32_t* pair_counts, uint32_t* trace, void* stream) {
     if (!render_colors || !render_alphas || !last_ids) return GS_ERR_INVALID_ARG;
+    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
                  offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold,
-                 channels, 0, 1};
-    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
+                 channels, 0, 1, bin_counts, bin_capacity};
     launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts, trace,
                       static_cast<cudaStream_t>(stream));
     return check_launch();
 }
 
-int gs_rasterize_bwd(const float* means2d, const float* conics, const float* colors,
-                     const float* opacities, const float* backgrounds, const int32_t* masks,
-                     int C, int N, int channels, int width, int height, int tile_size,
-                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
-                     float alpha_cutoff, const float* render_alphas, const int32_t* last_ids,
-                     const float* grad_render_colors, const float* grad_render_alphas,
-                     float* grad_means2d, float* grad_conics, float* grad_colors,
-                     float* grad_opacities, float* grad_backgrounds, float* grad_means2d_abs,
-                     const uint32_t* trace, int32_t* d_status, void* stream) {
-    (void)d_status;
-    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
-                        tile_size, offsets, flatten_ids, n_isects))
-        return GS_ERR_INVALID_ARG;
+int raster_bwd(const float* means2d, const float* conics, const float* colors,
+               const float* opacities, const float* backgrounds, const int32_t* masks, int C,
+               int N, int channels, int width, int height, const int32_t* offsets,
+               const int32_t* bin_counts, int bin_capacity, const int32_t* flatten_ids,
+               int64_t n_isects, float alpha_cutoff, const float* render_alphas,
+               const int32_t* last_ids, const float* grad_render_colors,
+               const float* grad_render_alphas, float* grad_means2d, float* grad_conics,
+               float* grad_colors, float* grad_opacities, float* grad_backgrounds,
+               float* grad_means2d_abs, const uint32_t* trace, void* stream) {
     if (!render_alphas || !last_ids || !grad_render_colors || !grad_render_alphas)
         return GS_ERR_INVALID_ARG;
     const int64_t CN = (int64_t)C * N;
@@ -362,6 +361,7 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
     if (grad_backgrounds && !backgrounds) return GS_ERR_INVALID_ARG;
     // |.| of a sum over channels is not the sum over channel chunks of |.|
     if (grad_means2d_abs && channels > 4) return GS_ERR_INVALID_ARG;
+    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t f = sizeof(float);
     if (CN > 0) {
@@ -377,13 +377,127 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
         return GS_ERR_CUDA;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
-                 offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f, channels, 0, 1};
+                 offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f, channels, 0, 1,
+                 bin_counts, bin_capacity};
     RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                   grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                   grad_means2d_abs};
-    if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     launch_raster_bwd(a, g, trace, s);
     return check_launch();
+}
+
+// Bin form: capacity in [1, kMaxBinCapacity], positions tiles * capacity
+// below 2^31 (last_ids are positions into the bins).
+int bin_args_ok(int C, int width, int height, int tile_size, int capacity, const int32_t* bins,
+                const int32_t* counts, int64_t* n_slots) {
+    if (C < 1 || width < 1 || height < 1 || tile_size < 1) return 0;
+    if (capacity < 1 || capacity > kMaxBinCapacity || !bins || !counts) return 0;
+    const int64_t tw = (width + tile_size - 1) / tile_size, th = (height + tile_size - 1) / tile_size;
+    *n_slots = (int64_t)C * tw * th * capacity;
+    return *n_slots < ((int64_t)1 << 31);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gs_rasterize_fwd(const float* means2d, const float* conics, const float* colors,
+                     const float* opacities, const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height, int tile_size,
+                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, float transmittance_threshold, float* render_colors,
+                     float* render_alphas, int32_t* last_ids, int32_t* pair_counts,
+                     uint32_t* trace, int32_t* d_status, void* stream) {
+    (void)d_status;
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects))
+        return GS_ERR_INVALID_ARG;
+    return raster_fwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
+                      transmittance_threshold, render_colors, render_alphas, last_ids,
+                      pair_counts, trace, stream);
+}
+
+int gs_rasterize_bwd(const float* means2d, const float* conics, const float* colors,
+                     const float* opacities, const float* backgrounds, const int32_t* masks,
+                     int C, int N, int channels, int width, int height, int tile_size,
+                     const int32_t* offsets, const int32_t* flatten_ids, int64_t n_isects,
+                     float alpha_cutoff, const float* render_alphas, const int32_t* last_ids,
+                     const float* grad_render_colors, const float* grad_render_alphas,
+                     float* grad_means2d, float* grad_conics, float* grad_colors,
+                     float* grad_opacities, float* grad_backgrounds, float* grad_means2d_abs,
+                     const uint32_t* trace, int32_t* d_status, void* stream) {
+    (void)d_status;
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects))
+        return GS_ERR_INVALID_ARG;
+    return raster_bwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
+                      render_alphas, last_ids, grad_render_colors, grad_render_alphas,
+                      grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
+                      grad_means2d_abs, trace, stream);
+}
+
+int gs_bin_splats(const float* means2d, const float* radii, int elliptical, const float* depths,
+                  int C, int N, int tile_size, int tile_width, int tile_height, int capacity,
+                  int32_t* bins, int32_t* bin_counts, int32_t* d_status, void* stream) {
+    if (!isect_args_ok(means2d, radii, C, N, tile_size, tile_width, tile_height))
+        return GS_ERR_INVALID_ARG;
+    if (capacity < 1 || capacity > kMaxBinCapacity || !bins || !bin_counts) return GS_ERR_INVALID_ARG;
+    const int64_t nbins = (int64_t)C * tile_width * tile_height;
+    if (nbins * capacity >= ((int64_t)1 << 31)) return GS_ERR_INVALID_ARG;
+    if ((int64_t)C * N > 0 && !depths) return GS_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(bin_counts, 0, (size_t)nbins * sizeof(int32_t), s) != cudaSuccess)
+        return GS_ERR_CUDA;
+    const int rc = launch_bin_splats(means2d, radii, elliptical, depths, C, N, tile_size,
+                                     tile_width, tile_height, capacity, bins, bin_counts,
+                                     d_status, s);
+    if (rc != GS_OK) return rc;
+    return check_launch();
+}
+
+int gs_rasterize_fwd_bins(const float* means2d, const float* conics, const float* colors,
+                          const float* opacities, const float* backgrounds, const int32_t* masks,
+                          int C, int N, int channels, int width, int height, int tile_size,
+                          const int32_t* bins, const int32_t* bin_counts, int capacity,
+                          float alpha_cutoff, float transmittance_threshold,
+                          float* render_colors, float* render_alphas, int32_t* last_ids,
+                          int32_t* pair_counts, uint32_t* trace, int32_t* d_status,
+                          void* stream) {
+    (void)d_status;
+    int64_t n_slots = 0;
+    if (!bin_args_ok(C, width, height, tile_size, capacity, bins, bin_counts, &n_slots) ||
+        !raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, bin_counts, bins, n_slots))
+        return GS_ERR_INVALID_ARG;
+    return raster_fwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, nullptr, bin_counts, capacity, bins, n_slots, alpha_cutoff,
+                      transmittance_threshold, render_colors, render_alphas, last_ids,
+                      pair_counts, trace, stream);
+}
+
+int gs_rasterize_bwd_bins(const float* means2d, const float* conics, const float* colors,
+                          const float* opacities, const float* backgrounds, const int32_t* masks,
+                          int C, int N, int channels, int width, int height, int tile_size,
+                          const int32_t* bins, const int32_t* bin_counts, int capacity,
+                          float alpha_cutoff, const float* render_alphas,
+                          const int32_t* last_ids, const float* grad_render_colors,
+                          const float* grad_render_alphas, float* grad_means2d,
+                          float* grad_conics, float* grad_colors, float* grad_opacities,
+                          float* grad_backgrounds, float* grad_means2d_abs,
+                          const uint32_t* trace, int32_t* d_status, void* stream) {
+    (void)d_status;
+    int64_t n_slots = 0;
+    if (!bin_args_ok(C, width, height, tile_size, capacity, bins, bin_counts, &n_slots) ||
+        !raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, bin_counts, bins, n_slots))
+        return GS_ERR_INVALID_ARG;
+    return raster_bwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, nullptr, bin_counts, capacity, bins, n_slots, alpha_cutoff,
+                      render_alphas, last_ids, grad_render_colors, grad_render_alphas,
+                      grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
+                      grad_means2d_abs, trace, stream);
 }
 
 int gs_project(const float* means, const float* covars, const float* viewmats,

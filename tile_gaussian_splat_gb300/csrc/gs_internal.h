@@ -103,6 +103,10 @@ struct RasterArgs {
     int channels, ch_off;
     int first_chunk;  // forward: writes alphas, last ids, counts, trace;
                       // backward: adds the render_alpha gradient's terms
+    // bin lists instead of offsets (offsets == nullptr): tile t's list is
+    // flatten_ids[t * bin_capacity, + min(bin_counts[t], bin_capacity))
+    const int32_t* bin_counts;
+    int bin_capacity;
 };
 
 // trace (may be null): per list entry 8 words, the tile pixels that composited it.
@@ -138,5 +142,15 @@ void launch_project(const float* means, const float* covars, const float* viewma
                     const float* intrinsics, int C, int N, const ProjectArgs& pa, int32_t* radii,
                     float* means2d, float* depths, float* conics, float* compensations,
                     float* radii_float, cudaStream_t s);
+
+// ---- bins.cu
+// Largest bin capacity (the bin sort holds a bin's keys in shared memory).
+constexpr int kMaxBinCapacity = 16384;
+// Fills bins (C*TH*TW, capacity) and counts (zeroed by the caller); reports
+// GS_ERR_CAPACITY to d_status for a bin with more splats than capacity.
+int launch_bin_splats(const float* means2d, const float* radii, int elliptical,
+                      const float* depths, int C, int N, int tile_size, int tile_width,
+                      int tile_height, int capacity, int32_t* bins, int32_t* counts,
+                      int32_t* d_status, cudaStream_t s);
 
 }  // namespace gs

@@ -153,8 +153,14 @@ __device__ __forceinline__ TileRange tile_range(const RasterArgs& a) {
     r.ty = local / a.tile_width;
     r.tx = local - r.ty * a.tile_width;
     const int64_t ntiles = (int64_t)a.C * per_camera;
-    r.start = a.offsets[r.tile];
-    r.end = r.tile + 1 < ntiles ? (int64_t)a.offsets[r.tile + 1] : a.n_isects;
+    if (a.bin_counts) {
+        const int n = a.bin_counts[r.tile];
+        r.start = r.tile * a.bin_capacity;
+        r.end = r.start + (n < 0 ? 0 : (n > a.bin_capacity ? a.bin_capacity : n));
+    } else {
+        r.start = a.offsets[r.tile];
+        r.end = r.tile + 1 < ntiles ? (int64_t)a.offsets[r.tile + 1] : a.n_isects;
+    }
     // offsets from gs_tile_offsets are always inside [0, n_isects]; clamping
     // keeps a corrupted table from reading outside flatten_ids
     r.end = r.end < 0 ? 0 : (r.end > a.n_isects ? a.n_isects : r.end);
