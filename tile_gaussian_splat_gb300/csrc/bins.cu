@@ -11,9 +11,10 @@
 //               the tile's counter.  The order inside a bin is the order the
 //               atomics happened to take.
 //   k_bin_sort  one block per bin: its entries, keyed (depth bits << 32 |
-//               splat index), are sorted in shared memory by a bitonic
-//               network, written back in order and followed by -1s.  The
-//               result does not depend on the append order.
+//               splat index), are sorted by a bitonic network (short strides
+//               in registers with warp shuffles, long ones in shared memory),
+//               written back in order and followed by -1s.  The result does
+//               not depend on the append order.
 #include <cstdint>
 
 #include "gs_device.cuh"
@@ -94,21 +95,59 @@ __global__ void __launch_bounds__(kFillThreads)
     }
 }
 
-// Bitonic sort of a bin's keys in shared memory; n2 = next power of two of
-// the bin's entry count, padded with all-ones keys that sort last.
+// One compare-exchange of a bitonic stage between lanes: element i (this
+// lane's) and i ^ stride (lane ^ stride, stride < 32) of a 64-element chunk;
+// ascending where bit `size` of i is clear.
+__device__ __forceinline__ uint64_t cas_lanes(uint64_t x, int i, int size, int stride, int lane) {
+    const uint64_t y = ((uint64_t)__shfl_xor_sync(0xffffffffu, (uint32_t)(x >> 32), stride) << 32) |
+                       __shfl_xor_sync(0xffffffffu, (uint32_t)x, stride);
+    const bool asc = (i & size) == 0;
+    const bool lower = (lane & stride) == 0;
+    const uint64_t lo = x < y ? x : y, hi = x < y ? y : x;
+    return lower == asc ? lo : hi;
+}
+
+// Strides 32 .. 1 of bitonic level `size` (or all levels up to 64 when
+// full) on a 64-element chunk held as x0 = element lane, x1 = element
+// lane + 32.
+__device__ __forceinline__ void chunk_stages(uint64_t& x0, uint64_t& x1, int base, int size_lo,
+                                             int size_hi, int lane) {
+    for (int size = size_lo; size <= size_hi; size <<= 1) {
+        for (int stride = (size < 64 ? size : 64) >> 1; stride > 0; stride >>= 1) {
+            if (stride == 32) {
+                const bool asc = ((base + lane) & size) == 0;
+                if ((x0 > x1) == asc) {
+                    const uint64_t t = x0;
+                    x0 = x1;
+                    x1 = t;
+                }
+            } else {
+                x0 = cas_lanes(x0, base + lane, size, stride, lane);
+                x1 = cas_lanes(x1, base + lane + 32, size, stride, lane);
+            }
+        }
+    }
+}
+
+// Bitonic sort of a bin's keys in shared memory over n2 = the next power of
+// two (at least 64) of the bin's entry count, padded with all-ones keys that
+// sort last.  Strides below 64 run in registers with warp shuffles on
+// 64-element chunks; only the longer strides go through shared memory with
+// a block barrier.
 __global__ void __launch_bounds__(kBinSortThreads)
     k_bin_sort(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
                int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
                int32_t* d_status) {
     extern __shared__ uint64_t keys[];
+    constexpr int kW = kBinSortThreads / kWarp;
     const int64_t b = blockIdx.x;
     if (b >= nbins) return;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int total = counts[b];
     if (total > capacity && tid == 0) report(d_status, GS_ERR_CAPACITY);
     const int cnt = total < capacity ? total : capacity;
     int32_t* bin = bins + b * capacity;
-    int n2 = 1;
+    int n2 = 64;
     while (n2 < cnt) n2 <<= 1;
     if (cnt > 1) {
         for (int k = tid; k < n2; k += kBinSortThreads) {
@@ -121,9 +160,9 @@ __global__ void __launch_bounds__(kBinSortThreads)
         }
         __syncthreads();
         for (int size = 2; size <= n2; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            // shared-memory stages of this level (strides >= 64)
+            for (int stride = size >> 1; stride >= 64; stride >>= 1) {
                 for (int p = tid; p < (n2 >> 1); p += kBinSortThreads) {
-                    // p-th compare-exchange of this stage: elements lo < hi
                     const int lo = ((p / stride) * 2 * stride) + (p % stride);
                     const int hi = lo + stride;
                     const bool ascending = (lo & size) == 0;
@@ -135,6 +174,16 @@ __global__ void __launch_bounds__(kBinSortThreads)
                 }
                 __syncthreads();
             }
+            // the rest in registers: all levels up to 64 at once, then per level
+            const int size_lo = size <= 64 ? 2 : size, size_hi = size <= 64 ? 64 : size;
+            for (int c = warp; c < n2 / 64; c += kW) {
+                uint64_t x0 = keys[c * 64 + lane], x1 = keys[c * 64 + lane + 32];
+                chunk_stages(x0, x1, c * 64, size_lo, size_hi, lane);
+                keys[c * 64 + lane] = x0;
+                keys[c * 64 + lane + 32] = x1;
+            }
+            __syncthreads();
+            if (size < 64) size = 64;  // levels 2..64 are done
         }
         for (int k = tid; k < cnt; k += kBinSortThreads) bin[k] = (int32_t)(uint32_t)keys[k];
     }
@@ -144,7 +193,7 @@ __global__ void __launch_bounds__(kBinSortThreads)
 }  // namespace
 
 int bin_sort_smem_bytes(int capacity) {
-    int n2 = 1;
+    int n2 = 64;
     while (n2 < capacity) n2 <<= 1;
     return n2 * (int)sizeof(uint64_t);
 }
