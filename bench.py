@@ -318,6 +318,26 @@ def _traffic_for(kernel, launches_per_step):
     return e.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(x, world, dev):
+    """The largest x over the replicas (each rank passes its own); x itself
+    when there is one rank.  dev: where the reduction tensor lives (the GPU
+    with NCCL, the CPU with gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, ms, world):
+    """Units per second of all replicas together over the slowest rank's time
+    (weak scaling: every rank processes units_per_rank)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, scene):
     import torch
     import torch.distributed as dist
@@ -372,20 +392,12 @@ def run_ours(args, rank, world, scene):
     stage_ms = np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(5)]
                          for k in range(args.steps)])
     step_ms = stage_ms.sum(axis=1)
-    ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(step_ms.mean()), world, dev)
 
     # end to end through host buffers (pipelined: see Path.run_e2e)
     h2d, d2h = path.setup_e2e()
     path.run_e2e(3)
-    e2e = path.run_e2e(max(5, min(args.steps, 20)))
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(path.run_e2e(max(5, min(args.steps, 20))), world, dev)
 
     proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
     bins = time_bins(path, max_list, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
@@ -453,7 +465,7 @@ def run_ours(args, rank, world, scene):
         roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["achieved_gbs"],
                 "peak": hbm_peak, "unit": "GB/s", "frac": stages[dom]["frac"],
                 "traffic": traffic, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
-    value = pixels / (ms * 1e-3) / 1e6 * world
+    value = whole_job_rate(pixels, ms, world) / 1e6
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -481,7 +493,7 @@ def run_ours(args, rank, world, scene):
         "roofline": roof,
         "project": proj,
         "bins": bins,
-        "e2e": {"value": round(pixels / (e2e * 1e-3) / 1e6 * world, 2),
+        "e2e": {"value": round(whole_job_rate(pixels, e2e, world) / 1e6, 2),
                 "unit": "Mpixel/s (pinned host inputs -> image + gradients on host, "
                         "uploads/downloads overlapped with the previous/next step)",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
