@@ -241,12 +241,13 @@ static_assert(kPPT == 4, "a warp's trace words of one entry are one uint4");
 template <int BATCH, bool TRACE_IN, bool FAST>
 struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
-    float4 mo[BATCH];   // mx, my, opacity, fast form: 0 no, 1 yes, 2 yes without clamp
-    float4 q[BATCH];    // a, b, c, -
+    float4 mo[BATCH];   // mx, my, opacity, forward: fast form (0 no, 1 yes, 2 yes
+                        // without clamp); backward: list position (int bits)
+    float4 q[BATCH];    // a, b, c, backward: flatten id (int bits)
     float4 qf[FAST ? BATCH : 1];  // fast form: a/2, b, c/2, - (forward only)
     float4 col[BATCH];  // up to 4 channels of the launch's chunk
-    int32_t gid[BATCH];
-    int32_t j[BATCH];   // list position
+    int32_t j[FAST ? BATCH : 1];  // list position (forward; the backward keeps it
+                                  // in mo.w and the flatten id in q.w)
     uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
     uint8_t idx[kWarps][BATCH];  // per warp: staged slots that can reach its pixels
     int32_t nw[kWarps];          // per warp: length of idx
@@ -344,13 +345,18 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
                    fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
             // 2: fast form, and o <= 0.98 so o exp(-s) (s >= 0) never reaches the
             // 0.99 clamp, whatever the exponential's 2^-22 rounding
-            st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
-                                     fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f);
-            st.q[pos] = q[r];
-            if (!REVERSE) st.qf[pos] = f;
+            if (!REVERSE) {
+                st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
+                                         fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f);
+                st.q[pos] = q[r];
+                st.qf[pos] = f;
+                st.j[pos] = (int32_t)jj[r];
+            } else {
+                st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
+                                         __int_as_float((int32_t)jj[r]));
+                st.q[pos] = make_float4(q[r].x, q[r].y, q[r].z, __int_as_float(gid[r]));
+            }
             st.col[pos] = col;
-            st.gid[pos] = gid[r];
-            st.j[pos] = (int32_t)jj[r];
             if (TRACE_IN) {
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = tw[r][w];
@@ -581,11 +587,12 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 
 // ----------------------------------------------------------------- backward
 
-// Per-pixel state of one warp's 128 pixels.  Pixel (slot k, lane l) lives at
-// k * 32 + ((l + 8 k) & 31): an owner's accesses for one slot hit 32
-// distinct banks, and the 4 pixels of one column (same lane, slots 0..3)
-// fall in 4 different banks when other lanes gather them.
-// Fields: T, Q and the upstream colour gradient g[CH].
+// Per-pixel state of one warp's 128 pixels, pixel (slot k, lane l) at index
+// k * 32 + l: (T, Q) as one float2 and the upstream colour gradient g[CH]
+// as one float4, so a packed pair reads its pixel's state with two loads
+// and writes it back with one.  The packed pairs of a round are in
+// ascending pixel order, so neighbouring lanes mostly read neighbouring
+// entries.
 //
 // The walk's remainder rem[CH] and running product T_after enter the alpha
 // gradient only as  sum_c g_c (color_c - rem_c) + g_a T_after
@@ -593,11 +600,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
 // Both rem_c and T_after follow  x <- alpha y + (1 - alpha) x  (with y =
 // color_c and y = 0), so Q follows  Q <- alpha (g . color) + (1 - alpha) Q
 // from  Q = g . background - g_a.  One scalar replaces CH + 1 of them.
-template <int CH>
-struct StateLayout {
-    static constexpr int kTc = 0, kQ = 1, kG = 2;
-    static constexpr int kFields = 2 + CH;
-};
+
 // Gradient fields in the reduction buffer: colours[CH], then these.
 template <int CH>
 struct GradLayout {
@@ -605,13 +608,10 @@ struct GradLayout {
                          kQc = CH + 5, kAx = CH + 6, kAy = CH + 7;
 };
 
-__device__ __forceinline__ int sidx(int p) {  // p = k * 32 + lane
-    return (p & ~31) | ((p + ((p >> 5) << 3)) & 31);
-}
-
 template <int CH, int F>
 struct BwdWarpSmem {
-    float state[StateLayout<CH>::kFields][kWarpPix];
+    float2 tq[kWarpPix];  // (T, Q) of pixel k * 32 + lane
+    float4 g4[kWarpPix];  // upstream colour gradient of the pixel (CH <= 4 used)
     int16_t list[2][kWarpPix];    // packed valid pairs: k * 32 + owner lane (double buffer)
     // entries buffered per reduction: one (entry, field) sum per lane
     static constexpr int kRed = kWarp / F;
@@ -667,7 +667,6 @@ __device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslot
 template <int CH, bool ABS, bool TRACE>
 __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     k_raster_bwd(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
-    using S = StateLayout<CH>;
     using G = GradLayout<CH>;
     constexpr int F = CH + (ABS ? 8 : 6);
     constexpr int kBatch = kBatchBwd;
@@ -697,7 +696,6 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         const int y = ps.y0 + k;
-        const int si = sidx(k * kWarp + lane);
         py[k] = (float)y + 0.5f;
         ra[k] = 0.0f;
         last[k] = -1;
@@ -715,14 +713,15 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         }
         const float Tc = 1.0f - ra[k];
         float Q = -ga;
+        float gq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             Q += gc[c] * bgv[c];
-            w.state[S::kG + c][si] = gc[c];
+            gq[c] = gc[c];
             sb[c] += gc[c] * Tc;
         }
-        w.state[S::kTc][si] = Tc;
-        w.state[S::kQ][si] = Q;
+        w.g4[k * kWarp + lane] = make_float4(gq[0], gq[1], gq[2], gq[3]);
+        w.tq[k * kWarp + lane] = make_float2(Tc, Q);
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
     if (tid == 0) s_jmax = -1;
@@ -756,10 +755,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         const int nw = st.nw[warp];
         for (int ii = 0; ii < nw; ++ii) {
             const int i = st.idx[warp][ii];
-            const int32_t j = st.j[i];
+            const float4 mo = st.mo[i];  // mx, my, opacity, list position
+            const int32_t j = __float_as_int(mo.w);
             if (j > warp_max) continue;  // warp-uniform
-            const float4 mo = st.mo[i];
-            const float4 q = st.q[i];
+            const float4 q = st.q[i];    // a, b, c, flatten id
             // 1. which pixels of the warp have a valid pair with this entry
             int count = 0;
             if (TRACE) {
@@ -794,19 +793,20 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             const float4 col = st.col[i];
             for (int L = lane; L < count; L += kWarp) {
                 const int p = w.list[lb][L];
-                const int si = sidx(p);
                 const int ol = p & 31;
                 const int row = ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
                 const ColumnTerms ct =
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
                 const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
                 const float dx = ct.dx;
-                const float Tc = w.state[S::kTc][si];
+                const float2 tq = w.tq[p];
+                const float Tc = tq.x, Q = tq.y;
                 // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
                 // cutoff and last_id >= j (from the trace, or tested while
                 // packing); the T < 1 guard depends on the walk and is tested here
                 if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
-                const float Q = w.state[S::kQ][si];
+                const float4 g4 = w.g4[p];
+                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 const float one_m = 1.0f - e.alpha;
                 const float Tb = __fdividef(Tc, one_m);
@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 float gcol = 0.0f;  // g . color
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
-                    const float gcc = w.state[S::kG + c][si];
+                    const float gcc = gv[c];
                     v[c] += gcc * vis;
                     gcol += gcc * colv[c];
                 }
@@ -833,14 +833,13 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     v[G::kAx] += fabsf(gmx);
                     v[G::kAy] += fabsf(gmy);
                 }
-                w.state[S::kQ][si] = e.alpha * gcol + one_m * Q;
-                w.state[S::kTc][si] = Tb;
+                w.tq[p] = make_float2(Tb, e.alpha * gcol + one_m * Q);
             }
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
             for (int f = 0; f < F; ++f) reinterpret_cast<float*>(w.red[nslots][f])[lane] = v[f];
             if (lane == 0) {
-                w.red_gid[nslots] = st.gid[i];
+                w.red_gid[nslots] = __float_as_int(q.w);
                 w.red_n[nslots] = min(count, kWarp);
             }
             // the next entry packs into the other list buffer; the warp sync
