@@ -102,7 +102,11 @@ size_t gs_isect_workspace_size(int C, int N, int tile_width, int tile_height,
  * Two calls:
  *   1. Size query: keys == NULL.  Writes tiles_per_gauss (if not NULL) and
  *      the total count I to *h_n_isects (host).  This call synchronises
- *      `stream`, because the caller must size keys/flatten_ids from I.
+ *      `stream`, because the caller must size keys/flatten_ids from I.  The
+ *      count reaches the host through one word of mapped pinned host memory
+ *      that the library allocates once per calling thread and device (kept
+ *      for the thread's lifetime), so the query does not wait behind large
+ *      host<->device copies queued on other streams.
  *      workspace needs gs_isect_workspace_size(C, N, TW, TH, 0, sort).
  *   2. Emit: keys != NULL, n_isects = I from the query.  Writes keys
  *      uint64 (I), flatten_ids int32 (I) and, if not NULL, tiles_per_gauss

@@ -131,6 +131,38 @@ IsectLayout carve_isect(void* ws, const IsectPlan& p, int64_t n_isects, bool que
     return L;
 }
 
+// One word of mapped pinned host memory per calling thread and device, for
+// the size query's count: the device stores it directly, so the query does
+// not wait behind large copies queued on the copy engines.  Allocated on
+// first use and kept for the thread's lifetime.
+struct MappedWord {
+    unsigned long long* host = nullptr;
+    unsigned long long* dev = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+
+bool mapped_word(MappedWord* out) {
+    thread_local MappedWord words[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    MappedWord& w = words[dev];
+    if (!w.host) {
+        void* h = nullptr;
+        void* d = nullptr;
+        if (cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+            return false;
+        if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+            cudaFreeHost(h);
+            return false;
+        }
+        w.host = static_cast<unsigned long long*>(h);
+        w.dev = static_cast<unsigned long long*>(d);
+    }
+    *out = w;
+    return true;
+}
+
 int check_launch() {
     return cudaGetLastError() == cudaSuccess ? GS_OK : GS_ERR_CUDA;
 }
@@ -214,10 +246,18 @@ int gs_isect_tiles(const float* means2d, const float* radii, int elliptical, con
                            tiles_per_gauss, L.total, s);
         if (check_launch() != GS_OK) return GS_ERR_CUDA;
         unsigned long long total = 0;
-        if (cudaMemcpyAsync(&total, L.total, sizeof(total), cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess)
-            return GS_ERR_CUDA;
-        if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+        MappedWord mw;
+        if (mapped_word(&mw)) {
+            launch_publish_total(L.total, mw.dev, s);
+            if (check_launch() != GS_OK) return GS_ERR_CUDA;
+            if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+            total = *static_cast<volatile unsigned long long*>(mw.host);
+        } else {  // no mapped host memory: a copy
+            if (cudaMemcpyAsync(&total, L.total, sizeof(total), cudaMemcpyDeviceToHost, s) !=
+                cudaSuccess)
+                return GS_ERR_CUDA;
+            if (cudaStreamSynchronize(s) != cudaSuccess) return GS_ERR_CUDA;
+        }
         *h_n_isects = (int64_t)total;
         return total >= ((unsigned long long)1 << 31) ? GS_ERR_CAPACITY : GS_OK;
     }

@@ -64,6 +64,9 @@ void launch_isect_count(const float* means2d, const float* radii, int elliptical
 // Emits keys/ids for splats in `order` (nullptr = index order) with a
 // decoupled look-back scan of their counts.  up_hist (may be null) receives
 // histograms of the up_passes 8-bit digits of the key's upper word.
+// *host_word (mapped pinned host memory, device address) = *total.
+void launch_publish_total(const unsigned long long* total, unsigned long long* host_word,
+                          cudaStream_t s);
 // Tile rects (x0, y0, x1, y1) of every splat, in index order, plus the
 // histograms of the four 8-bit digits of the depth bits (hist [4][256]).
 void launch_rect_hist(const float* means2d, const float* radii, int elliptical,

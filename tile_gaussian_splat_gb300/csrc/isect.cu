@@ -329,6 +329,14 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Copies the device total to a mapped host word (a plain store over the
+// host link, so it does not wait for the copy engines).
+__global__ void k_publish_total(const unsigned long long* __restrict__ total,
+                                volatile unsigned long long* host_word) {
+    *host_word = *total;
+    __threadfence_system();
+}
+
 int grid_for(int64_t n, int per_thread) {
     int64_t g = (n + (int64_t)kThreads * per_thread - 1) / ((int64_t)kThreads * per_thread);
     if (g < 1) g = 1;
@@ -345,6 +353,11 @@ void launch_isect_count(const float* means2d, const float* radii, int elliptical
     k_isect_count<<<grid_for(CN, 4), kThreads, 0, s>>>(means2d, radii, elliptical, CN,
                                                        (float)tile_size, tile_width, tile_height,
                                                        tiles_per_gauss, total);
+}
+
+void launch_publish_total(const unsigned long long* total, unsigned long long* host_word,
+                          cudaStream_t s) {
+    k_publish_total<<<1, 1, 0, s>>>(total, host_word);
 }
 
 void launch_rect_hist(const float* means2d, const float* radii, int elliptical,
