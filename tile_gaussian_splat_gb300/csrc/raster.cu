@@ -285,21 +285,27 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
         if (i < n) {
             jj[r] = REVERSE ? hi - 1 - i : lo + i;
             const int64_t g = a.flatten_ids[jj[r]];
-            if ((uint64_t)g < (uint64_t)CN) {
+            const bool valid_id = (uint64_t)g < (uint64_t)CN;
+            bool any = valid_id;
+            if (TRACE_IN && valid_id) {
+                // the forward's masks say exactly which warps composited it;
+                // an entry none of them composited needs no splat data
+                const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
+                any = false;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    tw[r][w] = t[w];
+                    reach[w] = (tw[r][w].x | tw[r][w].y | tw[r][w].z | tw[r][w].w) != 0u;
+                    any |= reach[w];
+                }
+            }
+            if (any) {
                 const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
                 const float* qq = a.conics + 3 * g;
                 mo[r] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
                 q[r] = make_float4(qq[0], qq[1], qq[2], 0.0f);
                 gid[r] = (int32_t)g;
-                if (TRACE_IN) {
-                    // the forward's masks say exactly which warps composited it
-                    const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) {
-                        tw[r][w] = t[w];
-                        reach[w] = (tw[r][w].x | tw[r][w].y | tw[r][w].z | tw[r][w].w) != 0u;
-                    }
-                } else {
+                if (!TRACE_IN) {
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w)
                         reach[w] =
