@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import DEV, gpu_forward, scene_to_dev, to_dev, u64
+from gpu_util import DEV, gpu_forward, scene_to_dev, to_dev
 from tile_gaussian_splat_gb300 import binding as gs
 from tile_gaussian_splat_gb300 import scenes
 
@@ -156,6 +156,17 @@ def test_backward_over_bins_equals_sorted():
             x, y = a[k].cpu().numpy(), b[k].cpu().numpy()
             scale = np.abs(x).max() + 1e-30
             np.testing.assert_allclose(y, x, rtol=1e-4, atol=1e-6 * scale, err_msg=k)
+
+
+def test_bins_empty_and_invisible():
+    for N, far in ((0, False), (50, True)):
+        s = scenes.random_small(6, C=2, N=N, W=64, H=48)
+        if far:
+            s.means2d[:] = -1000.0
+        st = gs.new_status(DEV)
+        b, c = _gpu_bins(s, scene_to_dev(s), 8, st)
+        gs.check_status(st)
+        assert (c == 0).all() and (b == -1).all()
 
 
 def test_bin_argument_errors():

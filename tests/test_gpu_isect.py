@@ -89,6 +89,15 @@ def test_single_tile_grid():
     assert _check_isect(s) > 0
 
 
+def test_three_tile_passes():
+    # 256x256 tiles (16 bits) and 3 cameras (2 bits): three 8-bit camera|tile
+    # passes, so emission starts in the workspace buffer and the passes
+    # alternate twice before the widening one
+    s = scenes.random_small(5, C=3, N=3000, W=4096, H=4096, sigma=(2.0, 60.0))
+    assert gs.gs_tile_bits(s.tile_width, s.tile_height) == 16
+    assert _check_isect(s) > 0
+
+
 def test_max_camera_bits():
     # tile_bits + camera bits == 32: 2^16 tiles (256x256 grid), 2^16 cameras
     C = 65536
