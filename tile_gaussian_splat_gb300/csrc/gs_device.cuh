@@ -78,6 +78,26 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+// The lanes of the warp whose `valid` is set and whose digit d (its low
+// `nbits` bits, nbits <= 8, the same in every lane) equals this lane's:
+// one ballot per digit bit, each lane keeping the lanes that agree with it
+// on that bit.  All 32 lanes must call it.  In the radix passes' ranking
+// (twelve calls back to back per thread) this measured 8-10 % faster per
+// emit+sort call than the match.any instruction; in the emission's
+// histograms (two calls per pair among other work) match.any stays faster.
+__device__ __forceinline__ unsigned digit_peers(uint32_t d, bool valid, int nbits) {
+    unsigned pm = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        if (b < nbits) {
+            const unsigned bit = (d >> b) & 1u;
+            const unsigned bb = __ballot_sync(0xffffffffu, bit);
+            pm &= bit ? bb : ~bb;
+        }
+    }
+    return pm;
+}
+
 // Block-wide exclusive scan of one int64 per thread (blockDim.x == 32*W).
 // `scratch` holds >= 32 int64.  Returns the exclusive prefix; *total gets the
 // block sum.  Contains __syncthreads.

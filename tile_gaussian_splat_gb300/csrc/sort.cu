@@ -8,8 +8,8 @@
 //   1. takes a virtual block id from an atomic ticket (so a block only ever
 //      waits on blocks that are already running);
 //   2. loads its tile of keys warp-striped (coalesced) into registers;
-//   3. ranks each key among equal digits of its warp (match.any + popc),
-//      keeping input order (stability);
+//   3. ranks each key among equal digits of its warp (bit-sliced ballots +
+//      popc), keeping input order (stability);
 //   4. publishes its 256 digit counts, then walks back over predecessors'
 //      words (bounded wait) to get its exclusive prefix per digit;
 //   5. reorders the tile by digit in shared memory and writes it out, so
@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(kThreads, 4)
     for (int i = 0; i < ITEMS + kLag; ++i) {
         if (i < ITEMS) {
             const bool valid = warp_base + i * kWarp + lane < n;
-            const uint32_t d = valid ? digit_of(key[i], shift, dmask) : 0x100u + lane;
-            peers[i] = __match_any_sync(0xffffffffu, d);
+            const uint32_t d = valid ? digit_of(key[i], shift, dmask) : 0u;
+            // every lane calls it; bits above a narrower digit are 0 in every lane
+            const unsigned pm = digit_peers(d, valid, 8);
+            peers[i] = valid ? pm : (1u << lane);
             uint32_t old = 0;
             if (valid && (peers[i] & lt) == 0)
                 old = atomicAdd(&sm.warp_count[warp][d], (uint32_t)__popc(peers[i]));
