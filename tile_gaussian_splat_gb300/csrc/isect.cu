@@ -145,11 +145,20 @@ struct EmitSmem {
     uint32_t blk;
 };
 
+// One count per valid lane into bins[d].  A digit shared by every valid lane
+// of the warp (the high digit of neighbouring tiles, mostly) is added once;
+// otherwise each lane adds its own (neighbouring tiles' low digits rarely
+// collide, so the shared-memory atomics seldom serialise).
 __device__ __forceinline__ void hist_inc(uint32_t* bins, uint32_t d, bool valid) {
-    unsigned act = __ballot_sync(0xffffffffu, valid);
-    if (!valid) return;
-    unsigned peers = __match_any_sync(act, d);
-    if ((peers & lanemask_lt()) == 0) atomicAdd(&bins[d], (uint32_t)__popc(peers));
+    const unsigned act = __ballot_sync(0xffffffffu, valid);
+    if (act == 0) return;
+    const int first = __ffs(act) - 1;
+    const uint32_t d0 = __shfl_sync(0xffffffffu, d, first);
+    if (__all_sync(0xffffffffu, !valid || d == d0)) {
+        if ((int)(threadIdx.x & 31) == first) atomicAdd(&bins[d0], (uint32_t)__popc(act));
+    } else if (valid) {
+        atomicAdd(&bins[d], 1u);
+    }
 }
 
 // Exclusive prefix of this chunk's total over earlier chunks, by warp 0: the
