@@ -618,48 +618,82 @@ template <int CH, int F>
 struct BwdWarpSmem {
     float2 tq[kWarpPix];  // (T, Q) of pixel k * 32 + lane
     float4 g4[kWarpPix];  // upstream colour gradient of the pixel (CH <= 4 used)
-    int16_t list[2][kWarpPix];    // packed valid pairs: k * 32 + owner lane (double buffer)
+    int16_t list[kWarpPix];  // packed valid pairs: k * 32 + owner lane
     // entries buffered per reduction: one (entry, field) sum per lane
     static constexpr int kRed = kWarp / F;
-    float4 red[kRed][F][kWarp / 4];  // per (entry, field): the lanes' terms
+    // per (entry, field): the 32 lanes' terms (lanes without a pair hold 0),
+    // then 16 bytes of padding, so that row r starts in bank group r mod 8
+    // and the 8 lanes of a quarter warp, summing rows r .. r + 7, read chunk
+    // i of each without a bank conflict
+    float4 red[kRed][F][kWarp / 4 + 1];
     int32_t red_gid[kRed];
-    int32_t red_n[kRed];  // lanes holding terms (the packed pairs fill lanes 0..n-1)
+};
+
+// A lane's share of every flush: field f of buffered entry e, where
+// (e, f) = (lane / F, lane mod F) never changes, so the gradient array, its
+// stride per splat and the shared-memory row are worked out once per thread.
+struct FlushTask {
+    float* base;     // gradient array + field offset
+    uint32_t row;    // shared-memory address of red[e][f][0]
+    int e;           // buffered entry (kRed or more: no task)
+    int stride;      // floats per splat in that array
 };
 
 template <int CH, int F>
-__device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslots,
-                                                const RasterArgs& a, const RasterGrads& gr,
-                                                int lane) {
+__device__ __forceinline__ FlushTask flush_task(BwdWarpSmem<CH, F>& w, const RasterArgs& a,
+                                                const RasterGrads& gr, int lane) {
     using G = GradLayout<CH>;
+    FlushTask t;
+    t.e = lane / F;
+    const int f = lane - t.e * F;
+    const int e = t.e < BwdWarpSmem<CH, F>::kRed ? t.e : 0;
+    t.row = (uint32_t)__cvta_generic_to_shared(&w.red[e][f][0]);
+    if (f < CH) {
+        t.base = gr.grad_colors + a.ch_off + f;
+        t.stride = a.channels;
+    } else if (f == G::kOp) {
+        t.base = gr.grad_opacities;
+        t.stride = 1;
+    } else if (f <= G::kMy) {
+        t.base = gr.grad_means2d + (f - G::kMx);
+        t.stride = 2;
+    } else if (f <= G::kQc) {
+        t.base = gr.grad_conics + (f - G::kQa);
+        t.stride = 3;
+    } else {
+        t.base = gr.grad_means2d_abs + (f - G::kAx);
+        t.stride = 2;
+    }
+    return t;
+}
+
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Sums each buffered (entry, field) over the lanes that hold terms and adds
+// it to the splat's gradient with one atomic: lane t owns task t.
+template <int CH, int F>
+__device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslots,
+                                                const FlushTask& task, int lane) {
     static_assert(BwdWarpSmem<CH, F>::kRed >= 1, "one reduction task per lane");
     __syncwarp();
-    const int t = lane;
-    if (t < nslots * F) {
-        const int e = t / F, f = t - (t / F) * F;
-        const int nch = (w.red_n[e] + 3) >> 2;  // 16-byte chunks holding terms
-        // chunk (i + t) mod 8 at step i: the 8 lanes of a quarter warp read 8
-        // different chunks, so the rows (all starting at bank 0) do not clash
+    if (task.e < nslots) {
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int i = 0; i < kWarp / 4; ++i) {
-            const int c = (i + t) & (kWarp / 4 - 1);
-            if (c < nch) {
-                const float4 q = w.red[e][f][c];
-                acc = __fadd2_rn(acc, make_float2(q.x, q.y));
-                acc = __fadd2_rn(acc, make_float2(q.z, q.w));
-            }
+        for (int c = 0; c < kWarp / 4; ++c) {
+            const float4 q = lds128(task.row + 16u * (uint32_t)c);
+            acc = __fadd2_rn(acc, make_float2(q.x, q.y));
+            acc = __fadd2_rn(acc, make_float2(q.z, q.w));
         }
         const float sum = acc.x + acc.y;
-        if (sum != 0.0f) {
-            const int64_t g = w.red_gid[e];
-            float* dst;
-            if (f < CH) dst = gr.grad_colors + g * a.channels + a.ch_off + f;
-            else if (f == G::kOp) dst = gr.grad_opacities + g;
-            else if (f <= G::kMy) dst = gr.grad_means2d + 2 * g + (f - G::kMx);
-            else if (f <= G::kQc) dst = gr.grad_conics + 3 * g + (f - G::kQa);
-            else dst = gr.grad_means2d_abs + 2 * g + (f - G::kAx);
-            atomicAdd(dst, sum);
-        }
+        if (sum != 0.0f)
+            atomicAdd(task.base + (int64_t)w.red_gid[task.e] * task.stride, sum);
     }
     __syncwarp();
 }
@@ -753,8 +787,8 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     const unsigned lt = lanemask_lt();
     const int x_tile = tr.tx * kTile;
     const int y_tile = tr.ty * kTile;
+    const FlushTask task = flush_task<CH, F>(w, a, gr, lane);
     int nslots = 0;
-    int lb = 0;  // list buffer of the current entry
     for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
         const int64_t b0 = max(tr.start, b1 - kBatch);
         stage_batch<true, TRACE, kBatch, CH>(a, box, b0, b1, trace, st);
@@ -766,6 +800,8 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             if (j > warp_max) continue;  // warp-uniform
             const float4 q = st.q[i];    // a, b, c, flatten id
             // 1. which pixels of the warp have a valid pair with this entry
+            //    (the sync orders the previous entry's list reads first)
+            __syncwarp();
             int count = 0;
             if (TRACE) {
                 const uint4 m4 = st.tr[i][warp];
@@ -773,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
 #pragma unroll
                 for (int k = 0; k < kPPT; ++k) {
                     if ((m[k] >> lane) & 1u)
-                        w.list[lb][count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
                     count += __popc(m[k]);
                 }
             } else {
@@ -786,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
                                        e.alpha >= a.alpha_cutoff && last[k] >= j;
                     const unsigned m = __ballot_sync(0xffffffffu, valid);
-                    if (valid) w.list[lb][count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
+                    if (valid) w.list[count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
                     count += __popc(m);
                 }
             }
@@ -798,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             for (int f = 0; f < F; ++f) v[f] = 0.0f;
             const float4 col = st.col[i];
             for (int L = lane; L < count; L += kWarp) {
-                const int p = w.list[lb][L];
+                const int p = w.list[L];
                 const int ol = p & 31;
                 const int row = ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
                 const ColumnTerms ct =
@@ -844,20 +880,14 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
             for (int f = 0; f < F; ++f) reinterpret_cast<float*>(w.red[nslots][f])[lane] = v[f];
-            if (lane == 0) {
-                w.red_gid[nslots] = __float_as_int(q.w);
-                w.red_n[nslots] = min(count, kWarp);
-            }
-            // the next entry packs into the other list buffer; the warp sync
-            // after that packing orders this entry's reads before its reuse
-            lb ^= 1;
+            if (lane == 0) w.red_gid[nslots] = __float_as_int(q.w);
             if (++nslots == BwdWarpSmem<CH, F>::kRed) {
-                flush_reduction<CH, F>(w, nslots, a, gr, lane);
+                flush_reduction<CH, F>(w, nslots, task, lane);
                 nslots = 0;
             }
         }
     }
-    if (nslots) flush_reduction<CH, F>(w, nslots, a, gr, lane);
+    if (nslots) flush_reduction<CH, F>(w, nslots, task, lane);
 }
 
 template <int CH>
