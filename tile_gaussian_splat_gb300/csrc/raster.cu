@@ -422,14 +422,22 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     float2 T[kPairs], acc[kPairs][4], npy[kPairs];
     float py[kPPT];
     int32_t last[kPPT], n_eval[kPPT], n_comp[kPPT], n_last[kPPT];
-    bool done[kPPT];
+    // A pixel that has stopped (outside the image, or its transmittance fell
+    // below the threshold) takes no further entry: its cutoff becomes +inf,
+    // so "not stopped and alpha >= cutoff" is one comparison and no flag
+    // stays live across entries.  The pair counters keep an explicit flag.
+    float cut[kPPT];
+    bool done_c[COUNT ? kPPT : 1];
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         last[k] = -1;
         n_eval[k] = n_comp[k] = n_last[k] = 0;
-        done[k] = !(ps.x < a.width && ps.y0 + k < a.height);
+        const bool outside = !(ps.x < a.width && ps.y0 + k < a.height);
+        cut[k] = outside ? INFINITY : a.alpha_cutoff;
+        if (COUNT) done_c[k] = outside;
         py[k] = (float)(ps.y0 + k) + 0.5f;
     }
+    auto stopped = [&](int k) { return COUNT ? done_c[k] : cut[k] == INFINITY; };
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) {
         T[p] = splat2(1.0f);
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
     for (int64_t b0 = tr.start; b0 < tr.end; b0 += kBatch) {
         bool all_done = true;
 #pragma unroll
-        for (int k = 0; k < kPPT; ++k) all_done &= done[k];
+        for (int k = 0; k < kPPT; ++k) all_done &= stopped(k);
         if (__syncthreads_count(all_done) == kThreads) break;
         const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
         const int32_t b0_32 = (int32_t)b0;  // list positions are below 2^31
@@ -483,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                             const int k = 2 * p + e;
                             const float r_e = comp(const_cast<float2&>(raw), e);
                             const float alpha = kClamp ? fminf(r_e, kAlphaClamp) : r_e;
-                            took[k] = !done[k] && alpha >= a.alpha_cutoff;
-                            if (COUNT) n_eval[k] += done[k] ? 0 : 1;
+                            took[k] = alpha >= cut[k];
+                            if (COUNT) n_eval[k] += done_c[k] ? 0 : 1;
                             // a pair not taken adds exactly 0 (finite colours, T)
                             comp(aw, e) = took[k] ? alpha : 0.0f;
                         }
@@ -501,8 +509,10 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                                 ++n_comp[k];
                                 n_last[k] = n_eval[k];
                             }
-                            done[k] = done[k] ||
-                                      (took[k] && comp(T[p], e) < a.transmittance_threshold);
+                            const bool stop =
+                                took[k] && comp(T[p], e) < a.transmittance_threshold;
+                            cut[k] = stop ? INFINITY : cut[k];
+                            if (COUNT) done_c[k] = done_c[k] || stop;
                         }
                     }
                 };
@@ -518,8 +528,8 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                     for (int k = 0; k < kPPT; ++k) {
                         const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
                         alpha[k] = e.alpha;
-                        took[k] = !done[k] && e.s >= 0.0f && e.alpha >= a.alpha_cutoff;
-                        if (COUNT) n_eval[k] += done[k] ? 0 : 1;
+                        took[k] = e.s >= 0.0f && e.alpha >= cut[k];
+                        if (COUNT) n_eval[k] += done_c[k] ? 0 : 1;
                     }
 #pragma unroll
                     for (int k = 0; k < kPPT; ++k) {
@@ -537,7 +547,10 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                             ++n_comp[k];
                             n_last[k] = n_eval[k];
                         }
-                        if (Tk < a.transmittance_threshold) done[k] = true;
+                        if (Tk < a.transmittance_threshold) {
+                            cut[k] = INFINITY;
+                            if (COUNT) done_c[k] = true;
+                        }
                     }
                 }
                 if (TRACE) {
@@ -553,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                 if ((ii & 15) == 15) {
                     bool d = true;
 #pragma unroll
-                    for (int k = 0; k < kPPT; ++k) d &= done[k];
+                    for (int k = 0; k < kPPT; ++k) d &= stopped(k);
                     if (__all_sync(0xffffffffu, d)) break;
                 }
             }
