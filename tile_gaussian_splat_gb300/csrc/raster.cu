@@ -393,6 +393,18 @@ __device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
 
 // ------------------------------------------------------------------ forward
 
+// *dst = v by lane 0 only, as one predicated store (written as a branch
+// around the store, the per-entry trace store made the forward 4 % slower).
+__device__ __forceinline__ void st_shared_lane0(uint32_t* dst, uint4 v, int lane) {
+    const uint32_t addr = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %0, 0;\n\t"
+        "@p st.shared.v4.u32 [%1], {%2, %3, %4, %5};\n\t}"
+        :
+        : "r"(lane), "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+        : "memory");
+}
+
 // Component i (0 or 1, a compile-time constant after unrolling) of a pair.
 __device__ __forceinline__ float& comp(float2& v, int i) { return i ? v.y : v.x; }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
@@ -559,8 +571,7 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                                                 __ballot_sync(0xffffffffu, took[1]),
                                                 __ballot_sync(0xffffffffu, took[2]),
                                                 __ballot_sync(0xffffffffu, took[3]));
-                    if (lane == 0)
-                        *reinterpret_cast<uint4*>(&s_trace[j - b0_32][warp * kPPT]) = m4;
+                    st_shared_lane0(&s_trace[j - b0_32][warp * kPPT], m4, lane);
                 }
                 // leave the batch early once every pixel of the warp has stopped
                 if ((ii & 15) == 15) {
