@@ -641,7 +641,7 @@ struct GradLayout {
 template <int CH, int F>
 struct BwdWarpSmem {
     float2 tq[kWarpPix];  // (T, Q) of pixel k * 32 + lane
-    float4 g4[kWarpPix];  // upstream colour gradient of the pixel (CH <= 4 used)
+    float4 g4[kWarpPix];  // upstream colour gradient g[CH]; with CH < 4 .w = pixel centre y
     int16_t list[kWarpPix];  // packed valid pairs: k * 32 + owner lane
     // entries buffered per reduction: one (entry, field) sum per lane
     static constexpr int kRed = kWarp / F;
@@ -784,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             gq[c] = gc[c];
             sb[c] += gc[c] * Tc;
         }
-        w.g4[k * kWarp + lane] = make_float4(gq[0], gq[1], gq[2], gq[3]);
+        // with fewer than 4 channels the spare lane holds the pixel centre's y
+        w.g4[k * kWarp + lane] = make_float4(gq[0], gq[1], gq[2], CH < 4 ? py[k] : gq[3]);
         w.tq[k * kWarp + lane] = make_float2(Tc, Q);
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
@@ -860,10 +861,13 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             for (int L = lane; L < count; L += kWarp) {
                 const int p = w.list[L];
                 const int ol = p & 31;
-                const int row = ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
+                const float4 g4 = w.g4[p];
+                const float pyv = CH < 4 ? g4.w
+                                         : (float)(y_tile + ((warp * kWarp + ol) / kTile) * kPPT +
+                                                   (p >> 5)) + 0.5f;
                 const ColumnTerms ct =
                     column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
-                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)(y_tile + row) + 0.5f);
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, pyv);
                 const float dx = ct.dx;
                 const float2 tq = w.tq[p];
                 const float Tc = tq.x, Q = tq.y;
@@ -871,7 +875,6 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 // cutoff and last_id >= j (from the trace, or tested while
                 // packing); the T < 1 guard depends on the walk and is tested here
                 if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
-                const float4 g4 = w.g4[p];
                 const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 const float one_m = 1.0f - e.alpha;
