@@ -44,7 +44,8 @@ FP32_LANES = 128
 SM_MAX_MHZ = 2070.0
 L2_FLUSH_BYTES = 256 << 20
 
-# algorithmic FP32-pipe operations (FMA = 1) per pair, stated in the design doc
+# algorithmic FP32-pipe operations (FMA = 1) per pair, counted from the
+# per-pixel formulas of the compositing and its adjoint
 FWD_OPS_EVAL = 15     # dx, dy, quadratic form (9), o*exp, clamp, two tests
 FWD_OPS_COMP = 7      # T*alpha, 3 colour FMAs, 1-alpha, T update, threshold test
 BWD_OPS_EVAL = 15     # re-evaluation of alpha for every entry up to last_id
@@ -417,7 +418,7 @@ def run_ours(args, rank, world, scene):
     from tile_gaussian_splat_gb300 import binding as gsb
     key_bits = gsb.gs_tile_bits(s.tile_width, s.tile_height) + max(0, (s.C - 1).bit_length())
     up_passes = (key_bits + 7) // 8
-    # algorithmic bytes (stated in the design doc): what each stage must read and write
+    # algorithmic bytes: what each stage must read and write
     # emit+sort: rects + depth histograms (read mean, radii, depth; write a
     # 16-byte rect) 36 B/splat; depth sort 12 + 3 x 16 B/splat; emission
     # (order + rect gather) 20 B/splat and an 8-byte key+id per intersection;
