@@ -110,11 +110,12 @@ def _bwd_case(s, masks=None, absgrad=True, seed=1, nudges=1):
     return rb, got, excluded.reshape(s.C, s.N)
 
 
-def _compare_grads(rb, got, excluded, rtol=1e-3, atol=1e-6):
+def _compare_grads(rb, got, excluded, rtol=1e-3, atol=1e-6, cancel_rel=1e-4, loose_rel=4e-6):
     """Strict bound |g - r| <= rtol |r| + atol on every element whose sum is
-    not dominated by cancellation; elements whose |r| is below 1e-4 of the sum
-    of |terms| (the float-summation error scale of any order) are held to
-    4e-6 of that sum instead.  Returns (checked, cancellation-bound) counts."""
+    not dominated by cancellation; elements whose |r| is below cancel_rel of
+    the sum of |terms| (the float-summation error scale of any order) are held
+    to loose_rel of that sum instead.  Returns (checked, cancellation-bound)
+    counts."""
     stats = [0, 0]
     for name, mag, w in [("grad_means2d", "mag_means2d", 2), ("grad_conics", "mag_conics", 3),
                          ("grad_colors", "mag_colors", rb["grad_colors"].shape[-1]),
@@ -125,12 +126,12 @@ def _compare_grads(rb, got, excluded, rtol=1e-3, atol=1e-6):
         keep = ~excluded if w == 1 else np.repeat(~excluded[..., None], w, axis=-1)
         g, r, m = g[keep], r[keep], m[keep]
         err = np.abs(g - r)
-        cancel = np.abs(r) < 1e-4 * m
+        cancel = np.abs(r) < cancel_rel * m
         strict_bad = (err > rtol * np.abs(r) + atol) & ~cancel
         assert not strict_bad.any(), (
             f"{name}: {strict_bad.sum()} of {g.size} off; worst err "
             f"{err[strict_bad].max()} (ref {r[strict_bad][np.argmax(err[strict_bad])]})")
-        loose_bad = (err > 4e-6 * m + atol) & cancel
+        loose_bad = (err > loose_rel * m + atol) & cancel
         assert not loose_bad.any(), f"{name}: {loose_bad.sum()} cancellation-bound elements off"
         stats[0] += g.size
         stats[1] += int(cancel.sum())
@@ -238,3 +239,41 @@ def test_backward_trace_equals_recompute(case):
         x, y = a[k].cpu().numpy(), b[k].cpu().numpy()
         scale = np.abs(x).max() + 1e-30
         np.testing.assert_allclose(y, x, rtol=1e-4, atol=1e-6 * scale, err_msg=k)
+
+
+@pytest.mark.parametrize("cutoff,thr", [(0.0, 1e-4), (1.0 / 255.0, 0.0), (1.0 / 255.0, 0.999),
+                                        (0.3, 0.5), (-1.0, 1e-4)])
+def test_cutoff_and_threshold_extremes(cutoff, thr):
+    # a zero or negative cutoff takes every pair with s >= 0 (alpha 0 included,
+    # so last ids move on pairs that add nothing); threshold 0 never stops a
+    # pixel, 0.999 stops it at its first composite; the trace-driven backward
+    # must agree with the recomputing one under each setting
+    s = scenes.random_small(11, C=2, N=1500, W=80, H=56, sigma=(0.5, 9.0))
+    s.alpha_cutoff = np.float32(cutoff)
+    s.transmittance_threshold = np.float32(thr)
+    iso, ref = _oracle_forward(s)
+    d = scene_to_dev(s)
+    compare_forward(ref, gpu_forward(s, d))
+    rb, got, excluded = _bwd_case(s, absgrad=False)
+    if cutoff > 0:
+        _compare_grads(rb, got, excluded)
+    else:
+        # without a positive cutoff every pixel of a splat's tile rectangle adds
+        # a term, out to s of 20 and more, where the exponential's relative
+        # error (2.4e-7 + 1e-7 s) reaches 1e-5 of a term: sums of |terms| near
+        # 1e3 for results near 1 then carry errors of about 2e-5 of the sum
+        _compare_grads(rb, got, excluded, cancel_rel=1e-3, loose_rel=4e-5)
+    f, tr = _gpu_fwd_with_trace(s, d)
+    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, seed=3)
+    outs = []
+    for trace in (None, tr):
+        outs.append(gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"],
+                                        d["backgrounds"], None, s.width, s.height, 16,
+                                        f["offsets"], f["flatten_ids"], s.alpha_cutoff,
+                                        f["render_alphas"], f["last_ids"], to_dev(g_rgb),
+                                        to_dev(g_a), trace=trace))
+    torch.cuda.synchronize()
+    for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities"):
+        x, y = outs[0][k].cpu().numpy(), outs[1][k].cpu().numpy()
+        np.testing.assert_allclose(y, x, rtol=1e-4, atol=1e-6 * (np.abs(x).max() + 1e-30),
+                                   err_msg=k)
