@@ -873,13 +873,17 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                 const float Tc = tq.x, Q = tq.y;
                 // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
                 // cutoff and last_id >= j (from the trace, or tested while
-                // packing); the T < 1 guard depends on the walk and is tested here
-                if (!(Tc < 1.0f && e.alpha < 1.0f)) continue;
+                // packing), so alpha is finite; the T < 1 guard depends on the
+                // walk and is tested here.  A pair failing it adds nothing and
+                // leaves the pixel's state as it was: it runs with alpha 0 and
+                // no alpha gradient (no branch around the pair's work)
+                const bool ok = Tc < 1.0f && e.alpha < 1.0f;
+                const float al = ok ? e.alpha : 0.0f;
                 const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
                 const float colv[4] = {col.x, col.y, col.z, col.w};
-                const float one_m = 1.0f - e.alpha;
+                const float one_m = 1.0f - al;
                 const float Tb = __fdividef(Tc, one_m);
-                const float vis = Tb * e.alpha;
+                const float vis = Tb * al;
                 float gcol = 0.0f;  // g . color
 #pragma unroll
                 for (int c = 0; c < CH; ++c) {
@@ -888,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     gcol += gcc * colv[c];
                 }
                 const float g_alpha = Tb * (gcol - Q);
-                const float g_raw = e.raw < kAlphaClamp ? g_alpha : 0.0f;
+                const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
                 v[G::kOp] += g_raw * e.resp;
                 const float g_s = -g_raw * e.raw;
                 const float gmx = g_s * (q.x * dx + q.y * e.dy);
@@ -902,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
                     v[G::kAx] += fabsf(gmx);
                     v[G::kAy] += fabsf(gmy);
                 }
-                w.tq[p] = make_float2(Tb, e.alpha * gcol + one_m * Q);
+                w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
             }
             // 3. this entry's terms into the warp's reduction buffer
 #pragma unroll
