@@ -241,13 +241,11 @@ static_assert(kPPT == 4, "a warp's trace words of one entry are one uint4");
 template <int BATCH, bool TRACE_IN, bool FAST>
 struct StageSmem {
     static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
-    float4 mo[BATCH];   // mx, my, opacity, forward: fast form (0 no, 1 yes, 2 yes
-                        // without clamp); backward: list position (int bits)
+    float4 mo[BATCH];   // mx, my, opacity, list position (int bits)
     float4 q[BATCH];    // a, b, c, backward: flatten id (int bits)
-    float4 qf[FAST ? BATCH : 1];  // fast form: a/2, b, c/2, - (forward only)
+    float4 qf[FAST ? BATCH : 1];  // forward: a/2, b, c/2, fast form (0 no, 1 yes,
+                                  // 2 yes without clamp)
     float4 col[BATCH];  // up to 4 channels of the launch's chunk
-    int32_t j[FAST ? BATCH : 1];  // list position (forward; the backward keeps it
-                                  // in mo.w and the flatten id in q.w)
     uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
     uint8_t idx[kWarps][BATCH];  // per warp: staged slots that can reach its pixels
     int32_t nw[kWarps];          // per warp: length of idx
@@ -353,10 +351,10 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
             // 0.99 clamp, whatever the exponential's 2^-22 rounding
             if (!REVERSE) {
                 st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
-                                         fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f);
+                                         __int_as_float((int32_t)jj[r]));
                 st.q[pos] = q[r];
+                f.w = fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f;
                 st.qf[pos] = f;
-                st.j[pos] = (int32_t)jj[r];
             } else {
                 st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
                                          __int_as_float((int32_t)jj[r]));
@@ -473,14 +471,14 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
             for (int ii = 0; ii < nw; ++ii) {
                 const int i = st.idx[warp][ii];
                 const float4 mo = st.mo[i];
-                const int32_t j = st.j[i];
+                const int32_t j = __float_as_int(mo.w);
+                const float4 h = st.qf[i];  // a/2, b, c/2, fast-form flag
                 const float4 col = st.col[i];
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 bool took[kPPT];
                 // fast form (warp-uniform): branch-free compositing
                 auto fast_pairs = [&](auto clamp_tag) {
                     constexpr bool kClamp = decltype(clamp_tag)::value;
-                    const float4 h = st.qf[i];
                     const FastColumn fc = fast_column(mo.x, h, px);
                     const float2 qa2 = splat2(fc.qa2), bdx = splat2(fc.bdx), c2 = splat2(h.z);
                     const float2 my = splat2(mo.y), op = splat2(mo.z);
@@ -528,9 +526,9 @@ __global__ void __launch_bounds__(kThreads, GS_FWD_MIN_BLOCKS)
                         }
                     }
                 };
-                if (mo.w > 1.5f) {
+                if (h.w > 1.5f) {
                     fast_pairs(std::integral_constant<bool, false>{});
-                } else if (mo.w != 0.0f) {
+                } else if (h.w != 0.0f) {
                     fast_pairs(std::integral_constant<bool, true>{});
                 } else {  // exact-order form, with the s >= 0 test
                     const float4 q = st.q[i];
@@ -822,7 +820,9 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             const int i = st.idx[warp][ii];
             const float4 mo = st.mo[i];  // mx, my, opacity, list position
             const int32_t j = __float_as_int(mo.w);
-            if (j > warp_max) continue;  // warp-uniform
+            // warp-uniform; with a trace it never holds (a composited pair
+            // has j <= its pixel's last id <= warp_max), so it is not tested
+            if (!TRACE && j > warp_max) continue;
             const float4 q = st.q[i];    // a, b, c, flatten id
             // 1. which pixels of the warp have a valid pair with this entry
             //    (the sync orders the previous entry's list reads first)
