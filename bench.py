@@ -499,7 +499,9 @@ def run_ours(args, rank, world, scene):
                         "uploads/downloads overlapped with the previous/next step)",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e, 3)},
-        "gpu_launches": args.steps * (1 + 1 + 4 + 1 + up_passes + 1 + 1 + 1),
+        # per step: count, count word, rects + depth histograms, 4 depth
+        # passes, emit, the camera/tile passes, ranges, forward, backward
+        "gpu_launches": args.steps * (1 + 1 + 1 + 4 + 1 + up_passes + 1 + 1 + 1),
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
     }
