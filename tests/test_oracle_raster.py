@@ -403,3 +403,42 @@ def test_double_twin_matches_float_forward(seed):
     assert ok.mean() > 0.9
     np.testing.assert_allclose(f32["render_colors"][ok], rgb[ok], atol=2e-6, rtol=0)
     np.testing.assert_allclose(f32["render_alphas"][..., 0][ok], alpha[ok], atol=2e-6, rtol=0)
+
+
+# ------------------------------------------- cutoff and threshold readings
+
+
+def test_cutoff_zero_takes_vanishing_pairs():
+    # a splat whose alpha at the pixel is exactly 0 (s huge) is skipped under
+    # the default cutoff but taken under a zero cutoff: its position becomes
+    # the last id while the colour and T stay those of the front splat
+    s = _scene([[7.5, 7.5], [7.5, 7.5]], [[1, 0, 1], [1e4, 0, 1e4]], [[1, 0, 0], [0, 1, 0]],
+               [0.5, 0.5], [1.0, 2.0], [3.0, 3.0], 16, 16)
+    iso = _setup(s)
+    x, y = 12, 7  # centre (12.5, 7.5), dx = -5: s = 12.5 for the first, 1.25e5 for the second
+    a = _fwd(s, iso, cut=np.float32(1.0 / 255.0))
+    b = _fwd(s, iso, cut=np.float32(0.0))
+    alpha0 = 0.5 * np.exp(-12.5)
+    assert alpha0 < 1.0 / 255.0  # the front splat is itself below the default cutoff
+    assert a["last_ids"][0, y, x] == -1
+    assert b["last_ids"][0, y, x] == 1
+    # render_alpha = 1 - T carries the float rounding of T = 1 - alpha0
+    np.testing.assert_allclose(b["render_alphas"][0, y, x, 0], alpha0, atol=1.2e-7)
+    np.testing.assert_allclose(b["render_colors"][0, y, x], [alpha0, 0, 0], rtol=1e-5)
+
+
+def test_threshold_zero_never_stops_and_high_threshold_stops_at_first():
+    # three opaque splats over the same pixel: T = 0.01^k after k of them.
+    # Threshold 0: all three are composited (T never falls below 0); a
+    # threshold above 0.01 stops after the first
+    s = _scene([[7.5, 7.5]] * 3, [[1, 0, 1]] * 3, [[1, 0, 0], [0, 1, 0], [0, 0, 1]],
+               [0.99, 0.99, 0.99], [1.0, 2.0, 3.0], [3.0, 3.0, 3.0], 16, 16)
+    iso = _setup(s)
+    x, y = 7, 7  # the centre pixel: s = 0, alpha = 0.99
+    a = _fwd(s, iso, thr=np.float32(0.0))
+    b = _fwd(s, iso, thr=np.float32(0.999))
+    assert a["last_ids"][0, y, x] == 2
+    np.testing.assert_allclose(a["render_alphas"][0, y, x, 0], 1 - 0.01 ** 3, rtol=1e-6)
+    np.testing.assert_allclose(a["render_colors"][0, y, x], [0.99, 0.0099, 0.000099], rtol=1e-5)
+    assert b["last_ids"][0, y, x] == 0
+    np.testing.assert_allclose(b["render_colors"][0, y, x], [0.99, 0, 0], rtol=1e-6)
