@@ -700,8 +700,9 @@ __device__ __forceinline__ float4 lds128(uint32_t addr) {
     return v;
 }
 
-// Sums each buffered (entry, field) over the lanes that hold terms and adds
-// it to the splat's gradient with one atomic: lane t owns task t.
+// Sums each buffered (entry, field) over the warp's 32 lanes (a lane without
+// a pair wrote 0) and adds it to the splat's gradient with one atomic: lane
+// t owns task t.
 template <int CH, int F>
 __device__ __forceinline__ void flush_reduction(BwdWarpSmem<CH, F>& w, int nslots,
                                                 const FlushTask& task, int lane) {
