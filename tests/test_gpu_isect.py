@@ -190,3 +190,44 @@ def test_repeat_runs_bit_identical():
         b = gpu_isect(s, d)
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 127, 128, 129, 1003, 70_001])
+def test_tile_offsets_aligned_and_unaligned(n):
+    # four keys per thread with 16-byte loads when aligned, scalar loads when
+    # not; the key before a thread's first comes from the neighbouring lane:
+    # both give the oracle's offsets bit for bit, at every tail length
+    C, TW, TH = 2, 7, 5
+    tb = gs.gs_tile_bits(TW, TH)
+    rng = np.random.default_rng(n)
+    cam = rng.integers(0, C, n).astype(np.uint64)
+    tile = rng.integers(0, TW * TH, n).astype(np.uint64)
+    upper = np.sort((cam << np.uint64(tb)) | tile)
+    keys = (upper << np.uint64(32)) | rng.integers(0, 2**32, n, dtype=np.uint64)
+    ref = oracle.tile_offsets(keys, C, TW, TH)
+    buf = torch.from_numpy(np.concatenate([keys[:1], keys]).view(np.int64)).to(DEV)
+    for k in (buf[1:].clone(), buf[1:]):  # 16-byte aligned copy, then an 8-byte offset view
+        st = gs.new_status(DEV)
+        off = gs.gs_tile_offsets(k, C, TW, TH, d_status=st)
+        assert int(st.item()) == 0
+        np.testing.assert_array_equal(off.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("pos", [512, 513, 515, 516, 640, 999])
+def test_tile_offsets_errors_inside_long_lists(pos):
+    # an unsorted step or an out-of-grid key at group starts, ends and lane
+    # boundaries of the vector path is reported
+    C, TW, TH = 1, 8, 8
+    n = 1000
+    rng = np.random.default_rng(pos)
+    # one descending step at pos: tiles 10..20 before it, 0..9 from it on
+    unsorted = np.concatenate([np.sort(rng.integers(10, 21, pos)),
+                               np.sort(rng.integers(0, 10, n - pos))]).astype(np.uint64)
+    # keys from pos on all past the grid (and sorted, so no other error)
+    grid = np.sort(rng.integers(0, TW * TH, n)).astype(np.uint64)
+    grid[pos:] = np.uint64(TW * TH + 3)
+    for u, code in ((unsorted, 7), (grid, 3)):
+        keys = torch.from_numpy((u << np.uint64(32)).view(np.int64)).to(DEV)
+        st = gs.new_status(DEV)
+        gs.gs_tile_offsets(keys, C, TW, TH, d_status=st)
+        assert int(st.item()) == code, (code, pos)

@@ -21,8 +21,10 @@
 //                  tile word; the depth bits are attached by the last radix
 //                  pass (or k_widen), which reads them from the depths array
 //                  through L2.
-//   k_tile_ranges  one thread per sorted key: where the tile id changes, the
-//                  tiles in between get this key's position.
+//   k_tile_ranges  four consecutive sorted keys per thread (two 16-byte
+//                  loads when the keys are 16-byte aligned; the key before
+//                  them comes from the neighbouring lane): where the tile id
+//                  changes, the tiles in between get the key's position.
 #include <cstdint>
 
 #include "gs_device.cuh"
@@ -314,27 +316,66 @@ __device__ __forceinline__ int64_t flat_tile(uint64_t key, int C, int64_t per_ca
     return (int64_t)cam * per_camera + (int64_t)tile;
 }
 
+// Tile ids of positions i - 1 and i (position n is the end: every tile
+// after the last key starts there) -> offsets of the tiles in between.
+__device__ __forceinline__ void range_step(int64_t i, int64_t n, uint64_t prev_key,
+                                           uint64_t key, int C, int64_t per_camera,
+                                           int tile_bits, int32_t* __restrict__ offsets,
+                                           int32_t* d_status) {
+    const int64_t ntiles = (int64_t)C * per_camera;
+    bool ok_cur = true, ok_prev = true;
+    const int64_t cur = i < n ? flat_tile(key, C, per_camera, tile_bits, &ok_cur) : ntiles;
+    const int64_t prev = i > 0 ? flat_tile(prev_key, C, per_camera, tile_bits, &ok_prev) : -1;
+    if (!ok_cur) {
+        report(d_status, GS_ERR_KEY_OUT_OF_GRID);
+        return;
+    }
+    if (!ok_prev) return;  // reported by that key's own step
+    if (cur < prev) {
+        report(d_status, GS_ERR_UNSORTED);
+        return;
+    }
+    for (int64_t t = prev + 1; t <= cur && t < ntiles; ++t) offsets[t] = (int32_t)i;
+}
+
+template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
     k_tile_ranges(const uint64_t* __restrict__ keys, int64_t n, int C, int tile_width,
                   int tile_height, int tile_bits, int32_t* __restrict__ offsets,
                   int32_t* d_status) {
     const int64_t per_camera = (int64_t)tile_width * tile_height;
-    const int64_t ntiles = (int64_t)C * per_camera;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i <= n; i += stride) {
-        bool ok_cur = true, ok_prev = true;
-        int64_t cur = i < n ? flat_tile(keys[i], C, per_camera, tile_bits, &ok_cur) : ntiles;
-        int64_t prev = i > 0 ? flat_tile(keys[i - 1], C, per_camera, tile_bits, &ok_prev) : -1;
-        if (!ok_cur) {
-            report(d_status, GS_ERR_KEY_OUT_OF_GRID);
-            continue;
+    const int lane = threadIdx.x & 31;
+    const int64_t groups = (n + 1 + 3) / 4;  // positions 0 .. n, four per thread
+    const int64_t warps = (int64_t)gridDim.x * (kThreads / kWarp);
+    // whole warps step together, so every lane takes part in the shuffle
+    for (int64_t wg = ((int64_t)blockIdx.x * (kThreads / kWarp) + (threadIdx.x >> 5)) * kWarp;
+         wg < groups; wg += warps * kWarp) {
+        const int64_t g = wg + lane;
+        const int64_t p0 = 4 * g;
+        uint64_t k[4] = {0, 0, 0, 0};
+        if (VEC && p0 + 3 < n) {
+            const ulonglong2 a = reinterpret_cast<const ulonglong2*>(keys)[2 * g];
+            const ulonglong2 b = reinterpret_cast<const ulonglong2*>(keys)[2 * g + 1];
+            k[0] = a.x;
+            k[1] = a.y;
+            k[2] = b.x;
+            k[3] = b.y;
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (p0 + u < n) k[u] = keys[p0 + u];
         }
-        if (!ok_prev) continue;  // reported by that key's own thread
-        if (cur < prev) {
-            report(d_status, GS_ERR_UNSORTED);
-            continue;
+        // the key at p0 - 1 is the previous lane's last one (its group is
+        // complete whenever this one has a position <= n)
+        uint64_t before = __shfl_up_sync(0xffffffffu, k[3], 1);
+        if (lane == 0 && p0 > 0 && p0 <= n) before = keys[p0 - 1];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = p0 + u;
+            if (i > n) break;
+            range_step(i, n, u == 0 ? before : k[u - 1], k[u], C, per_camera, tile_bits,
+                       offsets, d_status);
         }
-        for (int64_t t = prev + 1; t <= cur && t < ntiles; ++t) offsets[t] = (int32_t)i;
     }
 }
 
@@ -407,8 +448,13 @@ void launch_widen(const uint32_t* k32, const int32_t* v32, const uint32_t* dbits
 
 void launch_tile_ranges(const uint64_t* keys, int64_t n, int C, int tile_width, int tile_height,
                         int tile_bits, int32_t* offsets, int32_t* d_status, cudaStream_t s) {
-    k_tile_ranges<<<grid_for(n + 1, 4), kThreads, 0, s>>>(keys, n, C, tile_width, tile_height,
-                                                          tile_bits, offsets, d_status);
+    const int grid = grid_for(n + 1, 4);
+    if ((reinterpret_cast<uintptr_t>(keys) & 15) == 0)
+        k_tile_ranges<true><<<grid, kThreads, 0, s>>>(keys, n, C, tile_width, tile_height,
+                                                       tile_bits, offsets, d_status);
+    else
+        k_tile_ranges<false><<<grid, kThreads, 0, s>>>(keys, n, C, tile_width, tile_height,
+                                                        tile_bits, offsets, d_status);
 }
 
 }  // namespace gs
