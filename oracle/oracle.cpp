@@ -40,6 +40,10 @@
 
 namespace {
 
+// Largest channel count (the library's limit; per-pixel channel arrays are
+// sized for it).
+constexpr int kMaxChannels = 1024;
+
 constexpr float kAlphaClamp = 0.99f;  // upper clamp of alpha (the 0.99 in the
                                       // path's statement; GS_ALPHA_CLAMP's header
                                       // is not on the pages)
@@ -301,7 +305,8 @@ int64_t orc_bin_splats(const float* means2d, const float* radii, int elliptical,
 //   stats[0] += pairs evaluated (entries visited, until the pixel stops)
 //   stats[1] += pairs composited
 //   stats[2] += pixels flagged near-tie (below)
-//   near_tie[pixel] = 1 when a decision was taken within a relative margin:
+//   near_tie[pixel] = the number of decisions (saturating at 255) taken
+//     within a relative margin:
 //     |alpha - cutoff| <= tie_rel * cutoff, 0 < |s| <= tie_rel, or
 //     |T - threshold| <= tie_rel_T * threshold after a composite.  At such
 //     pixels an exp or rounding-order difference of a few ulp can flip the
@@ -331,11 +336,11 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
     int64_t start = a.offsets[t];
     int64_t end = t + 1 < tiles ? a.offsets[t + 1] : a.n_isects;
     float T = 1.0f;
-    float rgb[64];
+    float rgb[kMaxChannels];
     for (int ch = 0; ch < a.channels; ++ch) rgb[ch] = 0.0f;
     int32_t last = -1;
     int64_t evaluated = 0, composited = 0;
-    bool tie = false;
+    int n_tie = 0;  // decisions taken within the margins
     bool masked = a.masks != nullptr && a.masks[t] == 0;
     if (!masked) {
         float px = (float)x + 0.5f, py = (float)y + 0.5f;
@@ -349,14 +354,14 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             bool pair_tie = s != 0.0f && std::fabs(s) <= tie_rel;
             if (!(s >= 0.0f)) {
                 if (pair_tie && tie_splats) tie_splats[g] = 1;
-                tie |= pair_tie;
+                n_tie += pair_tie ? 1 : 0;
                 continue;
             }
             float raw = a.opacities[g] * std::exp(-s);
             float alpha = raw > kAlphaClamp ? kAlphaClamp : raw;
             pair_tie |= std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff;
             if (pair_tie && tie_splats) tie_splats[g] = 1;
-            tie |= pair_tie;
+            n_tie += pair_tie ? 1 : 0;
             if (alpha < a.alpha_cutoff) continue;
             float w = T * alpha;
             const float* col = a.colors + (int64_t)a.channels * g;
@@ -366,7 +371,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             ++composited;
             if (std::fabs(T - a.transmittance_threshold) <=
                 tie_rel_T * a.transmittance_threshold) {
-                tie = true;
+                ++n_tie;
                 if (tie_splats) tie_splats[g] = 1;
             }
             if (T < a.transmittance_threshold) break;
@@ -382,9 +387,9 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
     if (stats) {
         stats[0] += evaluated;
         stats[1] += composited;
-        stats[2] += tie ? 1 : 0;
+        stats[2] += n_tie > 0 ? 1 : 0;
     }
-    if (near_tie) near_tie[p] = tie ? 1 : 0;
+    if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
 }
 
 // Renders every pixel (pixels == nullptr) or only the listed flat pixel
@@ -400,7 +405,7 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
                       float* render_colors, float* render_alphas, int32_t* last_ids,
                       int64_t* stats, uint8_t* near_tie, float tie_rel, float tie_rel_T,
                       uint8_t* tie_splats) {
-    if (channels < 1 || channels > 64) return 1;
+    if (channels < 1 || channels > kMaxChannels) return 1;
     FwdArgs a = {means2d,   conics,     colors,      opacities, backgrounds,
                  masks,     C,          N,           channels,  width,
                  height,    tile_size,  tile_width,  tile_height, offsets,
@@ -435,7 +440,7 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
                           const int32_t* flatten_ids, int64_t n_isects, double alpha_cutoff,
                           double transmittance_threshold, double* render_colors,
                           double* render_alphas, double* margins) {
-    if (channels < 1 || channels > 64) return 1;
+    if (channels < 1 || channels > kMaxChannels) return 1;
     (void)N;
     int64_t tiles = C * tile_height * tile_width;
     double m_cut = 1e30, m_clamp = 1e30, m_thr = 1e30;
@@ -445,7 +450,7 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
                 int64_t t = (c * tile_height + y / tile_size) * tile_width + x / tile_size;
                 int64_t start = offsets[t];
                 int64_t end = t + 1 < tiles ? offsets[t + 1] : n_isects;
-                double T = 1.0, rgb[64];
+                double T = 1.0, rgb[kMaxChannels];
                 for (int ch = 0; ch < channels; ++ch) rgb[ch] = 0.0;
                 double px = x + 0.5, py = y + 0.5;
                 for (int64_t j = start; j < end; ++j) {
@@ -500,8 +505,9 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
 // Every gradient output is zeroed first (the bridge allocates them zeroed).
 // Per-pair terms are float as listed; they are summed in double and rounded
 // to float once.  pixels/n_pixels restricts the walk to listed pixels.
-// near_tie (optional, per pixel) marks pixels where alpha was within tie_rel
-// of the cutoff or raw alpha within tie_rel of the clamp; tie_splats
+// near_tie (optional, per pixel) counts (saturating at 255) the pairs whose
+// alpha was within tie_rel of the cutoff or raw alpha within tie_rel of the
+// clamp; tie_splats
 // (optional, per splat) marks the splats of those pairs.
 // magnitudes (optional, double) receives, per gradient element, the sum of
 // the absolute values of its per-pair terms, laid out as grad_means2d (2CN),
@@ -518,7 +524,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                       float* grad_conics, float* grad_colors, float* grad_opacities,
                       float* grad_backgrounds, float* grad_means2d_abs, uint8_t* near_tie,
                       float tie_rel, double* magnitudes, uint8_t* tie_splats) {
-    if (channels < 1 || channels > 64) return 1;
+    if (channels < 1 || channels > kMaxChannels) return 1;
     int64_t CN = C * N;
     std::vector<double> gm(2 * CN, 0.0), gq(3 * CN, 0.0), gc((size_t)channels * CN, 0.0),
         go(CN, 0.0), gb((size_t)channels * C, 0.0), gma(2 * CN, 0.0);
@@ -544,8 +550,8 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
         int32_t last = last_ids[p];
         float Tc = 1.0f - ra;
         float Ta = 1.0f;
-        float rem[64];
-        bool tie = false;
+        float rem[kMaxChannels];
+        int n_tie = 0;
         for (int ch = 0; ch < channels; ++ch) {
             rem[ch] = backgrounds ? backgrounds[c * channels + ch] : 0.0f;
             if (grad_backgrounds) gb[c * channels + ch] += (double)(g_rgb[ch] * Tc);
@@ -567,7 +573,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                 bool pair_tie = std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff ||
                                 std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp;
                 if (pair_tie && tie_splats) tie_splats[g] = 1;
-                tie |= pair_tie;
+                n_tie += pair_tie ? 1 : 0;
             }
             if (!valid) continue;
             float Tb = Tc / (1.0f - alpha);
@@ -605,7 +611,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             Ta *= 1.0f - alpha;
             Tc = Tb;
         }
-        if (near_tie) near_tie[p] = tie ? 1 : 0;
+        if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
     }
     for (int64_t i = 0; i < 2 * CN; ++i) grad_means2d[i] = (float)gm[i];
     for (int64_t i = 0; i < 3 * CN; ++i) grad_conics[i] = (float)gq[i];

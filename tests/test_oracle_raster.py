@@ -442,3 +442,93 @@ def test_threshold_zero_never_stops_and_high_threshold_stops_at_first():
     np.testing.assert_allclose(a["render_colors"][0, y, x], [0.99, 0.0099, 0.000099], rtol=1e-5)
     assert b["last_ids"][0, y, x] == 0
     np.testing.assert_allclose(b["render_colors"][0, y, x], [0.99, 0, 0], rtol=1e-6)
+
+
+# ------------------------------------------------------------------- absgrad
+
+
+def test_absgrad_four_pixels_golden():
+    # one splat whose per-pixel mean-gradient terms change sign across the
+    # pixels: absgrad is the sum of their absolute values, not |their sum|
+    rows = read_golden("absgrad_four_pixels.txt")
+    pixels = [[float(v) for v in r[0]] for r in rows if len(r) == 1]
+    (gx, gy), (ax, ay) = [[float(v) for v in part] for part in rows[-1]]
+    s = _scene([[8.0, 8.0]], [[0.25, 0.0, 0.25]], [[1.0, 0.0, 0.0]], [0.5], [1.0], [3.0],
+               16, 16)
+    iso = _setup(s)
+    g_rgb = np.zeros((1, 16, 16, 3), np.float32)
+    for x, y, g in pixels:
+        g_rgb[0, int(y), int(x), 0] = g
+    g_a = np.zeros((1, 16, 16, 1), np.float32)
+    fwd = _fwd(s, iso)
+    got = _bwd(s, iso, fwd, g_rgb, g_a, absgrad=True)
+    np.testing.assert_allclose(got["grad_means2d"][0, 0], [gx, gy], rtol=1e-6)
+    np.testing.assert_allclose(got["grad_means2d_abs"][0, 0], [ax, ay], rtol=1e-6)
+
+
+@pytest.mark.parametrize("seed", [0, 3])
+def test_absgrad_is_sum_of_per_pixel_finite_differences(seed):
+    # absgrad of splat g = sum over pixels p of |dL_p/dmean_g|, where L_p is
+    # pixel p's share of the loss (g_p . rgb_p + g_a,p alpha_p).  Each
+    # per-pixel derivative is a central difference of the double-precision
+    # forward: one pair of forward runs per (splat, axis) gives the whole
+    # image, hence every pixel's difference at once
+    s, iso = _fd_scene(seed, C=1, N=10, W=32, H=32, sigma=(1.5, 5.0), opacity=(0.3, 0.95))
+    rng = np.random.default_rng(100 + seed)
+    g_rgb = rng.standard_normal((1, 32, 32, 3)).astype(np.float32)
+    g_a = rng.standard_normal((1, 32, 32, 1)).astype(np.float32)
+    got = _bwd(s, iso, _fwd(s, iso), g_rgb, g_a, absgrad=True)
+
+    def per_pixel_loss(means):
+        rgb, alpha, _ = oracle.rasterize_fwd_f64(
+            means, s.conics, s.colors, s.opacities, s.backgrounds, s.width, s.height,
+            s.tile_size, iso["offsets"], iso["ids"], float(s.alpha_cutoff),
+            float(s.transmittance_threshold))
+        return (rgb * g_rgb).sum(axis=-1) + alpha * g_a[..., 0]
+
+    h = 1e-5
+    base = s.means2d.astype(np.float64)
+    ref_abs = np.zeros_like(base)
+    ref_sum = np.zeros_like(base)
+    for n in range(s.N):
+        for k in range(2):
+            hi, lo = base.copy(), base.copy()
+            hi[0, n, k] += h
+            lo[0, n, k] -= h
+            fd = (per_pixel_loss(hi) - per_pixel_loss(lo)) / (2 * h)
+            ref_abs[0, n, k] = np.abs(fd).sum()
+            ref_sum[0, n, k] = fd.sum()
+    # the terms do change sign: |sum| is well below the sum of |terms|
+    assert (np.abs(ref_sum) < 0.5 * ref_abs).any()
+    scale = ref_abs.max()
+    np.testing.assert_allclose(got["grad_means2d_abs"], ref_abs, rtol=1e-3, atol=1e-5 * scale)
+    np.testing.assert_allclose(got["grad_means2d"], ref_sum, rtol=1e-3, atol=1e-5 * scale)
+
+
+def test_many_channels_reduce_to_three_channel_runs():
+    # channels are independent in the compositing and every gradient term is
+    # a per-channel sum: a 300-channel scene whose colours repeat one
+    # 3-channel scene 100 times renders that scene 100 times over, and its
+    # colour gradients are the 3-channel ones (with the upstream gradient
+    # repeated, the opacity and geometry gradients scale by 100)
+    s3 = scenes.random_small(12, C=1, N=40, W=48, H=32)
+    iso = _setup(s3)
+    rng = np.random.default_rng(7)
+    g3 = rng.standard_normal((1, 32, 48, 3)).astype(np.float32)
+    ga = np.zeros((1, 32, 48, 1), np.float32)
+    f3 = _fwd(s3, iso)
+    b3 = _bwd(s3, iso, f3, g3, ga)
+    s300 = scenes.random_small(12, C=1, N=40, W=48, H=32)
+    s300.colors = np.ascontiguousarray(np.tile(s3.colors, (1, 1, 100)))
+    s300.backgrounds = np.ascontiguousarray(np.tile(s3.backgrounds, (1, 100)))
+    f300 = _fwd(s300, iso)
+    assert f300["render_colors"].shape[-1] == 300
+    np.testing.assert_array_equal(f300["render_colors"],
+                                  np.tile(f3["render_colors"], (1, 1, 1, 100)))
+    np.testing.assert_array_equal(f300["last_ids"], f3["last_ids"])
+    b300 = _bwd(s300, iso, f300, np.tile(g3, (1, 1, 1, 100)), ga)
+    np.testing.assert_allclose(b300["grad_colors"], np.tile(b3["grad_colors"], (1, 1, 100)),
+                               rtol=1e-6, atol=1e-7)
+    for k in ("grad_opacities", "grad_means2d", "grad_conics"):
+        np.testing.assert_allclose(b300[k], 100 * b3[k].astype(np.float64), rtol=2e-4,
+                                   atol=1e-4 * np.abs(100 * b3[k]).max(), err_msg=k)
