@@ -9,8 +9,8 @@ step's CUDA events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle on bounded samples of the same
-workload (host cores; there is no other implementation of this path).
+--impl reference times the CPU oracle, one camera of the same workload per
+step, on the host cores (there is no other implementation of this path).
 N > 1 runs N independent replicas (one per rank, launched by torchrun);
 the path has no exchange step.
 """
@@ -31,25 +31,33 @@ import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
+# the OpenMP oracle's threads sleep between its calls instead of spinning
+os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")
 
 METRIC = "Msplat-isect/s + Mpixel/s fwd(+bwd) at 1 GB300; % HBM / FP32-SFU roofline"
 WORKLOADS = {
     2: "w2: 1 camera x 100,000 splats, 1024x1024, tile 16, elliptical radii",
     3: "w3: 4 cameras x 1,000,000 splats, 1920x1080, tile 16, elliptical radii",
     4: "w4: 1 camera x 6,000,000 splats, 3840x2160, tile 16, elliptical radii",
+    5: "w5: backward on the w2 scene, upstream gradients N(0,1) seed 1",
 }
 WORKLOAD = WORKLOADS[3]
-SM_COUNT = 152
-FP32_LANES = 128
-SM_MAX_MHZ = 2070.0
 L2_FLUSH_BYTES = 256 << 20
 
-# algorithmic FP32-pipe operations (FMA = 1) per pair, counted from the
-# per-pixel formulas of the compositing and its adjoint
-FWD_OPS_EVAL = 15     # dx, dy, quadratic form (9), o*exp, clamp, two tests
-FWD_OPS_COMP = 7      # T*alpha, 3 colour FMAs, 1-alpha, T update, threshold test
-BWD_OPS_EVAL = 15     # re-evaluation of alpha for every entry up to last_id
-BWD_OPS_VALID = 40    # recovery, colour/opacity/mean/conic terms, recurrences
+# Algorithmic work per pair, counted from the per-pixel formulas (FMA = one
+# operation):
+#   forward, per evaluated pair: dx, dy, the quadratic form, the exponent's
+#     scale, o * exp, the clamp and the two tests (13 FP32) + one ex2 (SFU);
+#     per composited pair: T alpha, three colour FMAs, the T update and the
+#     threshold test (6 FP32)
+#   backward, per valid pair: alpha re-evaluation, T_before recovery,
+#     colour / opacity / mean / conic terms and the recurrences (45 FP32) +
+#     one ex2 and one reciprocal (SFU)
+FWD_OPS_EVAL = 13
+FWD_OPS_COMP = 6
+FWD_SFU_EVAL = 1
+BWD_OPS_VALID = 45
+BWD_SFU_VALID = 2
 
 
 def _peaks():
@@ -359,15 +367,8 @@ def run_ours(args, rank, world, scene):
     path.gs.check_status(path.status, "warmup")
 
     # work measures for the roofline (outside the timed region)
-    counts = torch.zeros((s.C, s.height, s.width, 3), dtype=torch.int32, device=dev)
-    path.forward(pair_counts=counts)
-    n_eval = int(counts[..., 0].sum(dtype=torch.int64))
-    n_comp = int(counts[..., 1].sum(dtype=torch.int64))
-    bwd_eval = int(counts[..., 2].sum(dtype=torch.int64))
-    offs = path.offsets.reshape(-1).to(torch.int64)
-    ends = torch.cat([offs[1:], torch.tensor([path.I], device=dev)])
-    list_len = (ends - offs)
-    max_list = int(list_len.max())
+    work = work_counts(path)
+    max_list = work.pop("max_tile_list")
 
     if world > 1:
         dist.barrier()
@@ -402,70 +403,39 @@ def run_ours(args, rank, world, scene):
 
     proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
     bins = time_bins(path, max_list, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
+    I = path.I
+    del path
+    torch.cuda.empty_cache()
+
+    hbm_peak, peak_kind = _peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = measure_peaks(dev, sm_count)
+    others = {} if args.main_only else time_other_workloads(
+        dev, flush, peaks, hbm_peak, max(5, min(args.steps, 10)), max(args.warmup, 3))
 
     if rank != 0:
         return None
-
-    hbm_peak, peak_kind = _peaks()
     proj.update(achieved_gbs=round(proj["bytes"] / (proj["ms"] * 1e-3) / 1e9, 1))
     proj["frac"] = round(proj["achieved_gbs"] / hbm_peak, 4)
     bins.update(achieved_gbs=round(bins["bytes"] / (bins["ms"] * 1e-3) / 1e9, 1))
     bins["frac"] = round(bins["achieved_gbs"] / hbm_peak, 4)
     st = stage_ms.mean(axis=0)
-    names = ["isect_query", "isect_emit_sort", "tile_ranges", "raster_fwd", "raster_bwd"]
-    CN, I = s.C * s.N, path.I
-    tiles = s.C * s.tile_width * s.tile_height
-    from tile_gaussian_splat_gb300 import binding as gsb
-    key_bits = gsb.gs_tile_bits(s.tile_width, s.tile_height) + max(0, (s.C - 1).bit_length())
-    up_passes = (key_bits + 7) // 8
-    # algorithmic bytes: what each stage must read and write
-    # emit+sort: rects + depth histograms (read mean, radii, depth; write a
-    # 16-byte rect) 36 B/splat; depth sort 12 + 3 x 16 B/splat; emission
-    # (order + rect gather) 20 B/splat and an 8-byte key+id per intersection;
-    # camera|tile passes 16 B per intersection each, the last one 24 B (read
-    # 8, write the 12-byte output, gather 4 bytes of depth)
-    tile_pass_bytes = (16 * (up_passes - 1) + 24) if up_passes else 24
-    bytes_ = {
-        "isect_query": CN * (8 + 8 + 4),
-        "isect_emit_sort": CN * (36 + 60 + 20) + I * (8 + tile_pass_bytes),
-        "tile_ranges": I * 8 + tiles * 4,
-    }
     clk = clocks.summary()
-    mhz = SM_MAX_MHZ
-    alu_peak = SM_COUNT * FP32_LANES * mhz * 1e6
-    fwd_ops = FWD_OPS_EVAL * n_eval + FWD_OPS_COMP * n_comp
-    bwd_ops = BWD_OPS_EVAL * bwd_eval + BWD_OPS_VALID * n_comp
-    stages = {}
-    for i, n in enumerate(names):
-        e = {"ms": round(float(st[i]), 4)}
-        if n in bytes_:
-            gbs = bytes_[n] / (st[i] * 1e-3) / 1e9
-            e.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / hbm_peak, 4))
-        elif n == "raster_fwd":
-            a = fwd_ops / (st[i] * 1e-3)
-            e.update(bound="alu", achieved_tops=round(a / 1e12, 3), frac=round(a / alu_peak, 4),
-                     mpix_s=round(pixels / (st[i] * 1e-3) / 1e6, 1))
-        else:
-            a = bwd_ops / (st[i] * 1e-3)
-            e.update(bound="alu", achieved_tops=round(a / 1e12, 3), frac=round(a / alu_peak, 4),
-                     mpix_s=round(pixels / (st[i] * 1e-3) / 1e6, 1))
-        stages[n] = e
-    isect_ms = float(st[0] + st[1] + st[2])
-    dom = names[int(np.argmax(st))]
-    src = {"raster_fwd": "tile_gaussian_splat_gb300/csrc/raster.cu",
-           "raster_bwd": "tile_gaussian_splat_gb300/csrc/raster.cu"}.get(
-        dom, "tile_gaussian_splat_gb300/csrc/sort.cu")
+    stages = stage_report(s, I, st, work, peaks, hbm_peak)
+    dom = STAGES[int(np.argmax(st))]
     traffic = _traffic_for({"raster_fwd": "k_raster_fwd", "raster_bwd": "k_raster_bwd"}.get(
         dom, dom), 1)
     if dom in ("raster_fwd", "raster_bwd"):
         roof = {"bound": "alu", "kernel": "k_" + dom, "achieved": stages[dom]["achieved_tops"],
-                "peak": round(alu_peak / 1e12, 2), "unit": "Tops/s (FP32 pipe, FMA=1)",
-                "frac": stages[dom]["frac"], "traffic": traffic,
-                "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz"}
+                "peak": round(peaks["fp32_ops"] / 1e12, 2),
+                "unit": "Tops/s (FP32 pipe, FMA = 1 op)", "frac": stages[dom]["frac"],
+                "sfu_frac": stages[dom]["sfu_frac"], "traffic": traffic,
+                "peak_source": peaks["source"], "ops_per_pair": stages[dom]["ops_model"]}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": stages[dom]["achieved_gbs"],
                 "peak": hbm_peak, "unit": "GB/s", "frac": stages[dom]["frac"],
                 "traffic": traffic, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}
+    isect_ms = float(st[0] + st[1] + st[2])
     value = whole_job_rate(pixels, ms, world) / 1e6
     line = {
         "metric": METRIC,
@@ -480,32 +450,244 @@ def run_ours(args, rank, world, scene):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded workload 3 generator)",
-        "config": {"workload": WORKLOADS[args.workload], "C": s.C, "N": s.N, "width": s.width,
-                   "height": s.height, "tile_size": 16, "n_isects": I,
-                   "max_tile_list": max_list, "pixels_per_step": pixels,
-                   "l2": "flushed between steps (256 MB write outside the step events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(s, I, max_list, world),
         "msplat_isect_per_s": round(I / (isect_ms * 1e-3) / 1e6, 1),
         "mpixel_per_s_fwd": stages["raster_fwd"]["mpix_s"],
         "mpixel_per_s_bwd": stages["raster_bwd"]["mpix_s"],
         "stages": stages,
-        "work": {"pairs_evaluated_fwd": n_eval, "pairs_composited": n_comp,
-                 "pairs_evaluated_bwd": bwd_eval},
+        "isect_sort_ranges": isect_summary(s, I, st, hbm_peak),
+        "work": work,
         "roofline": roof,
+        "peaks": peaks,
         "project": proj,
         "bins": bins,
+        "workloads": others,
         "e2e": {"value": round(whole_job_rate(pixels, e2e, world) / 1e6, 2),
-                "unit": "Mpixel/s (pinned host inputs -> image + gradients on host, "
-                        "uploads/downloads overlapped with the previous/next step)",
+                "unit": "Mpixel/s",
+                "note": "pinned host inputs -> image + gradients on the host; uploads and "
+                        "downloads overlapped with the previous/next step",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e, 3)},
-        # per step: count, count word, rects + depth histograms, 4 depth
-        # passes, emit, the camera/tile passes, ranges, forward, backward
-        "gpu_launches": args.steps * (1 + 1 + 1 + 4 + 1 + up_passes + 1 + 1 + 1),
+        "gpu_launches": args.steps * launches_per_step(s),
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
     }
     return line
+
+
+STAGES = ["isect_query", "isect_emit_sort", "tile_ranges", "raster_fwd", "raster_bwd"]
+
+
+def launches_per_step(s):
+    """Kernels of one step: count, count word, rects + depth histograms, 4
+    depth passes, emit, the camera/tile passes, ranges, forward, backward."""
+    return 1 + 1 + 1 + 4 + 1 + up_passes(s) + 1 + 1 + 1
+
+
+def up_passes(s):
+    from tile_gaussian_splat_gb300 import binding as gsb
+    key_bits = gsb.gs_tile_bits(s.tile_width, s.tile_height) + max(0, (s.C - 1).bit_length())
+    return (key_bits + 7) // 8
+
+
+def impl_bytes(s, I):
+    """Bytes each intersection stage of this implementation must move:
+    query: mean 8 + radii 8 + count 4 per splat; emit+sort: rects + depth
+    histograms (read mean, radii, depth; write a 16-byte rect) 36 B/splat,
+    depth sort 12 + 3 x 16 B/splat, emission (order + rect gather) 20 B/splat
+    and an 8-byte key+id per intersection, camera|tile passes 16 B per
+    intersection each, the last one 24 B (read 8, write the 12-byte output,
+    gather 4 bytes of depth); ranges: 8 B per intersection + 4 B per tile."""
+    CN = s.C * s.N
+    up = up_passes(s)
+    tile_pass_bytes = (16 * (up - 1) + 24) if up else 24
+    return {"isect_query": CN * (8 + 8 + 4),
+            "isect_emit_sort": CN * (36 + 60 + 20) + I * (8 + tile_pass_bytes),
+            "tile_ranges": I * 8 + s.C * s.tile_width * s.tile_height * 4}
+
+
+def method_bytes(s, I):
+    """The method's own traffic as the pages' pipeline moves it (count + scan
+    24 B per splat; emission 24 B per splat + 12 B per intersection; an LSD
+    sort over the significant key bits: an 8-byte histogram read plus 24 B
+    per intersection per 8-bit pass; ranges 8 B per intersection + 4 B per
+    tile)."""
+    CN = s.C * s.N
+    from tile_gaussian_splat_gb300 import binding as gsb
+    key_bits = 32 + gsb.gs_tile_bits(s.tile_width, s.tile_height) + \
+        max(0, (s.C - 1).bit_length())
+    passes = (key_bits + 7) // 8
+    return {"isect_query": CN * 24,
+            "isect_emit_sort": CN * 24 + I * 12 + I * (8 + 24 * passes),
+            "tile_ranges": I * 8 + s.C * s.tile_width * s.tile_height * 4}
+
+
+def isect_summary(s, I, st, hbm_peak):
+    """Intersect + sort + ranges as one stage, under both byte models."""
+    ms = float(st[0] + st[1] + st[2])
+    out = {"ms": round(ms, 4), "msplat_isect_per_s": round(I / (ms * 1e-3) / 1e6, 1)}
+    for name, model in (("impl", impl_bytes(s, I)), ("method", method_bytes(s, I))):
+        b = sum(model.values())
+        gbs = b / (ms * 1e-3) / 1e9
+        out[f"bytes_{name}"] = int(b)
+        out[f"achieved_gbs_{name}"] = round(gbs, 1)
+        out[f"frac_{name}"] = round(gbs / hbm_peak, 4)
+    return out
+
+
+def stage_report(s, I, st, work, peaks, hbm_peak):
+    pixels = s.C * s.width * s.height
+    ib, mb = impl_bytes(s, I), method_bytes(s, I)
+    stages = {}
+    for i, n in enumerate(STAGES):
+        sec = float(st[i]) * 1e-3
+        e = {"ms": round(float(st[i]), 4)}
+        if n in ib:
+            gbs = ib[n] / sec / 1e9
+            e.update(bound="hbm", achieved_gbs=round(gbs, 1), frac=round(gbs / hbm_peak, 4),
+                     achieved_gbs_method=round(mb[n] / sec / 1e9, 1),
+                     frac_method=round(mb[n] / sec / 1e9 / hbm_peak, 4))
+        else:
+            if n == "raster_fwd":
+                ops = FWD_OPS_EVAL * work["pairs_evaluated_fwd"] + \
+                    FWD_OPS_COMP * work["pairs_composited"]
+                sfu = FWD_SFU_EVAL * work["pairs_evaluated_fwd"]
+                model = f"{FWD_OPS_EVAL} FP32 + {FWD_SFU_EVAL} SFU per evaluated pair, " \
+                        f"{FWD_OPS_COMP} FP32 per composited pair"
+                # the same count over every list entry up to each pixel's stop
+                # (entries the kernel skips as unreachable included)
+                ops_all = FWD_OPS_EVAL * work["pairs_to_termination"] + \
+                    FWD_OPS_COMP * work["pairs_composited"]
+                e["frac_all_entries"] = round(ops_all / sec / peaks["fp32_ops"], 4)
+            else:
+                ops = BWD_OPS_VALID * work["pairs_composited"]
+                sfu = BWD_SFU_VALID * work["pairs_composited"]
+                model = f"{BWD_OPS_VALID} FP32 + {BWD_SFU_VALID} SFU per valid pair"
+            e.update(bound="alu", achieved_tops=round(ops / sec / 1e12, 3),
+                     frac=round(ops / sec / peaks["fp32_ops"], 4),
+                     sfu_frac=round(sfu / sec / peaks["sfu_ops"], 4), ops_model=model,
+                     mpix_s=round(pixels / sec / 1e6, 1))
+        stages[n] = e
+    return stages
+
+
+def workload_config(s, I, max_list, world):
+    return {"workload": WORKLOADS[3] if s.C == 4 else s.name, "C": s.C, "N": s.N,
+            "width": s.width, "height": s.height, "tile_size": 16, "n_isects": int(I),
+            "max_tile_list": int(max_list), "pixels_per_step": s.C * s.width * s.height,
+            "l2": "flushed between steps (256 MB write outside the step events)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def measure_peaks(dev, sm_count):
+    """FP32 and ex2 throughput from the library's probes (gs_peak_probe),
+    timed with CUDA events on the launching stream, best of 5 after 2
+    warm-ups; 8 blocks of 256 threads per SM (64 warps)."""
+    import torch
+
+    from tile_gaussian_splat_gb300 import binding as gsb
+
+    blocks = sm_count * 8
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    res = {}
+    for kind, name, iters in ((0, "ffma", 20000), (1, "ffma2", 10000), (2, "ex2", 2500)):
+        best = None
+        for k in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            ops = gsb.gs_peak_probe(kind, iters, blocks, out)
+            b.record()
+            b.synchronize()
+            if k >= 2:
+                r = ops / (a.elapsed_time(b) * 1e-3)
+                best = r if best is None else max(best, r)
+        res[name] = best
+    fp32 = max(res["ffma"], res["ffma2"])
+    return {"fp32_ops": fp32, "sfu_ops": res["ex2"],
+            "ffma_tops": round(res["ffma"] / 1e12, 2), "ffma2_tops": round(res["ffma2"] / 1e12, 2),
+            "ex2_tops": round(res["ex2"] / 1e12, 3), "sm_count": sm_count,
+            "source": "measured: gs_peak_probe FFMA / packed FFMA2 / ex2.approx loops, "
+                      f"{sm_count} SMs x 64 warps, best of 5 (FP32 peak = the faster FMA form)"}
+
+
+def work_counts(path):
+    """Pairs of the step's forward and backward (one extra forward with the
+    pair counters, outside the timed region)."""
+    import torch
+
+    s, dev = path.s, path.dev
+    counts = torch.zeros((s.C, s.height, s.width, 3), dtype=torch.int32, device=dev)
+    path.forward(pair_counts=counts)
+    n_eval = int(counts[..., 0].sum(dtype=torch.int64))
+    n_comp = int(counts[..., 1].sum(dtype=torch.int64))
+    # entries up to each pixel's stop: the whole list, or up to its last id
+    # when T fell below the threshold
+    offs = path.offsets.reshape(-1).to(torch.int64)
+    ends = torch.cat([offs[1:], torch.tensor([path.I], device=dev)])
+    TW, TH = s.tile_width, s.tile_height
+    ys = torch.arange(s.height, device=dev) // 16
+    xs = torch.arange(s.width, device=dev) // 16
+    cs = torch.arange(s.C, device=dev)
+    t = (cs[:, None, None] * TH + ys[None, :, None]) * TW + xs[None, None, :]
+    start, end = offs[t], ends[t]
+    T = 1.0 - path.alpha[..., 0].to(torch.float64)
+    stopped = T < float(s.transmittance_threshold)
+    upto = torch.where(stopped, path.last.to(torch.int64) + 1 - start, end - start)
+    lens = ends - offs
+    return {"pairs_evaluated_fwd": n_eval, "pairs_composited": n_comp,
+            "pairs_to_termination": int(upto.clamp(min=0).sum()),
+            "max_tile_list": int(lens.max())}
+
+
+def time_steps(path, flush, steps, warmup):
+    """Per-stage CUDA-event times (ms) of `steps` steps, L2 flushed between."""
+    import torch
+
+    for _ in range(warmup):
+        path.step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for k in range(steps):
+        path.step(ev[k])
+        flush.zero_()
+    torch.cuda.synchronize()
+    return np.array([[ev[k][i].elapsed_time(ev[k][i + 1]) for i in range(5)]
+                     for k in range(steps)])
+
+
+def time_other_workloads(dev, flush, peaks, hbm_peak, steps, warmup):
+    """Workload 2 and workload 4 (the heavy-list scene) as whole steps, and
+    workload 5 (the backward on workload 2's scene) from workload 2's step."""
+    import torch
+
+    from tile_gaussian_splat_gb300 import scenes
+
+    out = {}
+    for k in (2, 4):
+        sc = scenes.workload(k)
+        path = Path(sc, dev)
+        st = time_steps(path, flush, steps, warmup)
+        path.gs.check_status(path.status, f"workload {k}")
+        work = work_counts(path)
+        m = st.mean(axis=0)
+        stages = stage_report(sc, path.I, m, work, peaks, hbm_peak)
+        px = sc.C * sc.width * sc.height
+        out[f"w{k}"] = {"workload": WORKLOADS[k], "ms_per_step": round(float(m.sum()), 4),
+                        "mpixel_per_s": round(px / (m.sum() * 1e-3) / 1e6, 1),
+                        "n_isects": path.I, "max_tile_list": work["max_tile_list"],
+                        "isect_sort_ranges": isect_summary(sc, path.I, m, hbm_peak),
+                        "stages": stages, "work": work}
+        if k == 2:
+            b = stages["raster_bwd"]
+            out["w5"] = {"workload": WORKLOADS[5], "ms": b["ms"], "mpixel_per_s": b["mpix_s"],
+                         "achieved_tops": b["achieved_tops"], "frac": b["frac"],
+                         "sfu_frac": b["sfu_frac"], "valid_pairs": work["pairs_composited"],
+                         "note": "the backward stage of the w2 step (trace-driven, upstream "
+                                 "gradients N(0,1) seed 1)"}
+        del path
+        torch.cuda.empty_cache()
+    return out
 
 
 def time_projection(dev, flush, warmup, steps):
@@ -584,78 +766,104 @@ def time_bins(path, max_list, flush, warmup, steps):
 # -------------------------------------------------------- oracle arm
 
 
-def cpu_sample(scene, budget_tiles=1000, seed=0):
-    """Times the oracle on a bounded sample of the workload: intersect + sort +
-    offsets of camera 0 (all its splats), forward + backward on budget_tiles
-    tiles spread over that camera.  Returns (seconds per full step estimate,
-    description)."""
+def oracle_camera_step(scene, c, g_rgb, g_a):
+    """One step of the oracle on camera c of the workload: intersect + sort +
+    offsets of its N splats (single-threaded C++), then the forward and the
+    backward over every pixel of that camera (the OpenMP build of the same
+    oracle, pixels handed out dynamically to every host core).  Returns
+    (seconds, intersections, isect seconds)."""
+    import oracle
+
+    s = scene
+    sl = slice(c, c + 1)
+    t0 = time.perf_counter()
+    tpg, keys, ids = oracle.isect_tiles(s.means2d[sl], s.radii[sl], s.depths[sl], 16,
+                                        s.tile_width, s.tile_height)
+    offsets = oracle.tile_offsets(keys, 1, s.tile_width, s.tile_height)
+    t_isect = time.perf_counter() - t0
+    fwd = oracle.rasterize_fwd(s.means2d[sl], s.conics[sl], s.colors[sl], s.opacities[sl], None,
+                               None, s.width, s.height, 16, offsets, ids, s.alpha_cutoff,
+                               s.transmittance_threshold, omp=True)
+    oracle.rasterize_bwd(s.means2d[sl], s.conics[sl], s.colors[sl], s.opacities[sl], None, None,
+                         s.width, s.height, 16, offsets, ids, s.alpha_cutoff,
+                         fwd["render_alphas"], fwd["last_ids"], g_rgb[sl], g_a[sl], omp=True)
+    return time.perf_counter() - t0, int(keys.size), t_isect
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(scene):
+    """The oracle timed on the host cores: one camera of the workload through
+    the whole path (see oracle_camera_step), about 2-10 s."""
     import oracle
     from tile_gaussian_splat_gb300 import scenes
 
-    s = scene
-    c = 0
-    m, r, dpt = s.means2d[c:c + 1], s.radii[c:c + 1], s.depths[c:c + 1]
-    t0 = time.perf_counter()
-    tpg, keys, ids = oracle.isect_tiles(m, r, dpt, 16, s.tile_width, s.tile_height)
-    offsets = oracle.tile_offsets(keys, 1, s.tile_width, s.tile_height)
-    t_isect = time.perf_counter() - t0
-    rng = np.random.default_rng(seed)
-    ntiles = s.tile_width * s.tile_height
-    tiles = rng.choice(ntiles, min(budget_tiles, ntiles), replace=False)
-    pix = []
-    for t in tiles:
-        ty, tx = divmod(int(t), s.tile_width)
-        for y in range(ty * 16, min(s.height, ty * 16 + 16)):
-            for x in range(tx * 16, min(s.width, tx * 16 + 16)):
-                pix.append(y * s.width + x)
-    pix = np.array(pix, np.int64)
-    g_rgb, g_a = scenes.upstream_grads(1, s.height, s.width, seed=1)
-    arrs = dict(means2d=m, conics=s.conics[c:c + 1], colors=s.colors[c:c + 1],
-                opacities=s.opacities[c:c + 1])
-    t0 = time.perf_counter()
-    fwd = oracle.rasterize_fwd(arrs["means2d"], arrs["conics"], arrs["colors"],
-                               arrs["opacities"], None, None, s.width, s.height, 16, offsets, ids,
-                               s.alpha_cutoff, s.transmittance_threshold, pixels=pix)
-    oracle.rasterize_bwd(arrs["means2d"], arrs["conics"], arrs["colors"], arrs["opacities"],
-                         None, None, s.width, s.height, 16, offsets, ids, s.alpha_cutoff,
-                         fwd["render_alphas"], fwd["last_ids"], g_rgb, g_a, pixels=pix)
-    t_raster = time.perf_counter() - t0
-    pixels = s.C * s.width * s.height
-    est = t_isect * s.C + t_raster / pix.size * pixels
-    desc = (f"oracle, 1 thread: isect+sort+offsets of camera 0 ({s.N} splats, {keys.size} "
-            f"keys) in {t_isect:.2f} s, x{s.C} cameras; fwd+bwd of {pix.size} pixels "
-            f"({tiles.size} random tiles) in {t_raster:.2f} s, scaled to {pixels} pixels")
-    return est, desc
+    g_rgb, g_a = scenes.upstream_grads(scene.C, scene.height, scene.width, seed=1)
+    sec, keys, t_isect = oracle_camera_step(scene, 0, g_rgb, g_a)
+    px = scene.width * scene.height
+    return {"value": round(px / sec / 1e6, 6), "unit": "Mpixel/s", "cores": oracle.threads_omp(),
+            "kind": "oracle",
+            "sample": f"oracle on camera 0 of {scene.C}: isect+sort+offsets of {scene.N} splats "
+                      f"({keys} keys, 1 thread, {t_isect:.2f} s), forward + backward of all "
+                      f"{px} pixels (OpenMP build, {oracle.threads_omp()} threads, dynamic "
+                      f"schedule over pixels); {sec:.2f} s",
+            "cpu": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args, rank, world):
+    """The oracle arm: each step runs the whole path on one camera of the
+    workload (cameras in turn), isect single-threaded and the raster on every
+    host core; the value is that camera's pixels over the step's own time."""
     if rank != 0:
         return None
+    import oracle
     from tile_gaussian_splat_gb300 import scenes
 
     scene = scenes.workload3()
-    pixels = scene.C * scene.width * scene.height
-    for _ in range(max(args.warmup, 3) if args.warmup else 0):
-        cpu_sample(scene, budget_tiles=8)
+    s = scene
+    # the workload's intersection count and longest list (set-up, not timed)
+    _, keys, _ = oracle.isect_tiles(s.means2d, s.radii, s.depths, 16, s.tile_width,
+                                    s.tile_height)
+    offs = oracle.tile_offsets(keys, s.C, s.tile_width, s.tile_height).reshape(-1)
+    I = int(keys.size)
+    max_list = int(np.diff(np.append(offs.astype(np.int64), I)).max())
+    del keys
+    g_rgb, g_a = scenes.upstream_grads(s.C, s.height, s.width, seed=1)
+    for k in range(args.warmup):
+        oracle_camera_step(s, k % s.C, g_rgb, g_a)
     per_step = []
-    desc = ""
     for k in range(args.steps):
-        est, desc = cpu_sample(scene, budget_tiles=24, seed=k)
-        per_step.append(est)
+        sec, _, _ = oracle_camera_step(s, k % s.C, g_rgb, g_a)
+        per_step.append(sec)
     sec = float(np.mean(per_step))
-    value = pixels / sec / 1e6
+    px = s.width * s.height
+    value = px / sec / 1e6
     return {
         "impl": "reference",
         "metric": METRIC,
         "value": round(value, 6),
         "unit": "Mpixel/s (whole step: isect+sort+ranges+fwd+bwd)",
-        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded workload 3 generator)",
-        "config": {"workload": WORKLOAD, "C": scene.C, "N": scene.N, "width": scene.width,
-                   "height": scene.height, "tile_size": 16},
-        "cpu_baseline": {"value": round(value, 6), "unit": "Mpixel/s", "cores": 1,
-                         "kind": "oracle", "sample": desc},
+        "config": workload_config(s, I, max_list, 1),
+        "cpu_baseline": {"value": round(value, 6), "unit": "Mpixel/s",
+                         "cores": oracle.threads_omp(), "kind": "oracle",
+                         "sample": f"each step: one camera of {s.C} in turn ({s.N} splats, "
+                                   f"{px} pixels): isect+sort+offsets single-threaded, "
+                                   f"forward + backward on {oracle.threads_omp()} threads "
+                                   "(OpenMP, dynamic schedule over pixels)",
+                         "cpu": cpu_model(), "nproc": os.cpu_count()},
         "e2e": {"value": round(value, 6), "unit": "Mpixel/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -668,6 +876,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--main-only", action="store_true",
+                    help="skip the workload 2/4/5 lines (profiling runs)")
     ap.add_argument("--workload", type=int, default=3, choices=[2, 3, 4],
                     help="3 is the measured workload; 2 and 4 serve profiling")
     args = ap.parse_args()
@@ -684,10 +894,8 @@ def main():
         sc = scenes.workload(args.workload)
         cpu = None
         if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == 3:
-            # before any CUDA work: the oracle runs in this process, single thread
-            est, desc = cpu_sample(sc)
-            cpu = {"value": round(sc.C * sc.width * sc.height / est / 1e6, 6),
-                   "unit": "Mpixel/s", "cores": 1, "kind": "oracle", "sample": desc}
+            # before any CUDA work: the oracle runs in this process
+            cpu = cpu_baseline(sc)
         line = run_ours(args, rank, world, sc)
         if line is not None:
             line["cpu_baseline"] = cpu

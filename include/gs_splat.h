@@ -368,8 +368,8 @@ int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit,
  * Same result as gs_sort_pairs (stable, ascending by key bits
  * [begin_bit, end_bit), in place), but it allocates nothing and takes no
  * workspace: its scratch space is one fixed device array inside the library
- * (about 17.6 MB, held on every GPU that loads the library until the process
- * exits), sized for n <= GS_SORT_NOALLOC_MAX_PAIRS.
+ * (20,980,224 bytes, about 21.0 MB, held on every GPU that loads the library
+ * until the process exits), sized for n <= GS_SORT_NOALLOC_MAX_PAIRS.
  *   - n > GS_SORT_NOALLOC_MAX_PAIRS returns GS_ERR_CAPACITY, nothing enqueued.
  *   - It runs on the current device.  Its first call on a device looks up the
  *     array's device address there (cudaGetSymbolAddress); make that first
@@ -383,6 +383,47 @@ int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit,
 int gs_sort_pairs_noalloc(uint64_t* keys, int32_t* values, int64_t n,
                           int begin_bit, int end_bit, int32_t* d_status,
                           void* stream);
+
+/*
+ * gs_peak_probe -- a measurement helper, not part of the path (the pages give
+ * no peak figures): a kernel of blocks x 256 threads, each running 8
+ * independent chains of `iters` x 4 operations of one kind:
+ *   kind 0: scalar FP32 fused multiply-add (x <- 0.999 x + 0.001)
+ *   kind 1: packed f32x2 fused multiply-add (the same on both halves)
+ *   kind 2: the ex2.approx special-function instruction (x <- 2^-x)
+ * out float32 (blocks * 256) receives each thread's sum of its chains (so no
+ * work is dead); *h_ops (host) the number of operations enqueued (an FMA is
+ * one operation, a packed FMA two).  Timing it with events on `stream` gives
+ * the GPU's FP32-pipe and special-function throughput, the denominators of
+ * the raster kernels' roofline fractions.  Asynchronous.
+ */
+int gs_peak_probe(int kind, int iters, int blocks, float* out, int64_t* h_ops, void* stream);
+
+/*
+ * gs_debug_sort_wait_timeout -- test hook for the failure path of the
+ * bounded inter-block waits (the pages' sort, gsplat 1.0.0, intersections.c,
+ * gs_radix_sort_without_gvl, returns an error instead of aborting; this makes
+ * the library's equivalent error happen on purpose, without a fault).
+ * Runs the histogram and ONE sorting pass of gs_sort_pairs (digit bits 0..7)
+ * over keys uint64 (n), values int32 (n), with two changes:
+ *   - the pass's block ticket starts at ticket_start (1 .. 64) instead of 0,
+ *     so the look-back words of virtual blocks 0 .. ticket_start - 1 are
+ *     never published;
+ *   - a look-back wait polls a word at most wait_polls (1 .. 2^20) times,
+ *     instead of 2^22, before it gives up.
+ * The first block then waits on a word that nobody writes, gives up after
+ * wait_polls polls and stores GS_ERR_TIMEOUT in *d_status (required, device)
+ * and in the workspace's abort flag; every other waiting block sees that flag
+ * within 256 polls; every block returns.  Nothing hangs and nothing faults:
+ * the pass writes only inside keys/values' [0, n) ranges and the workspace,
+ * but what it writes there is unspecified (callers keep a copy).
+ * workspace: at least gs_sort_workspace_size(n + ticket_start * 2048) bytes.
+ * Returns GS_OK once enqueued (errors of the arguments as usual); the status
+ * word shows the timeout after the stream is synchronised.  1 <= n < 2^30.
+ */
+int gs_debug_sort_wait_timeout(uint64_t* keys, int32_t* values, int64_t n, int ticket_start,
+                               int wait_polls, void* workspace, size_t workspace_bytes,
+                               int32_t* d_status, void* stream);
 
 #ifdef __cplusplus
 }

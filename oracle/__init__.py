@@ -17,6 +17,7 @@ import numpy as np
 from . import build as _build
 
 _lib = None
+_lib_omp = None
 
 P = ct.c_void_p
 I64 = ct.c_int64
@@ -25,43 +26,58 @@ F32 = ct.c_float
 F64 = ct.c_double
 
 
-def lib():
-    global _lib
+def lib(omp=False):
+    """The single-threaded oracle, or (omp=True) its OpenMP build, which runs
+    the raster pixel loops on every host core (timing only)."""
+    global _lib, _lib_omp
+    if omp:
+        if _lib_omp is None:
+            _lib_omp = _load(_build.build(omp=True))
+        return _lib_omp
     if _lib is None:
-        path = _build.build()
-        L = ct.CDLL(path)
-        L.orc_tile_bits.argtypes = [I32, I32]
-        L.orc_tile_bits.restype = I32
-        L.orc_bounds.argtypes = [P, P, I32, I64, I64, I32, I32, I32, P]
-        L.orc_bounds.restype = None
-        L.orc_isect_count.argtypes = [P, P, I32, I64, I64, I32, I32, I32, P]
-        L.orc_isect_count.restype = I64
-        L.orc_isect_emit.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, P, P, I64]
-        L.orc_isect_emit.restype = I64
-        L.orc_sort_stable.argtypes = [P, P, I64]
-        L.orc_sort_stable.restype = None
-        L.orc_sort_lsd.argtypes = [P, P, I64]
-        L.orc_sort_lsd.restype = I32
-        L.orc_tile_offsets.argtypes = [P, I64, I32, I32, I32, P]
-        L.orc_tile_offsets.restype = I32
-        L.orc_rasterize_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
-                                        P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32, F32,
-                                        P]
-        L.orc_rasterize_fwd.restype = I32
-        L.orc_rasterize_fwd_f64.argtypes = [P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
-                                            P, P, I64, F64, F64, P, P, P]
-        L.orc_rasterize_fwd_f64.restype = I32
-        L.orc_rasterize_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
-                                        P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
-                                        F32, P, P]
-        L.orc_rasterize_bwd.restype = I32
-        L.orc_bin_splats.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, I64, P, P]
-        L.orc_bin_splats.restype = I64
-        L.orc_project.argtypes = [P, P, P, P, I64, I64, I32, I32, F32, F32, F32, F32, I32, P, P,
-                                  P, P, P]
-        L.orc_project.restype = I32
-        _lib = L
+        _lib = _load(_build.build())
     return _lib
+
+
+def threads_omp():
+    """Threads the OpenMP build uses (OMP_NUM_THREADS, else every core)."""
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def _load(path):
+    L = ct.CDLL(path)
+    L.orc_tile_bits.argtypes = [I32, I32]
+    L.orc_tile_bits.restype = I32
+    L.orc_bounds.argtypes = [P, P, I32, I64, I64, I32, I32, I32, P]
+    L.orc_bounds.restype = None
+    L.orc_isect_count.argtypes = [P, P, I32, I64, I64, I32, I32, I32, P]
+    L.orc_isect_count.restype = I64
+    L.orc_isect_emit.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, P, P, I64]
+    L.orc_isect_emit.restype = I64
+    L.orc_sort_stable.argtypes = [P, P, I64]
+    L.orc_sort_stable.restype = None
+    L.orc_sort_lsd.argtypes = [P, P, I64]
+    L.orc_sort_lsd.restype = I32
+    L.orc_tile_offsets.argtypes = [P, I64, I32, I32, I32, P]
+    L.orc_tile_offsets.restype = I32
+    L.orc_rasterize_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
+                                    P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32, F32,
+                                    P]
+    L.orc_rasterize_fwd.restype = I32
+    L.orc_rasterize_fwd_f64.argtypes = [P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
+                                        P, P, I64, F64, F64, P, P, P]
+    L.orc_rasterize_fwd_f64.restype = I32
+    L.orc_rasterize_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
+                                    P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
+                                    F32, P, P]
+    L.orc_rasterize_bwd.restype = I32
+    L.orc_bin_splats.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, I64, P, P]
+    L.orc_bin_splats.restype = I64
+    L.orc_project.argtypes = [P, P, P, P, I64, I64, I32, I32, F32, F32, F32, F32, I32, P, P,
+                              P, P, P]
+    L.orc_project.restype = I32
+    return L
 
 
 def _ptr(a):
@@ -138,7 +154,7 @@ def tile_offsets(keys, C, tile_width, tile_height):
 
 def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, transmittance_threshold,
-                  pixels=None, tie_rel=0.0, tie_rel_T=None, out=None):
+                  pixels=None, tie_rel=0.0, tie_rel_T=None, out=None, omp=False):
     """Forward compositing.  Returns dict(render_colors (C,H,W,ch),
     render_alphas (C,H,W,1), last_ids (C,H,W), stats [evaluated, composited,
     near-tie pixels], near_tie (C,H,W) uint8)."""
@@ -161,7 +177,7 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
     out["tie_splats"] = np.zeros((C, N), np.uint8)
     stats = np.zeros(3, np.int64)
     px = None if pixels is None else _c(pixels, np.int64)
-    rc = lib().orc_rasterize_fwd(
+    rc = lib(omp).orc_rasterize_fwd(
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
         _ptr(masks), C, N, ch, width, height, tile_size, TW, TH, _ptr(offsets),
         _ptr(flatten_ids), flatten_ids.size, float(alpha_cutoff), float(transmittance_threshold),
@@ -203,7 +219,7 @@ def rasterize_fwd_f64(means2d, conics, colors, opacities, backgrounds, width, he
 def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, render_alphas, last_ids,
                   grad_render_colors, grad_render_alphas, want_grad_backgrounds=None,
-                  absgrad=False, pixels=None, tie_rel=0.0, magnitudes=False):
+                  absgrad=False, pixels=None, tie_rel=0.0, magnitudes=False, omp=False):
     """Backward.  Returns dict(grad_means2d, grad_conics, grad_colors,
     grad_opacities, grad_backgrounds (or None), grad_means2d_abs (or None),
     near_tie (C,H,W) uint8, and with magnitudes=True mag_* arrays: per
@@ -235,7 +251,7 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                tie_splats=np.zeros((C, N), np.uint8))
     px = None if pixels is None else _c(pixels, np.int64)
     mags = np.zeros((6 + ch) * C * N, np.float64) if magnitudes else None
-    rc = lib().orc_rasterize_bwd(
+    rc = lib(omp).orc_rasterize_bwd(
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
         _ptr(masks), C, N, ch, width, height, tile_size, TW, TH, _ptr(offsets),
         _ptr(flatten_ids), flatten_ids.size, float(alpha_cutoff), _ptr(render_alphas),

@@ -13,20 +13,30 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRCS = [os.path.join(HERE, "oracle.cpp"), os.path.join(HERE, "project.cpp")]
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboracle.so")
+# the same sources with OpenMP: pixels on every host core (timing only; the
+# tests load the single-threaded LIB)
+LIB_OMP = os.path.join(OUT_DIR, "liboracle_omp.so")
 
 FLAGS = ["-std=c++17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
-def build(force: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
-    if (not force and os.path.exists(LIB)
-            and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SRCS)):
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["g++", *FLAGS, *SRCS, "-o", tmp]
+def _build_one(out, extra, force):
+    if (not force and os.path.exists(out)
+            and all(os.path.getmtime(out) >= os.path.getmtime(s) for s in SRCS)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", *FLAGS, *extra, *SRCS, "-o", tmp]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False, omp: bool = False) -> str:
+    """Builds both libraries; returns the path of the one asked for."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    _build_one(LIB, [], force)
+    _build_one(LIB_OMP, ["-fopenmp"], force)
+    return LIB_OMP if omp else LIB
 
 
 if __name__ == "__main__":

@@ -44,7 +44,33 @@ namespace {
 // sized for it).
 constexpr int kMaxChannels = 1024;
 
-constexpr float kAlphaClamp = 0.99f;  // upper clamp of alpha (the 0.99 in the
+constexpr float kAlphaClamp = 0.99f;
+
+// Accumulation into shared sums.  The plain build (liboracle.so, the one the
+// tests load) is single-threaded and adds in pixel order.  The OpenMP build
+// (liboracle_omp.so, compiled from this same file with -fopenmp, used only to
+// time the oracle on all host cores) runs pixels on several threads, so its
+// adds and flag stores are atomic.
+inline void acc(double& dst, double v) {
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+    dst += v;
+}
+
+inline void acc_i64(int64_t& dst, int64_t v) {
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+    dst += v;
+}
+
+inline void set_flag(uint8_t& f) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+    f = 1;
+}  // upper clamp of alpha (the 0.99 in the
                                       // path's statement; GS_ALPHA_CLAMP's header
                                       // is not on the pages)
 
@@ -353,14 +379,14 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             float s = 0.5f * (q[0] * dx * dx + q[2] * dy * dy) + q[1] * dx * dy;
             bool pair_tie = s != 0.0f && std::fabs(s) <= tie_rel;
             if (!(s >= 0.0f)) {
-                if (pair_tie && tie_splats) tie_splats[g] = 1;
+                if (pair_tie && tie_splats) set_flag(tie_splats[g]);
                 n_tie += pair_tie ? 1 : 0;
                 continue;
             }
             float raw = a.opacities[g] * std::exp(-s);
             float alpha = raw > kAlphaClamp ? kAlphaClamp : raw;
             pair_tie |= std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff;
-            if (pair_tie && tie_splats) tie_splats[g] = 1;
+            if (pair_tie && tie_splats) set_flag(tie_splats[g]);
             n_tie += pair_tie ? 1 : 0;
             if (alpha < a.alpha_cutoff) continue;
             float w = T * alpha;
@@ -372,7 +398,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             if (std::fabs(T - a.transmittance_threshold) <=
                 tie_rel_T * a.transmittance_threshold) {
                 ++n_tie;
-                if (tie_splats) tie_splats[g] = 1;
+                if (tie_splats) set_flag(tie_splats[g]);
             }
             if (T < a.transmittance_threshold) break;
         }
@@ -385,9 +411,9 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
     out_alpha[p] = 1.0f - T;
     out_last[p] = last;
     if (stats) {
-        stats[0] += evaluated;
-        stats[1] += composited;
-        stats[2] += n_tie > 0 ? 1 : 0;
+        acc_i64(stats[0], evaluated);
+        acc_i64(stats[1], composited);
+        acc_i64(stats[2], n_tie > 0 ? 1 : 0);
     }
     if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
 }
@@ -411,12 +437,20 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
                  height,    tile_size,  tile_width,  tile_height, offsets,
                  flatten_ids, n_isects, alpha_cutoff, transmittance_threshold};
     if (pixels == nullptr) {
+        // OpenMP build: rows of pixels handed out dynamically (list lengths,
+        // and so the work per row, vary a lot)
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+#endif
         for (int64_t c = 0; c < C; ++c)
             for (int y = 0; y < height; ++y)
                 for (int x = 0; x < width; ++x)
                     fwd_pixel(a, c, x, y, render_colors, render_alphas, last_ids, stats,
                               near_tie, tie_rel, tie_rel_T, tie_splats);
     } else {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
         for (int64_t k = 0; k < n_pixels; ++k) {
             int64_t p = pixels[k];
             int64_t c = p / ((int64_t)width * height);
@@ -537,6 +571,9 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
     int64_t tiles = C * tile_height * tile_width;
     int64_t HW = (int64_t)width * height;
     int64_t count = pixels ? n_pixels : C * HW;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
     for (int64_t k = 0; k < count; ++k) {
         int64_t p = pixels ? pixels[k] : k;
         int64_t c = p / HW;
@@ -554,7 +591,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
         int n_tie = 0;
         for (int ch = 0; ch < channels; ++ch) {
             rem[ch] = backgrounds ? backgrounds[c * channels + ch] : 0.0f;
-            if (grad_backgrounds) gb[c * channels + ch] += (double)(g_rgb[ch] * Tc);
+            if (grad_backgrounds) acc(gb[c * channels + ch], (double)(g_rgb[ch] * Tc));
         }
         if (masks != nullptr && masks[t] == 0) continue;
         float px = (float)x + 0.5f, py = (float)y + 0.5f;
@@ -572,7 +609,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             if (last >= j && s >= 0.0f) {
                 bool pair_tie = std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff ||
                                 std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp;
-                if (pair_tie && tie_splats) tie_splats[g] = 1;
+                if (pair_tie && tie_splats) set_flag(tie_splats[g]);
                 n_tie += pair_tie ? 1 : 0;
             }
             if (!valid) continue;
@@ -581,30 +618,30 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             const float* col = colors + (int64_t)channels * g;
             float dot = 0.0f;
             for (int ch = 0; ch < channels; ++ch) {
-                gc[(int64_t)channels * g + ch] += (double)(g_rgb[ch] * vis);
-                if (mag_c) mag_c[(int64_t)channels * g + ch] += std::fabs((double)(g_rgb[ch] * vis));
+                acc(gc[(int64_t)channels * g + ch], (double)(g_rgb[ch] * vis));
+                if (mag_c) acc(mag_c[(int64_t)channels * g + ch], std::fabs((double)(g_rgb[ch] * vis)));
                 dot += g_rgb[ch] * (col[ch] - rem[ch]);
             }
             float g_alpha = Tb * (dot + g_a * Ta);
             float g_raw = raw < kAlphaClamp ? g_alpha : 0.0f;
-            go[g] += (double)(g_raw * resp);
+            acc(go[g], (double)(g_raw * resp));
             float g_s = -g_raw * raw;
             float gmx = g_s * (q[0] * dx + q[1] * dy);
             float gmy = g_s * (q[2] * dy + q[1] * dx);
-            gm[2 * g] += (double)gmx;
-            gm[2 * g + 1] += (double)gmy;
-            gma[2 * g] += (double)std::fabs(gmx);
-            gma[2 * g + 1] += (double)std::fabs(gmy);
-            gq[3 * g] += (double)(g_s * 0.5f * dx * dx);
-            gq[3 * g + 1] += (double)(g_s * dx * dy);
-            gq[3 * g + 2] += (double)(g_s * 0.5f * dy * dy);
+            acc(gm[2 * g], (double)gmx);
+            acc(gm[2 * g + 1], (double)gmy);
+            acc(gma[2 * g], (double)std::fabs(gmx));
+            acc(gma[2 * g + 1], (double)std::fabs(gmy));
+            acc(gq[3 * g], (double)(g_s * 0.5f * dx * dx));
+            acc(gq[3 * g + 1], (double)(g_s * dx * dy));
+            acc(gq[3 * g + 2], (double)(g_s * 0.5f * dy * dy));
             if (magnitudes) {
-                mag_m[2 * g] += std::fabs((double)gmx);
-                mag_m[2 * g + 1] += std::fabs((double)gmy);
-                mag_q[3 * g] += std::fabs((double)(g_s * 0.5f * dx * dx));
-                mag_q[3 * g + 1] += std::fabs((double)(g_s * dx * dy));
-                mag_q[3 * g + 2] += std::fabs((double)(g_s * 0.5f * dy * dy));
-                mag_o[g] += std::fabs((double)(g_raw * resp));
+                acc(mag_m[2 * g], std::fabs((double)gmx));
+                acc(mag_m[2 * g + 1], std::fabs((double)gmy));
+                acc(mag_q[3 * g], std::fabs((double)(g_s * 0.5f * dx * dx)));
+                acc(mag_q[3 * g + 1], std::fabs((double)(g_s * dx * dy)));
+                acc(mag_q[3 * g + 2], std::fabs((double)(g_s * 0.5f * dy * dy)));
+                acc(mag_o[g], std::fabs((double)(g_raw * resp)));
             }
             for (int ch = 0; ch < channels; ++ch)
                 rem[ch] = alpha * col[ch] + (1.0f - alpha) * rem[ch];

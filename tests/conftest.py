@@ -41,3 +41,26 @@ def read_golden(name):
                 continue
             rows.append([part.split() for part in line.split("|")])
     return rows
+
+
+def pytest_terminal_summary(terminalreporter):
+    # what each parity comparison left out or held to a looser bound: near-tie
+    # pixels (checked at the bound a flipped decision allows), splats left out
+    # of a backward comparison, and cancellation-bound gradient elements
+    mod = sys.modules.get("gpu_util")
+    log = getattr(mod, "PARITY_LOG", None) if mod is not None else None
+    if not log:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity exclusions and near-tie checks")
+    for rec in log:
+        rest = ", ".join(f"{k}={v:.3g}" if isinstance(v, float) else f"{k}={v}"
+                         for k, v in rec.items() if k != "test")
+        tr.write_line(f"{rec['test']}: {rest}")
+    path = os.environ.get("GS_PARITY_LOG")
+    if path:
+        import json
+
+        with open(path, "w") as f:
+            for rec in log:
+                f.write(json.dumps(rec) + "\n")

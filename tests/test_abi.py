@@ -74,3 +74,17 @@ def test_argument_errors_without_gpu(lib):
     assert lib.gs_sort_pairs(None, None, 5, 0, 64, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 65, None, 0, None, None) == 1
     assert lib.gs_sort_pairs(P(8), P(8), 5, 0, 64, None, 0, None, None) == 4
+
+
+def test_timeout_hook_argument_errors_without_gpu(lib):
+    P = ct.c_void_p
+    call = lambda n, t, w, ws=P(8), nb=1 << 40, st=P(8): lib.gs_debug_sort_wait_timeout(
+        P(8), P(8), n, t, w, ws, nb, st, None)
+    assert call(0, 1, 10) == 1             # n = 0
+    assert call(100, 0, 10) == 1           # ticket_start must be >= 1
+    assert call(100, 65, 10) == 1          # at most 64
+    assert call(100, 1, 0) == 1            # wait_polls >= 1
+    assert call(100, 1, (1 << 20) + 1) == 1
+    assert call(100, 1, 10, st=None) == 1  # the status word is required
+    assert call(100, 1, 10, ws=None) == 4  # workspace missing
+    assert call(100, 2, 10, nb=lib.gs_sort_workspace_size(100 + 2 * 2048) - 1) == 4

@@ -25,7 +25,7 @@ def test_forward_channels(ch):
     iso, ref = _oracle_forward(s)
     got = gpu_forward(s, scene_to_dev(s))
     assert got["render_colors"].shape == (s.C, s.height, s.width, ch)
-    compare_forward(ref, got)
+    compare_forward(ref, got, s)
 
 
 def test_forward_decisions_independent_of_channels():

@@ -17,7 +17,7 @@ import torch
 import oracle
 from gpu_util import (DEV, TIE_ALPHA, TIE_T, compare_forward, gpu_forward, scene_to_dev,
                       to_dev, u64)
-from test_gpu_raster import _compare_grads
+from test_gpu_raster import _compare_grads, _gpu_fwd_with_trace, _walked_splats
 from tile_gaussian_splat_gb300 import binding as gs
 from tile_gaussian_splat_gb300 import scenes
 
@@ -73,7 +73,7 @@ def test_full_size_workload(k):
                                s.width, s.height, 16, r_off, r_ids, s.alpha_cutoff,
                                s.transmittance_threshold, pixels=pix, tie_rel=TIE_ALPHA,
                                tie_rel_T=TIE_T)
-    ties = compare_forward(ref, got, pixels=pix)
+    ties = compare_forward(ref, got, s, pixels=pix)
     # the sample is biased to the heaviest tiles (lists of thousands of
     # entries), where a near tie on some entry is likelier
     assert ties <= 0.05 * pix.size
@@ -86,13 +86,17 @@ def test_full_size_workload(k):
     g_rgb.reshape(-1, 3)[bp] = rng.standard_normal((bp.size, 3)).astype(np.float32)
     g_a.reshape(-1)[bp] = rng.standard_normal(bp.size).astype(np.float32)
     # the GPU walks the oracle's forward state at those pixels (zero elsewhere:
-    # render_alpha 0 makes every pair invalid).  Splats with a backward alpha
-    # within TIE_ALPHA of the cutoff or clamp are nudged by 1 % in opacity
-    # (a deterministic change of the seeded input, as in test_gpu_raster)
-    for it in range(3):
+    # render_alpha 0 makes every pair invalid).  Splats that took part in a
+    # near-tie decision -- a backward alpha within TIE_ALPHA of the cutoff or
+    # clamp, or a forward stop within TIE_T of the threshold -- are nudged by
+    # 1 % in opacity (a deterministic change of the seeded input, as in
+    # test_gpu_raster), so the GPU forward that the chain below runs makes
+    # the oracle's decisions
+    for it in range(4):
         refb = oracle.rasterize_fwd(s.means2d, s.conics, s.colors, s.opacities, None, None,
                                     s.width, s.height, 16, r_off, r_ids, s.alpha_cutoff,
-                                    s.transmittance_threshold, pixels=bp)
+                                    s.transmittance_threshold, pixels=bp, tie_rel=TIE_ALPHA,
+                                    tie_rel_T=TIE_T)
         ra = np.zeros((s.C, s.height, s.width, 1), np.float32)
         li = np.full((s.C, s.height, s.width), -1, np.int32)
         ra.reshape(-1)[bp] = refb["render_alphas"].reshape(-1)[bp]
@@ -100,22 +104,35 @@ def test_full_size_workload(k):
         rb = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, None, None,
                                   s.width, s.height, 16, r_off, r_ids, s.alpha_cutoff, ra, li,
                                   g_rgb, g_a, pixels=bp, tie_rel=TIE_ALPHA, magnitudes=True)
-        tie = rb["tie_splats"].astype(bool)
-        if not tie.any() or it == 2:
+        tie = rb["tie_splats"].astype(bool) | refb["tie_splats"].astype(bool)
+        if not tie.any() or it == 3:
             break
         s.opacities[tie] *= np.where(s.opacities[tie] < 0.98, 1.01, 0.99).astype(np.float32)
-    gb = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], to_dev(s.opacities), None,
+    d["opacities"] = to_dev(s.opacities)
+    gb = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None,
                              None, s.width, s.height, 16, got["offsets"], got["flatten_ids"],
                              s.alpha_cutoff, to_dev(ra), to_dev(li), to_dev(g_rgb), to_dev(g_a))
     torch.cuda.synchronize()
-    excluded = np.zeros(s.C * s.N, bool)
-    offs = r_off.reshape(-1)
-    for p in np.nonzero(rb["near_tie"].reshape(-1))[0]:
-        c, rem = divmod(int(p), s.width * s.height)
-        t = (c * s.tile_height + (rem // s.width) // 16) * s.tile_width + (rem % s.width) // 16
-        if li.reshape(-1)[p] >= offs[t]:
-            excluded[r_ids[offs[t]:li.reshape(-1)[p] + 1]] = True
     touched = (rb["mag_opacities"] > 0).reshape(-1)
     assert touched.sum() > 1000
-    assert excluded.sum() <= 0.05 * touched.sum()
-    _compare_grads(rb, gb, excluded.reshape(s.C, s.N))
+    excluded = _walked_splats(s, r_off, r_ids, np.nonzero(rb["near_tie"].reshape(-1))[0], [li])
+    assert (excluded.reshape(-1) & touched).sum() <= 0.05 * touched.sum()
+    _compare_grads(rb, gb, excluded)
+
+    # the chain the bench times, at full size in its launch configuration:
+    # the GPU forward (with the trace) on the same scene, then the
+    # trace-driven GPU backward on the GPU's own forward state.  Every pixel
+    # carries GPU state, but only the sampled tiles have a nonzero upstream
+    # gradient, so the oracle's walk over those tiles gives every gradient
+    f, tr = _gpu_fwd_with_trace(s, d)
+    gc = gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None,
+                             None, s.width, s.height, 16, f["offsets"], f["flatten_ids"],
+                             s.alpha_cutoff, f["render_alphas"], f["last_ids"], to_dev(g_rgb),
+                             to_dev(g_a), trace=tr)
+    torch.cuda.synchronize()
+    compare_forward(refb, f, s, pixels=bp)
+    both = np.nonzero(((rb["near_tie"] > 0) | (refb["near_tie"] > 0)).reshape(-1))[0]
+    both = np.intersect1d(both, bp)
+    excluded = _walked_splats(s, r_off, r_ids, both, [li, f["last_ids"].cpu().numpy()])
+    assert (excluded.reshape(-1) & touched).sum() <= 0.05 * touched.sum()
+    _compare_grads(rb, gc, excluded)

@@ -123,5 +123,5 @@ def test_projected_scene_through_the_raster_path():
     iso, fwd = oracle.render(scene2d, tie_rel=TIE_ALPHA, tie_rel_T=TIE_T)
     np.testing.assert_array_equal(out["flatten_ids"].cpu().numpy(), iso["flatten_ids"])
     np.testing.assert_array_equal(out["offsets"].cpu().numpy(), iso["offsets"])
-    compare_forward(fwd, out)
+    compare_forward(fwd, out, scene2d)
     assert (fwd["render_alphas"] > 0.5).mean() > 0.05  # the scene covers the images

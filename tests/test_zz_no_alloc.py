@@ -28,7 +28,11 @@ def _pairs(seed, n, distinct):
 
 def test_noalloc_sort_equals_workspace_sort_twice():
     lib = gs.lib()
-    cases = [(1, 600_001, 5000, 0, 64), (2, 250_000, 300, 32, 47)]
+    # pass counts 8, 2 (even: the result ends in the caller's arrays), 3 at
+    # the largest n (odd: it ends in the library's alternate buffers and is
+    # copied back, with the array's capacity fully used) and 5
+    cases = [(1, 600_001, 5000, 0, 64), (2, 250_000, 300, 32, 47),
+             (3, gs.SORT_NOALLOC_MAX_PAIRS, 7000, 0, 24), (4, 1000, 50, 8, 48)]
     for seed, n, distinct, b0, b1 in cases:
         k_ref, v_ref = _pairs(seed, n, distinct)
         k, v = k_ref.clone(), v_ref.clone()

@@ -48,6 +48,8 @@ SIGNATURES = {
     "gs_sort_workspace_size": (SZ, [I64]),
     "gs_sort_pairs": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
     "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
+    "gs_debug_sort_wait_timeout": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
+    "gs_peak_probe": (I32, [I32, I32, I32, P, P, P]),
 }
 
 
@@ -344,3 +346,25 @@ def gs_rasterize_bwd_bins(means2d, conics, colors, opacities, backgrounds, masks
         _ptr(out["grad_backgrounds"]), _ptr(out["grad_means2d_abs"]), _ptr(trace),
         _ptr(d_status), _stream(stream)), "gs_rasterize_bwd_bins")
     return out
+
+
+def gs_debug_sort_wait_timeout(keys, values, ticket_start, wait_polls, d_status, stream=None):
+    """Test hook of the timeout path (see the header): one sorting pass whose
+    first look-back word is never published and whose waits poll at most
+    wait_polls times.  keys int64 (n), values int32 (n) are overwritten with
+    unspecified values; d_status receives GS_ERR_TIMEOUT."""
+    n = keys.numel()
+    ws = _empty(lib().gs_sort_workspace_size(n + ticket_start * 2048), torch.uint8, keys.device)
+    _check(lib().gs_debug_sort_wait_timeout(_ptr(keys), _ptr(values), n, ticket_start,
+                                            wait_polls, _ptr(ws), ws.numel(), _ptr(d_status),
+                                            _stream(stream)), "gs_debug_sort_wait_timeout")
+    return ws
+
+
+def gs_peak_probe(kind, iters, blocks, out, stream=None):
+    """Enqueues the throughput probe (kind 0 FMA, 1 packed FMA, 2 ex2) into
+    out (float32, blocks * 256); returns the number of operations."""
+    ops = ct.c_int64(0)
+    _check(lib().gs_peak_probe(kind, iters, blocks, _ptr(out), ct.byref(ops), _stream(stream)),
+           "gs_peak_probe")
+    return int(ops.value)

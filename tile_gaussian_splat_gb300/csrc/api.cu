@@ -59,6 +59,10 @@ struct Carver {
 
 constexpr int kMaxPasses = 8;
 
+// Limits of the timeout-path test hook (gs_debug_sort_wait_timeout).
+constexpr int kMaxDebugTickets = 64;
+constexpr int kMaxDebugPolls = 1 << 20;
+
 // Workspace of gs_isect_tiles.  Everything up to `zero_end` is cleared by one
 // memset per call; the sort buffers after it are fully overwritten.
 struct IsectLayout {
@@ -610,6 +614,47 @@ int gs_sort_pairs(uint64_t* keys, int32_t* values, int64_t n, int begin_bit, int
             cudaMemcpyAsync(values, sv, (size_t)n * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
             return GS_ERR_CUDA;
     }
+    return check_launch();
+}
+
+int gs_debug_sort_wait_timeout(uint64_t* keys, int32_t* values, int64_t n, int ticket_start,
+                               int wait_polls, void* workspace, size_t workspace_bytes,
+                               int32_t* d_status, void* stream) {
+    if (n < 1 || n >= ((int64_t)1 << 30) || !keys || !values || !d_status ||
+        ticket_start < 1 || ticket_start > kMaxDebugTickets || wait_polls < 1 ||
+        wait_polls > kMaxDebugPolls)
+        return GS_ERR_INVALID_ARG;
+    const int64_t n_virtual = n + (int64_t)ticket_start * kTile64;
+    if (!workspace || workspace_bytes < gs_sort_workspace_size(n_virtual)) return GS_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the layout of gs_sort_pairs for n_virtual pairs: its first look-back
+    // region has a word per digit for every virtual block the pass can name
+    // (tickets ticket_start .. ticket_start + blocks(n) - 1)
+    Carver cv{static_cast<char*>(workspace)};
+    int32_t* abort_flag = cv.take<int32_t>(1);
+    uint32_t* tickets = cv.take<uint32_t>(kMaxPasses);
+    uint32_t* hist = cv.take<uint32_t>(kMaxPasses * 256);
+    uint64_t* lb0 = cv.take<uint64_t>((size_t)sort_blocks(n_virtual, kTile64) * 256);
+    for (int i = 1; i < kMaxPasses; ++i)
+        cv.take<uint64_t>((size_t)sort_blocks(n_virtual, kTile64) * 256);
+    const size_t zero_end = cv.used;
+    uint64_t* alt_k = cv.take<uint64_t>((size_t)n);
+    int32_t* alt_v = cv.take<int32_t>((size_t)n);
+    if (cudaMemsetAsync(workspace, 0, zero_end, s) != cudaSuccess) return GS_ERR_CUDA;
+    const uint32_t first = (uint32_t)ticket_start;
+    // from a host variable: the copy has been staged when the call returns
+    if (cudaMemcpyAsync(tickets, &first, sizeof(first), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return GS_ERR_CUDA;
+    launch_digit_hist_u64(keys, n, 0, 8, hist, s);
+    launch_onesweep_u64(keys, values, alt_k, alt_v, n, 0, 8, hist, LookbackScratch{lb0, tickets},
+                        abort_flag, d_status, s, wait_polls);
+    return check_launch();
+}
+
+int gs_peak_probe(int kind, int iters, int blocks, float* out, int64_t* h_ops, void* stream) {
+    if (kind < 0 || kind > 2 || iters < 1 || blocks < 1 || !out || !h_ops)
+        return GS_ERR_INVALID_ARG;
+    *h_ops = launch_peak_probe(kind, iters, blocks, out, static_cast<cudaStream_t>(stream));
     return check_launch();
 }
 

@@ -16,9 +16,9 @@ constexpr uint64_t kFlagAggregate = 1;  // this block's own count
 constexpr uint64_t kFlagPrefix = 2;     // inclusive prefix up to this block
 constexpr uint64_t kFlagMask = 3;
 
-// Upper bound on polls of one look-back word.  A predecessor publishes within
-// microseconds; the bound only matters when something has already gone wrong,
-// and turns that into GS_ERR_TIMEOUT instead of a hang.
+// Default upper bound on polls of one look-back word.  A predecessor
+// publishes within microseconds; the bound only matters when something has
+// already gone wrong, and turns that into GS_ERR_TIMEOUT instead of a hang.
 constexpr int kSpinLimit = 1 << 22;
 
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
@@ -47,6 +47,7 @@ __device__ __forceinline__ void report(int32_t* d_status, int code) {
 struct ErrorSink {
     int32_t* abort_flag;  // workspace word, zeroed per call
     int32_t* d_status;    // caller's word or null
+    int spin_limit = kSpinLimit;  // polls of one look-back word before GS_ERR_TIMEOUT
     __device__ __forceinline__ void raise(int code) const {
         atomicCAS(abort_flag, 0, code);
         report(d_status, code);
@@ -61,7 +62,7 @@ __device__ __forceinline__ uint64_t wait_published(const uint64_t* p, const Erro
     uint64_t v = ld_relaxed_u64(p);
     int it = 0;
     while ((v & kFlagMask) == 0) {
-        if (++it >= kSpinLimit) {
+        if (++it >= err.spin_limit) {
             err.raise(GS_ERR_TIMEOUT);
             return kFlagPrefix;
         }

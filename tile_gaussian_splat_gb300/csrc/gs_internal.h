@@ -34,11 +34,13 @@ void launch_digit_hist_u32(const uint32_t* keys, int64_t n, int shift0, int end_
 // vals_in ==
 // nullptr means values are the element indices.  lookback needs
 // sort_blocks(n, tile) * 256 words, ticket one word, both zeroed.
+// spin_limit > 0 replaces the default bound on the polls of one look-back
+// word (a test of the timeout path uses a small one).
 void launch_onesweep_u64(const uint64_t* keys_in, const int32_t* vals_in, uint64_t* keys_out,
                          int32_t* vals_out, int64_t n, int shift, int end_bit,
                          const uint32_t* hist,
                          LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
-                         cudaStream_t s);
+                         cudaStream_t s, int spin_limit = 0);
 void launch_onesweep_u32(const uint32_t* keys_in, const int32_t* vals_in, uint32_t* keys_out,
                          int32_t* vals_out, int64_t n, int shift, int end_bit,
                          const uint32_t* hist,
@@ -145,6 +147,12 @@ void launch_project(const float* means, const float* covars, const float* viewma
                     const float* intrinsics, int C, int N, const ProjectArgs& pa, int32_t* radii,
                     float* means2d, float* depths, float* conics, float* compensations,
                     float* radii_float, cudaStream_t s);
+
+// ---- peaks.cu
+// Throughput probe: kind 0 scalar FP32 FMA, 1 packed f32x2 FMA, 2 ex2.approx;
+// blocks x 256 threads, iters rounds; out gets blocks * 256 floats.  Returns
+// the operations performed (an FMA is one operation, a packed FMA two).
+int64_t launch_peak_probe(int kind, int iters, int blocks, float* out, cudaStream_t s);
 
 // ---- bins.cu
 // Largest bin capacity (the bin sort holds a bin's keys in shared memory).

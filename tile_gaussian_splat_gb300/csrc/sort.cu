@@ -278,10 +278,11 @@ void launch_onesweep_u64(const uint64_t* keys_in, const int32_t* vals_in, uint64
                          int32_t* vals_out, int64_t n, int shift, int end_bit,
                          const uint32_t* hist,
                          LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
-                         cudaStream_t s) {
+                         cudaStream_t s, int spin_limit) {
     if (n <= 0) return;
     const int64_t blocks = sort_blocks(n, kTile64);
     ErrorSink err{abort_flag, d_status};
+    if (spin_limit > 0) err.spin_limit = spin_limit;
     const uint32_t dm = digit_mask(shift, end_bit);
     if (vals_in)
         k_onesweep<uint64_t, kItems64, false><<<(unsigned)blocks, kThreads, 0, s>>>(

@@ -33,12 +33,18 @@ constexpr size_t kBlocks = (size_t)((kNoAllocMaxPairs + kTile64 - 1) / kTile64);
 constexpr size_t kOffTickets = round_up(sizeof(int32_t));                       // after the error flag
 constexpr size_t kOffHist = kOffTickets + round_up(kPasses * sizeof(uint32_t));
 constexpr size_t kOffLookback = kOffHist + round_up(kPasses * 256 * sizeof(uint32_t));
-constexpr size_t kLookbackBytes = round_up(kBlocks * 256 * sizeof(uint64_t));
-constexpr size_t kOffAltKeys = kOffLookback + kPasses * kLookbackBytes;  // end of zeroed part
+// look-back words: a call over n pairs uses passes * sort_blocks(n) * 256 of
+// them, packed from kOffLookback (a pass's region starts right after the
+// previous pass's), so only that much needs clearing per call
+constexpr size_t kLookbackBytes = kPasses * kBlocks * 256 * sizeof(uint64_t);
+constexpr size_t kOffAltKeys = round_up(kOffLookback + kLookbackBytes);
 constexpr size_t kOffAltVals = kOffAltKeys + round_up(kNoAllocMaxPairs * sizeof(uint64_t));
 constexpr size_t kScratchBytes = kOffAltVals + round_up(kNoAllocMaxPairs * sizeof(int32_t));
 
-// About 17.6 MB per device.
+// 20,980,224 bytes (about 21.0 MB) per device: 8 passes x 512 blocks x 256
+// look-back words x 8 bytes, 8 MB of alternate keys, 4 MB of alternate
+// values and 8.7 KB of flag, tickets and histograms.
+static_assert(kScratchBytes == 20980224, "the stated size of the scratch array");
 static __device__ __align__(256) unsigned char g_sort_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -79,16 +85,19 @@ extern "C" int gs_sort_pairs_noalloc(uint64_t* keys, int32_t* values, int64_t n,
     uint64_t* alt_k = reinterpret_cast<uint64_t*>(base + kOffAltKeys);
     int32_t* alt_v = reinterpret_cast<int32_t*>(base + kOffAltVals);
     // the array keeps the previous call's contents: clear the flag, tickets,
-    // histograms and look-back words this call relies on starting at zero
-    if (cudaMemsetAsync(base, 0, kOffAltKeys, s) != cudaSuccess) return GS_ERR_CUDA;
-    launch_digit_hist_u64(keys, n, begin_bit, end_bit, hist, s);
+    // histograms and the look-back words of this call's passes, which must
+    // start at zero
     const int passes = (end_bit - begin_bit + 7) / 8;
+    const size_t lb_words = (size_t)sort_blocks(n, kTile64) * 256;
+    const size_t zero_bytes = kOffLookback + (size_t)passes * lb_words * sizeof(uint64_t);
+    if (cudaMemsetAsync(base, 0, zero_bytes, s) != cudaSuccess) return GS_ERR_CUDA;
+    launch_digit_hist_u64(keys, n, begin_bit, end_bit, hist, s);
     uint64_t* sk = keys;
     int32_t* sv = values;
     for (int pass = 0; pass < passes; ++pass) {
         uint64_t* dk = sk == keys ? alt_k : keys;
         int32_t* dv = sv == values ? alt_v : values;
-        uint64_t* lb = reinterpret_cast<uint64_t*>(base + kOffLookback + pass * kLookbackBytes);
+        uint64_t* lb = reinterpret_cast<uint64_t*>(base + kOffLookback) + (size_t)pass * lb_words;
         launch_onesweep_u64(sk, sv, dk, dv, n, begin_bit + 8 * pass, end_bit, hist + 256 * pass,
                             LookbackScratch{lb, tickets + pass}, abort_flag, d_status, s);
         sk = dk;
