@@ -63,7 +63,7 @@ def _load(path):
     L.orc_tile_offsets.restype = I32
     L.orc_rasterize_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                     P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32, F32,
-                                    P]
+                                    P, P]
     L.orc_rasterize_fwd.restype = I32
     L.orc_rasterize_fwd_f64.argtypes = [P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                         P, P, I64, F64, F64, P, P, P]
@@ -157,7 +157,9 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                   pixels=None, tie_rel=0.0, tie_rel_T=None, out=None, omp=False):
     """Forward compositing.  Returns dict(render_colors (C,H,W,ch),
     render_alphas (C,H,W,1), last_ids (C,H,W), stats [evaluated, composited,
-    near-tie pixels], near_tie (C,H,W) uint8)."""
+    near-tie pixels], near_tie (C,H,W) uint8 (near-threshold decisions per
+    pixel), tie_splats (C,N), comp_hash (C,H,W) uint64 (FNV-1a hash of the
+    composited list positions, in order))."""
     means2d = _c(means2d, np.float32)
     conics = _c(conics, np.float32)
     colors = _c(colors, np.float32)
@@ -175,6 +177,8 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                    last_ids=np.full((C, height, width), -2, np.int32),
                    near_tie=np.zeros((C, height, width), np.uint8))
     out["tie_splats"] = np.zeros((C, N), np.uint8)
+    if "comp_hash" not in out:
+        out["comp_hash"] = np.zeros((C, height, width), np.uint64)
     stats = np.zeros(3, np.int64)
     px = None if pixels is None else _c(pixels, np.int64)
     rc = lib(omp).orc_rasterize_fwd(
@@ -184,7 +188,7 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         _ptr(px), 0 if px is None else px.size, _ptr(out["render_colors"]),
         _ptr(out["render_alphas"]), _ptr(out["last_ids"]), _ptr(stats), _ptr(out["near_tie"]),
         float(tie_rel), float(tie_rel if tie_rel_T is None else tie_rel_T),
-        _ptr(out["tie_splats"]))
+        _ptr(out["tie_splats"]), _ptr(out["comp_hash"]))
     if rc != 0:
         raise ValueError("oracle forward: bad arguments")
     out["stats"] = stats

@@ -51,6 +51,10 @@ constexpr float kAlphaClamp = 0.99f;
 // (liboracle_omp.so, compiled from this same file with -fopenmp, used only to
 // time the oracle on all host cores) runs pixels on several threads, so its
 // adds and flag stores are atomic.
+// FNV-1a (64-bit) parameters of the composite-position hash.
+constexpr uint64_t kHashBasis = 14695981039346656037ull;
+constexpr uint64_t kHashPrime = 1099511628211ull;
+
 inline void acc(double& dst, double v) {
 #ifdef _OPENMP
 #pragma omp atomic
@@ -339,6 +343,10 @@ int64_t orc_bin_splats(const float* means2d, const float* radii, int elliptical,
 //     decision (T carries the accumulated error of every 1 - alpha, which is
 //     large relative to itself for alpha near 0.99, hence its own margin).
 //   tie_splats[g] = 1 for every splat g that took part in such a decision.
+//   comp_hash[pixel] = a 64-bit FNV-1a hash of the list positions j the pixel
+//     composited, in order (h = (h ^ j) * 1099511628211 from 14695981039346656037):
+//     another implementation's decisions at a pixel can be compared with these
+//     without listing them.
 struct FwdArgs {
     const float* means2d;
     const float* conics;
@@ -356,7 +364,7 @@ struct FwdArgs {
 
 static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
                       float* out_alpha, int32_t* out_last, int64_t* stats, uint8_t* near_tie,
-                      float tie_rel, float tie_rel_T, uint8_t* tie_splats) {
+                      float tie_rel, float tie_rel_T, uint8_t* tie_splats, uint64_t* comp_hash) {
     int64_t tiles = (int64_t)a.C * a.tile_height * a.tile_width;
     int64_t t = (c * a.tile_height + y / a.tile_size) * a.tile_width + x / a.tile_size;
     int64_t start = a.offsets[t];
@@ -367,6 +375,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
     int32_t last = -1;
     int64_t evaluated = 0, composited = 0;
     int n_tie = 0;  // decisions taken within the margins
+    uint64_t hash = kHashBasis;  // of the composited list positions, in order
     bool masked = a.masks != nullptr && a.masks[t] == 0;
     if (!masked) {
         float px = (float)x + 0.5f, py = (float)y + 0.5f;
@@ -385,7 +394,9 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             }
             float raw = a.opacities[g] * std::exp(-s);
             float alpha = raw > kAlphaClamp ? kAlphaClamp : raw;
-            pair_tie |= std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff;
+            // a cutoff <= 0 cannot be crossed by an alpha >= 0: no tie there
+            pair_tie |= a.alpha_cutoff > 0.0f &&
+                        std::fabs(alpha - a.alpha_cutoff) <= tie_rel * a.alpha_cutoff;
             if (pair_tie && tie_splats) set_flag(tie_splats[g]);
             n_tie += pair_tie ? 1 : 0;
             if (alpha < a.alpha_cutoff) continue;
@@ -395,6 +406,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             T = T * (1.0f - alpha);
             last = (int32_t)j;
             ++composited;
+            hash = (hash ^ (uint64_t)(uint32_t)j) * kHashPrime;
             if (std::fabs(T - a.transmittance_threshold) <=
                 tie_rel_T * a.transmittance_threshold) {
                 ++n_tie;
@@ -416,6 +428,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
         acc_i64(stats[2], n_tie > 0 ? 1 : 0);
     }
     if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
+    if (comp_hash) comp_hash[p] = hash;
 }
 
 // Renders every pixel (pixels == nullptr) or only the listed flat pixel
@@ -430,7 +443,7 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
                       float transmittance_threshold, const int64_t* pixels, int64_t n_pixels,
                       float* render_colors, float* render_alphas, int32_t* last_ids,
                       int64_t* stats, uint8_t* near_tie, float tie_rel, float tie_rel_T,
-                      uint8_t* tie_splats) {
+                      uint8_t* tie_splats, uint64_t* comp_hash) {
     if (channels < 1 || channels > kMaxChannels) return 1;
     FwdArgs a = {means2d,   conics,     colors,      opacities, backgrounds,
                  masks,     C,          N,           channels,  width,
@@ -446,7 +459,7 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
             for (int y = 0; y < height; ++y)
                 for (int x = 0; x < width; ++x)
                     fwd_pixel(a, c, x, y, render_colors, render_alphas, last_ids, stats,
-                              near_tie, tie_rel, tie_rel_T, tie_splats);
+                              near_tie, tie_rel, tie_rel_T, tie_splats, comp_hash);
     } else {
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 64)
@@ -456,7 +469,7 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
             int64_t c = p / ((int64_t)width * height);
             int64_t r = p % ((int64_t)width * height);
             fwd_pixel(a, c, (int)(r % width), (int)(r / width), render_colors, render_alphas,
-                      last_ids, stats, near_tie, tie_rel, tie_rel_T, tie_splats);
+                      last_ids, stats, near_tie, tie_rel, tie_rel_T, tie_splats, comp_hash);
         }
     }
     return 0;
@@ -539,9 +552,9 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
 // Every gradient output is zeroed first (the bridge allocates them zeroed).
 // Per-pair terms are float as listed; they are summed in double and rounded
 // to float once.  pixels/n_pixels restricts the walk to listed pixels.
-// near_tie (optional, per pixel) counts (saturating at 255) the pairs whose
-// alpha was within tie_rel of the cutoff or raw alpha within tie_rel of the
-// clamp; tie_splats
+// near_tie (optional, per pixel) counts the pairs whose alpha was within
+// tie_rel of the cutoff (low 4 bits) and those whose raw alpha was within
+// tie_rel of the clamp (high 4 bits), each saturating at 15; tie_splats
 // (optional, per splat) marks the splats of those pairs.
 // magnitudes (optional, double) receives, per gradient element, the sum of
 // the absolute values of its per-pair terms, laid out as grad_means2d (2CN),
@@ -588,7 +601,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
         float Tc = 1.0f - ra;
         float Ta = 1.0f;
         float rem[kMaxChannels];
-        int n_tie = 0;
+        int n_tie = 0, n_clamp_tie = 0;
         for (int ch = 0; ch < channels; ++ch) {
             rem[ch] = backgrounds ? backgrounds[c * channels + ch] : 0.0f;
             if (grad_backgrounds) acc(gb[c * channels + ch], (double)(g_rgb[ch] * Tc));
@@ -607,10 +620,12 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             bool valid = ra > 0.0f && s >= 0.0f && alpha >= alpha_cutoff && last >= j &&
                          Tc < 1.0f && alpha < 1.0f;
             if (last >= j && s >= 0.0f) {
-                bool pair_tie = std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff ||
-                                std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp;
-                if (pair_tie && tie_splats) set_flag(tie_splats[g]);
-                n_tie += pair_tie ? 1 : 0;
+                bool cut_tie = alpha_cutoff > 0.0f &&
+                               std::fabs(alpha - alpha_cutoff) <= tie_rel * alpha_cutoff;
+                bool clamp_tie = std::fabs(raw - kAlphaClamp) <= tie_rel * kAlphaClamp;
+                if ((cut_tie || clamp_tie) && tie_splats) set_flag(tie_splats[g]);
+                n_tie += cut_tie ? 1 : 0;
+                n_clamp_tie += clamp_tie ? 1 : 0;
             }
             if (!valid) continue;
             float Tb = Tc / (1.0f - alpha);
@@ -648,7 +663,8 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
             Ta *= 1.0f - alpha;
             Tc = Tb;
         }
-        if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
+        if (near_tie)
+            near_tie[p] = (uint8_t)(std::min(n_tie, 15) | (std::min(n_clamp_tie, 15) << 4));
     }
     for (int64_t i = 0; i < 2 * CN; ++i) grad_means2d[i] = (float)gm[i];
     for (int64_t i = 0; i < 3 * CN; ++i) grad_conics[i] = (float)gq[i];

@@ -140,3 +140,49 @@ def grad_tolerance_check(name, got, ref, rtol=1e-3, atol=1e-6, mask=None):
     bad = err > rtol * np.abs(ref) + atol
     assert not bad.any(), (f"{name}: {bad.sum()} of {bad.size} outside {rtol} rel + {atol}; "
                            f"worst err {err[bad].max()} at ref {ref[bad][np.argmax(err[bad])]}")
+
+
+_FNV_BASIS = 14695981039346656037
+_FNV_PRIME = 1099511628211
+
+
+def gpu_comp_hash(trace, offsets, last_ids, pixels, width, height):
+    """For each flat pixel index p = (c H + y) W + x in `pixels`, the FNV-1a
+    hash (the oracle's comp_hash) of the list positions the GPU forward
+    composited there, read from its trace: word 4 (q / 32) + y % 4 of entry
+    j, bit q % 32, with q = 16 ((y % 16) / 4) + x % 16 (the layout
+    gs_rasterize_fwd documents).  Only entries up to the pixel's last id are
+    read (later words may be unwritten)."""
+    TW, TH = (width + 15) // 16, (height + 15) // 16
+    offs = offsets.reshape(-1).cpu().numpy().astype(np.int64)
+    last = last_ids.reshape(-1).cpu().numpy()
+    out = {}
+    for p in np.asarray(pixels, np.int64).tolist():
+        c, rem = divmod(p, width * height)
+        y, x = divmod(rem, width)
+        t = (c * TH + y // 16) * TW + x // 16
+        start, lj = int(offs[t]), int(last[p])
+        h = _FNV_BASIS
+        if lj >= start:
+            rows = trace[start:lj + 1].cpu().numpy().view(np.uint32)
+            q = 16 * ((y % 16) // 4) + x % 16
+            bits = (rows[:, 4 * (q // 32) + (y % 16) % 4] >> np.uint32(q % 32)) & np.uint32(1)
+            for j in (start + np.nonzero(bits)[0]).tolist():
+                h = ((h ^ j) * _FNV_PRIME) % (1 << 64)
+        out[p] = h
+    return out
+
+
+def flipped_pixels(ref, rb, trace, got, width, height):
+    """Pixels to leave out of a GPU-forward -> GPU-backward comparison: those
+    flagged near a decision by the oracle's forward or backward where the
+    GPU's composited positions (from its trace) differ from the oracle's
+    (comp_hash), and those with a pair near the 0.99 clamp in the oracle's
+    backward (high bits of its near_tie), where the clamp's gradient switch
+    may flip.  Returns (pixels, flagged count, flipped count)."""
+    flagged = np.nonzero(((rb["near_tie"] > 0) | (ref["near_tie"] > 0)).reshape(-1))[0]
+    gh = gpu_comp_hash(trace, got["offsets"], got["last_ids"], flagged, width, height)
+    rh = ref["comp_hash"].reshape(-1)
+    flipped = np.array([p for p in flagged.tolist() if gh[p] != int(rh[p])], np.int64)
+    clamp = np.nonzero((rb["near_tie"].reshape(-1) >> 4) > 0)[0]
+    return np.union1d(flipped, clamp), int(flagged.size), int(flipped.size)

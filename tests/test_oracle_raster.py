@@ -532,3 +532,26 @@ def test_many_channels_reduce_to_three_channel_runs():
     for k in ("grad_opacities", "grad_means2d", "grad_conics"):
         np.testing.assert_allclose(b300[k], 100 * b3[k].astype(np.float64), rtol=2e-4,
                                    atol=1e-4 * np.abs(100 * b3[k]).max(), err_msg=k)
+
+
+def _fnv(positions):
+    h = 14695981039346656037
+    for j in positions:
+        h = ((h ^ j) * 1099511628211) % (1 << 64)
+    return h
+
+
+def test_composite_hash_lists_the_composited_positions():
+    # the two stacked splats of the golden case: the centre pixel composites
+    # list positions 0 and 1; a pixel only the wider back splat reaches
+    # composites position 1 alone; a pixel beyond both composites nothing
+    s = _scene([[7.5, 7.5], [7.5, 7.5]], [[1, 0, 1], [0.02, 0, 0.02]], [[1, 0, 0], [0, 1, 0]],
+               [0.5, 0.5], [1.0, 2.0], [3.0, 12.0], 16, 16)
+    out = _fwd(s, _setup(s))
+    assert out["comp_hash"][0, 7, 7] == _fnv([0, 1])
+    x = 12  # dx = -5: s = 12.5 for the front splat (alpha 2e-6), 0.25 for the back one
+    assert out["last_ids"][0, 7, x] == 1
+    assert out["comp_hash"][0, 7, x] == _fnv([1])
+    s.means2d[:] = 40.0  # nothing reaches any pixel of the tile it still lists
+    out = _fwd(s, _setup(s))
+    assert (out["comp_hash"] == _fnv([])).all()
