@@ -59,7 +59,11 @@ typedef enum gs_status {
     GS_ERR_TIMEOUT = 5,        /* a bounded inter-block wait ran out         */
     GS_ERR_CUDA = 6,           /* a CUDA runtime call failed                 */
     GS_ERR_UNSORTED = 7,       /* gs_tile_offsets was given unsorted keys    */
-    GS_ERR_COUNT_MISMATCH = 8  /* n_isects differs from the emitted total    */
+    GS_ERR_COUNT_MISMATCH = 8, /* n_isects differs from the emitted total    */
+    GS_ERR_OUT_OF_BOUNDS = 9   /* an index read from the inputs (a list range,
+                                  a flatten id) lies outside its array; only the
+                                  range-checking build (GS_DEBUG_BOUNDS) reports
+                                  it -- every build skips such an access */
 } gs_status;
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
@@ -319,12 +323,12 @@ int gs_rasterize_fwd(const float* means2d, const float* conics,
  *   grad_means2d (C,N,2), grad_conics (C,N,3), grad_colors (C,N,channels),
  *   grad_opacities (C,N); grad_backgrounds (C,channels) or NULL;
  *   grad_means2d_abs (C,N,2) or NULL.
- * Supported: 1 <= channels <= GS_MAX_CHANNELS, tile_size == 16;
- *   grad_means2d_abs only with channels <= 4 (else GS_ERR_INVALID_ARG: the
- *   absolute value of a sum over all channels cannot be formed from
- *   per-chunk parts).  More than 4 channels run as chunks of up to 4, whose
- *   contributions add up: every term above is linear in the per-channel
- *   products.
+ * Supported: 1 <= channels <= GS_MAX_CHANNELS, tile_size == 16.  More than
+ *   4 channels run as chunks of up to 4, whose contributions add up: every
+ *   term above is linear in the per-channel products.  grad_means2d_abs is
+ *   not (|.| of a sum over all channels cannot be formed from per-chunk
+ *   parts), so above 4 channels it comes from one more walk of the lists
+ *   with the full channel sums, read from global memory for every pair.
  */
 int gs_rasterize_bwd(const float* means2d, const float* conics,
                      const float* colors, const float* opacities,

@@ -19,7 +19,7 @@ def _scene(ch, seed=21, C=2, W=100, H=70, N=3000):
     return scenes.random_small(seed, C=C, N=N, W=W, H=H, sigma=(0.5, 10.0), channels=ch)
 
 
-@pytest.mark.parametrize("ch", [1, 2, 4, 5, 7, 16, 33])
+@pytest.mark.parametrize("ch", [1, 2, 4, 5, 7, 16, 33, 1024])
 def test_forward_channels(ch):
     s = _scene(ch)
     iso, ref = _oracle_forward(s)
@@ -59,9 +59,10 @@ def test_forward_decisions_independent_of_channels():
     assert err <= 1e-6
 
 
-@pytest.mark.parametrize("ch,absgrad", [(1, True), (2, True), (4, True), (5, False),
-                                        (7, False), (16, False)])
+@pytest.mark.parametrize("ch,absgrad", [(1, True), (2, True), (4, True), (5, True),
+                                        (7, True), (16, False), (16, True), (130, True)])
 def test_backward_channels(ch, absgrad):
+    # above 4 channels absgrad comes from its own full-channel pass
     s = _scene(ch, seed=23)
     rb, got, excluded = _bwd_case(s, absgrad=absgrad)
     _compare_grads(rb, got, excluded)
@@ -78,6 +79,7 @@ def test_backward_channels(ch, absgrad):
 
 @pytest.mark.parametrize("ch", [2, 7])
 def test_backward_channels_trace_equals_recompute(ch):
+    # absgrad included: above 4 channels its full-channel pass reads the trace too
     s = _scene(ch, seed=24)
     d = scene_to_dev(s)
     f, tr = _gpu_fwd_with_trace(s, d)
@@ -85,10 +87,10 @@ def test_backward_channels_trace_equals_recompute(ch):
     args = (d["means2d"], d["conics"], d["colors"], d["opacities"], d["backgrounds"], None,
             s.width, s.height, 16, f["offsets"], f["flatten_ids"], s.alpha_cutoff,
             f["render_alphas"], f["last_ids"], to_dev(g_rgb), to_dev(g_a))
-    a = gs.gs_rasterize_bwd(*args)
-    b = gs.gs_rasterize_bwd(*args, trace=tr)
+    a = gs.gs_rasterize_bwd(*args, absgrad=True)
+    b = gs.gs_rasterize_bwd(*args, absgrad=True, trace=tr)
     for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities",
-              "grad_backgrounds"):
+              "grad_backgrounds", "grad_means2d_abs"):
         x, y = a[k].cpu().numpy(), b[k].cpu().numpy()
         scale = np.abs(x).max() + 1e-30
         np.testing.assert_allclose(y, x, rtol=1e-4, atol=1e-6 * scale, err_msg=k)
@@ -98,14 +100,6 @@ def test_channel_argument_errors():
     s = _scene(5, seed=25, C=1, W=32, H=32, N=50)
     d = scene_to_dev(s)
     f = gpu_forward(s, d)
-    g_rgb, g_a = scenes.upstream_grads(1, 32, 32, channels=5)
-    # absgrad needs the full per-pixel channel sum: more than 4 channels is refused
-    with pytest.raises(gs.GsError) as e:
-        gs.gs_rasterize_bwd(d["means2d"], d["conics"], d["colors"], d["opacities"], None, None,
-                            32, 32, 16, f["offsets"], f["flatten_ids"], s.alpha_cutoff,
-                            f["render_alphas"], f["last_ids"], to_dev(g_rgb), to_dev(g_a),
-                            absgrad=True)
-    assert e.value.code == 1
     # more channels than GS_MAX_CHANNELS
     wide = torch.zeros((1, s.N, 1025), dtype=torch.float32, device=DEV)
     with pytest.raises(gs.GsError) as e:

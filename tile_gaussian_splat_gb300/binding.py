@@ -9,6 +9,7 @@ if the library is missing or no GPU is present, calls raise.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes as ct
 import os
 
@@ -16,12 +17,13 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgs_splat_gb300.so")
+LIB_DEBUG_PATH = os.path.join(_HERE, "libgs_splat_gb300_debug.so")
 
 GS_OK = 0
 STATUS_NAMES = {
     0: "GS_OK", 1: "GS_ERR_INVALID_ARG", 2: "GS_ERR_CAPACITY", 3: "GS_ERR_KEY_OUT_OF_GRID",
     4: "GS_ERR_WORKSPACE", 5: "GS_ERR_TIMEOUT", 6: "GS_ERR_CUDA", 7: "GS_ERR_UNSORTED",
-    8: "GS_ERR_COUNT_MISMATCH",
+    8: "GS_ERR_COUNT_MISMATCH", 9: "GS_ERR_OUT_OF_BOUNDS",
 }
 
 # exported symbol -> (restype, argtypes); mirrors include/gs_splat.h
@@ -62,21 +64,38 @@ class GsError(RuntimeError):
 _lib = None
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+            "g.build()'` (the CUDA library has no CPU fallback)")
+    L = ct.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     """Opens the library (once).  Raises if it was not built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
-                "g.build()'` (the CUDA library has no CPU fallback)")
-        L = ct.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def library(path):
+    """Routes this module's calls to another build of the library -- the
+    range-checking build, LIB_DEBUG_PATH -- while the block runs."""
+    global _lib
+    saved = lib()
+    _lib = _load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
 
 
 def _status_text(code):

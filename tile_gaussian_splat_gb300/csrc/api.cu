@@ -211,6 +211,7 @@ const char* gs_status_string(int status) {
         case GS_ERR_CUDA: return "CUDA runtime error";
         case GS_ERR_UNSORTED: return "keys are not sorted";
         case GS_ERR_COUNT_MISMATCH: return "n_isects differs from the emitted total";
+        case GS_ERR_OUT_OF_BOUNDS: return "an index read from the inputs is outside its array";
         default: return "unknown status";
     }
 }
@@ -376,13 +377,13 @@ int raster_fwd(const float* means2d, const float* conics, const float* colors,
                const int32_t* bin_counts, int bin_capacity, const int32_t* flatten_ids,
                int64_t n_isects, float alpha_cutoff, float transmittance_threshold,
                float* render_colors, float* render_alphas, int32_t* last_ids,
-               int32_t* pair_counts, uint32_t* trace, void* stream) {
+               int32_t* pair_counts, uint32_t* trace, int32_t* d_status, void* stream) {
     if (!render_colors || !render_alphas || !last_ids) return GS_ERR_INVALID_ARG;
     if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
                  offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold,
-                 channels, 0, 1, bin_counts, bin_capacity};
+                 channels, 0, 1, bin_counts, bin_capacity, d_status};
     launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts, trace,
                       static_cast<cudaStream_t>(stream));
     return check_launch();
@@ -396,15 +397,14 @@ int raster_bwd(const float* means2d, const float* conics, const float* colors,
                const int32_t* last_ids, const float* grad_render_colors,
                const float* grad_render_alphas, float* grad_means2d, float* grad_conics,
                float* grad_colors, float* grad_opacities, float* grad_backgrounds,
-               float* grad_means2d_abs, const uint32_t* trace, void* stream) {
+               float* grad_means2d_abs, const uint32_t* trace, int32_t* d_status,
+               void* stream) {
     if (!render_alphas || !last_ids || !grad_render_colors || !grad_render_alphas)
         return GS_ERR_INVALID_ARG;
     const int64_t CN = (int64_t)C * N;
     if (CN > 0 && (!grad_means2d || !grad_conics || !grad_colors || !grad_opacities))
         return GS_ERR_INVALID_ARG;
     if (grad_backgrounds && !backgrounds) return GS_ERR_INVALID_ARG;
-    // |.| of a sum over channels is not the sum over channel chunks of |.|
-    if (grad_means2d_abs && channels > 4) return GS_ERR_INVALID_ARG;
     if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t f = sizeof(float);
@@ -422,7 +422,7 @@ int raster_bwd(const float* means2d, const float* conics, const float* colors,
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
                  C, N, width, height, (width + 15) / 16, (height + 15) / 16,
                  offsets, flatten_ids, n_isects, alpha_cutoff, 0.0f, channels, 0, 1,
-                 bin_counts, bin_capacity};
+                 bin_counts, bin_capacity, d_status};
     RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                   grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                   grad_means2d_abs};
@@ -459,7 +459,7 @@ int gs_rasterize_fwd(const float* means2d, const float* conics, const float* col
     return raster_fwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
                       width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
                       transmittance_threshold, render_colors, render_alphas, last_ids,
-                      pair_counts, trace, stream);
+                      pair_counts, trace, d_status, stream);
 }
 
 int gs_rasterize_bwd(const float* means2d, const float* conics, const float* colors,
@@ -479,7 +479,7 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
                       width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
                       render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                       grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
-                      grad_means2d_abs, trace, stream);
+                      grad_means2d_abs, trace, d_status, stream);
 }
 
 int gs_bin_splats(const float* means2d, const float* radii, int elliptical, const float* depths,
@@ -518,7 +518,7 @@ int gs_rasterize_fwd_bins(const float* means2d, const float* conics, const float
     return raster_fwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
                       width, height, nullptr, bin_counts, capacity, bins, n_slots, alpha_cutoff,
                       transmittance_threshold, render_colors, render_alphas, last_ids,
-                      pair_counts, trace, stream);
+                      pair_counts, trace, d_status, stream);
 }
 
 int gs_rasterize_bwd_bins(const float* means2d, const float* conics, const float* colors,
@@ -541,7 +541,7 @@ int gs_rasterize_bwd_bins(const float* means2d, const float* conics, const float
                       width, height, nullptr, bin_counts, capacity, bins, n_slots, alpha_cutoff,
                       render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                       grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
-                      grad_means2d_abs, trace, stream);
+                      grad_means2d_abs, trace, d_status, stream);
 }
 
 int gs_project(const float* means, const float* covars, const float* viewmats,

@@ -42,6 +42,15 @@ __device__ __forceinline__ void report(int32_t* d_status, int code) {
     if (d_status) atomicCAS(d_status, 0, code);
 }
 
+// The range-checking build (-DGS_DEBUG_BOUNDS): where an index read from the
+// inputs (a list range, a flatten id) falls outside its array, every build
+// skips the access; this build also reports GS_ERR_OUT_OF_BOUNDS.
+#ifdef GS_DEBUG_BOUNDS
+#define GS_BOUNDS_REPORT(d_status) report((d_status), GS_ERR_OUT_OF_BOUNDS)
+#else
+#define GS_BOUNDS_REPORT(d_status) ((void)0)
+#endif
+
 // Errors seen by a look-back wait: the internal abort flag (workspace) stops
 // every other waiter at once, the caller's word gets the code.
 struct ErrorSink {

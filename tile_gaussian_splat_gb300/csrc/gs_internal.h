@@ -112,6 +112,7 @@ struct RasterArgs {
     // flatten_ids[t * bin_capacity, + min(bin_counts[t], bin_capacity))
     const int32_t* bin_counts;
     int bin_capacity;
+    int32_t* d_status;  // caller's status word or null
 };
 
 // trace (may be null): per list entry 8 words, the tile pixels that composited it.

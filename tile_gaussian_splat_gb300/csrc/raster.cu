@@ -155,6 +155,7 @@ __device__ __forceinline__ TileRange tile_range(const RasterArgs& a) {
     const int64_t ntiles = (int64_t)a.C * per_camera;
     if (a.bin_counts) {
         const int n = a.bin_counts[r.tile];
+        if (n < 0 && threadIdx.x == 0) GS_BOUNDS_REPORT(a.d_status);
         r.start = r.tile * a.bin_capacity;
         r.end = r.start + (n < 0 ? 0 : (n > a.bin_capacity ? a.bin_capacity : n));
     } else {
@@ -163,6 +164,8 @@ __device__ __forceinline__ TileRange tile_range(const RasterArgs& a) {
     }
     // offsets from gs_tile_offsets are always inside [0, n_isects]; clamping
     // keeps a corrupted table from reading outside flatten_ids
+    if ((r.end < 0 || r.end > a.n_isects || r.start < 0 || r.start > r.end) && threadIdx.x == 0)
+        GS_BOUNDS_REPORT(a.d_status);
     r.end = r.end < 0 ? 0 : (r.end > a.n_isects ? a.n_isects : r.end);
     r.start = r.start < 0 ? 0 : (r.start > r.end ? r.end : r.start);
     r.masked = a.masks != nullptr && a.masks[r.tile] == 0;
@@ -284,6 +287,7 @@ __device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&
             jj[r] = REVERSE ? hi - 1 - i : lo + i;
             const int64_t g = a.flatten_ids[jj[r]];
             const bool valid_id = (uint64_t)g < (uint64_t)CN;
+            if (!valid_id) GS_BOUNDS_REPORT(a.d_status);
             bool any = valid_id;
             if (TRACE_IN && valid_id) {
                 // the forward's masks say exactly which warps composited it;
@@ -925,6 +929,168 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     if (nslots) flush_reduction<CH, F>(w, nslots, task, lane);
 }
 
+// ------------------------------------------------- absgrad over many channels
+
+// With more than 4 channels the chunked backward cannot form absgrad: a
+// pair's mean-gradient term carries the alpha gradient summed over ALL
+// channels, and |.| of that sum is not the sum of |.| of per-chunk parts.
+// This pass walks the lists once more, exactly as the chunks do (trace-driven
+// or re-evaluating), with the full channel sums -- the pixel's upstream
+// colour gradient and the splat's colour are read from global memory for
+// each pair -- and adds only |dL/dmeans2d| to grad_means2d_abs.  Per pixel
+// the state is (T, Q), Q = sum_c g_c rem_c - g_a T_after, with the chunks'
+// recurrence Q <- alpha (g . color) + (1 - alpha) Q from g . background - g_a.
+struct AbsWarpSmem {
+    static constexpr int kRed = 16;  // entries buffered per reduction (2 fields)
+    float2 tq[kWarpPix];
+    int16_t list[kWarpPix];
+    float4 red[kRed][2][kWarp / 4 + 1];  // rows padded as in BwdWarpSmem
+    int32_t red_gid[kRed];
+};
+
+template <bool TRACE>
+__global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
+    k_raster_bwd_absgrad(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
+    constexpr int kBatch = kBatchBwd;
+    constexpr int kRed = AbsWarpSmem::kRed;
+    __shared__ StageSmem<kBatch, TRACE, false> st;
+    __shared__ AbsWarpSmem ws[kWarps];
+    __shared__ int s_jmax;
+    const TileRange tr = tile_range(a);
+    TileBox box[kWarps];
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) box[k] = warp_box(a, tr, k);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    AbsWarpSmem& w = ws[warp];
+    const PixelSlot ps = pixel_slot(tr);
+    const float px = (float)ps.x + 0.5f;
+    const int nch = a.channels;
+    int32_t last[kPPT];
+    float ra[kPPT], py[kPPT];
+    int my_max = -1;
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+        const int y = ps.y0 + k;
+        py[k] = (float)y + 0.5f;
+        ra[k] = 0.0f;
+        last[k] = -1;
+        float Q = 0.0f;
+        if (ps.x < a.width && y < a.height) {
+            const int64_t p = ((int64_t)tr.c * a.height + y) * a.width + ps.x;
+            ra[k] = gr.render_alphas[p];
+            last[k] = gr.last_ids[p];
+            Q = -gr.grad_render_alphas[p];
+            if (a.backgrounds)
+                for (int c = 0; c < nch; ++c)
+                    Q += gr.grad_render_colors[p * nch + c] * a.backgrounds[(int64_t)tr.c * nch + c];
+        }
+        w.tq[k * kWarp + lane] = make_float2(1.0f - ra[k], Q);
+        if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
+    }
+    if (tid == 0) s_jmax = -1;
+    __syncthreads();
+    if (tr.masked || tr.start == tr.end) return;  // block-uniform
+    const int warp_max = __reduce_max_sync(0xffffffffu, my_max);
+    if (lane == 0) atomicMax(&s_jmax, warp_max);
+    __syncthreads();
+    const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
+    const unsigned lt = lanemask_lt();
+    const int x_tile = tr.tx * kTile;
+    const int y_tile = tr.ty * kTile;
+    // flush task of this lane: field (lane & 1) of buffered entry lane / 2
+    const int task_e = lane >> 1;
+    const uint32_t task_row = (uint32_t)__cvta_generic_to_shared(&w.red[task_e][lane & 1][0]);
+    float* const task_base = gr.grad_means2d_abs + (lane & 1);
+    auto flush = [&](int nslots) {
+        __syncwarp();
+        if (task_e < nslots) {
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int c = 0; c < kWarp / 4; ++c) {
+                const float4 q = lds128(task_row + 16u * (uint32_t)c);
+                acc = __fadd2_rn(acc, make_float2(q.x, q.y));
+                acc = __fadd2_rn(acc, make_float2(q.z, q.w));
+            }
+            const float sum = acc.x + acc.y;
+            if (sum != 0.0f) atomicAdd(task_base + (int64_t)w.red_gid[task_e] * 2, sum);
+        }
+        __syncwarp();
+    };
+    int nslots = 0;
+    for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
+        const int64_t b0 = max(tr.start, b1 - kBatch);
+        stage_batch<true, TRACE, kBatch, 1>(a, box, b0, b1, trace, st);
+        const int nw = st.nw[warp];
+        for (int ii = 0; ii < nw; ++ii) {
+            const int i = st.idx[warp][ii];
+            const float4 mo = st.mo[i];  // mx, my, opacity, list position
+            const int32_t j = __float_as_int(mo.w);
+            if (!TRACE && j > warp_max) continue;  // warp-uniform
+            const float4 q = st.q[i];            // a, b, c, flatten id
+            const int32_t gid = __float_as_int(q.w);
+            __syncwarp();
+            int count = 0;
+            if (TRACE) {
+                const uint4 m4 = st.tr[i][warp];
+                const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int k = 0; k < kPPT; ++k) {
+                    if ((m[k] >> lane) & 1u)
+                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                    count += __popc(m[k]);
+                }
+            } else {
+                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+#pragma unroll
+                for (int k = 0; k < kPPT; ++k) {
+                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                    const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
+                                       e.alpha >= a.alpha_cutoff && last[k] >= j;
+                    const unsigned mk = __ballot_sync(0xffffffffu, valid);
+                    if (valid) w.list[count + __popc(mk & lt)] = (int16_t)(k * kWarp + lane);
+                    count += __popc(mk);
+                }
+            }
+            if (count == 0) continue;  // warp-uniform
+            __syncwarp();
+            float va = 0.0f, vb = 0.0f;
+            const float* const col = a.colors + (int64_t)gid * nch;
+            for (int L = lane; L < count; L += kWarp) {
+                const int p = w.list[L];
+                const int ol = p & 31;
+                const int xx = x_tile + (ol & (kTile - 1));
+                const int yy = y_tile + ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
+                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, (float)xx + 0.5f);
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)yy + 0.5f);
+                const float2 tq = w.tq[p];
+                const float Tc = tq.x, Q = tq.y;
+                const bool ok = Tc < 1.0f;  // as in the chunks' pair loop
+                const float al = ok ? e.alpha : 0.0f;
+                const float one_m = 1.0f - al;
+                const float Tb = __fdividef(Tc, one_m);
+                const float* gp =
+                    gr.grad_render_colors + (((int64_t)tr.c * a.height + yy) * a.width + xx) * nch;
+                float gcol = 0.0f;  // g . color over every channel
+                for (int c = 0; c < nch; ++c) gcol += gp[c] * col[c];
+                const float g_alpha = Tb * (gcol - Q);
+                const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
+                const float g_s = -g_raw * e.raw;
+                va += fabsf(g_s * (q.x * ct.dx + q.y * e.dy));
+                vb += fabsf(g_s * (q.z * e.dy + q.y * ct.dx));
+                w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
+            }
+            reinterpret_cast<float*>(w.red[nslots][0])[lane] = va;
+            reinterpret_cast<float*>(w.red[nslots][1])[lane] = vb;
+            if (lane == 0) w.red_gid[nslots] = gid;
+            if (++nslots == kRed) {
+                flush(nslots);
+                nslots = 0;
+            }
+        }
+    }
+    if (nslots) flush(nslots);
+}
+
 template <int CH>
 void fwd_chunk(const RasterArgs& a, float* render_colors, float* render_alphas,
                int32_t* last_ids, int32_t* pair_counts, uint32_t* trace, cudaStream_t s) {
@@ -992,16 +1158,28 @@ void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace
                        cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
+    // above 4 channels the chunks leave absgrad to its own full-channel pass
+    RasterGrads gc = g;
+    if (a.channels > 4) gc.grad_means2d_abs = nullptr;
     for (int off = 0; off < a.channels; off += 4) {
         a.ch_off = off;
         a.first_chunk = off == 0;
         const int ch = a.channels - off < 4 ? a.channels - off : 4;
         switch (ch) {
-            case 1: bwd_chunk<1>(a, g, trace, s); break;
-            case 2: bwd_chunk<2>(a, g, trace, s); break;
-            case 3: bwd_chunk<3>(a, g, trace, s); break;
-            default: bwd_chunk<4>(a, g, trace, s); break;
+            case 1: bwd_chunk<1>(a, gc, trace, s); break;
+            case 2: bwd_chunk<2>(a, gc, trace, s); break;
+            case 3: bwd_chunk<3>(a, gc, trace, s); break;
+            default: bwd_chunk<4>(a, gc, trace, s); break;
         }
+    }
+    if (a.channels > 4 && g.grad_means2d_abs) {
+        a.ch_off = 0;
+        a.first_chunk = 1;
+        const dim3 gd((unsigned)tiles), b(kThreads);
+        if (trace)
+            k_raster_bwd_absgrad<true><<<gd, b, 0, s>>>(a, g, trace);
+        else
+            k_raster_bwd_absgrad<false><<<gd, b, 0, s>>>(a, g, nullptr);
     }
 }
 
