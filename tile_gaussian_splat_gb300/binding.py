@@ -90,7 +90,7 @@ def library(path):
     """Routes this module's calls to another build of the library -- the
     range-checking build, LIB_DEBUG_PATH -- while the block runs."""
     global _lib
-    saved = lib()
+    saved = _lib
     _lib = _load(path)
     try:
         yield _lib

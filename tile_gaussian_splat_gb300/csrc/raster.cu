@@ -85,6 +85,35 @@ __device__ __forceinline__ float exp_neg(float s) {
     return y;
 }
 
+// exp(-s) for a pair of pixels: the scaling as one packed multiply (each
+// component rounded as the scalar multiply), then ex2.approx per pixel.
+__device__ __forceinline__ float2 exp_neg2(float2 s) {
+    constexpr float kMinusLog2e = -1.44269504088896341f;  // -1 / ln 2
+    const float2 t = __fmul2_rn(s, make_float2(kMinusLog2e, kMinusLog2e));
+    float y0, y1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(t.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y1) : "f"(t.y));
+    return make_float2(y0, y1);
+}
+
+// Packed f32x2 add as a PTX instruction with an explicit round-to-nearest
+// mode.  Products from the __fmul2_rn intrinsic feeding it stay unfused, so
+// each component rounds exactly as the scalar __fmul_rn / __fadd_rn sequence
+// (measured bit for bit on 4 M random quadratic forms; the packed add
+// intrinsic, and a PTX multiply feeding a PTX add, were fused into packed
+// FMAs by the code generator and rounded differently).
+__device__ __forceinline__ uint64_t pack2(float2 v) {
+    return (uint64_t)__float_as_uint(v.x) | ((uint64_t)__float_as_uint(v.y) << 32);
+}
+__device__ __forceinline__ float2 unpack2(uint64_t r) {
+    return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(r);
+}
+
 // s = 0.5 (a dx^2 + c dy^2) + b dx dy rounded exactly as written (no FMA
 // contraction), alpha = min(0.99, o exp(-s)).
 __device__ __forceinline__ PairEval eval_pair(const ColumnTerms& ct, float my, float c, float op,
@@ -490,17 +519,14 @@ __global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
                     const float2 my = splat2(mo.y), op = splat2(mo.z);
 #pragma unroll
                     for (int p = 0; p < kPairs; ++p) {
-                        // s = (a/2 dx) dx + (c/2 dy) dy + (b dx) dy, per pixel.  The
-                        // sums stay scalar: a packed product feeding a packed sum is
-                        // fused into one packed FMA by the code generator despite
-                        // the explicit rounding, which would round s differently.
-                        const float2 dy = __fadd2_rn(my, npy[p]);
+                        // s = ((a/2 dx) dx + (c/2 dy) dy) + (b dx) dy, per pixel, as
+                        // packed operations that round each component as the scalar
+                        // ones (intrinsic products, PTX sums: never fused)
+                        const float2 dy = add2_rn(my, npy[p]);
                         const float2 qc2 = __fmul2_rn(__fmul2_rn(c2, dy), dy);
                         const float2 qb = __fmul2_rn(bdx, dy);
-                        const float2 sv = make_float2(__fadd_rn(__fadd_rn(qa2.x, qc2.x), qb.x),
-                                                      __fadd_rn(__fadd_rn(qa2.y, qc2.y), qb.y));
-                        const float2 raw =
-                            __fmul2_rn(op, make_float2(exp_neg(sv.x), exp_neg(sv.y)));
+                        const float2 sv = add2_rn(add2_rn(qa2, qc2), qb);
+                        const float2 raw = __fmul2_rn(op, exp_neg2(sv));
                         float2 aw;
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
