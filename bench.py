@@ -403,6 +403,7 @@ def run_ours(args, rank, world, scene):
 
     proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
     bins = time_bins(path, max_list, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
+    steps_trace = time_steps_trace(path, flush, max(args.warmup, 3), max(5, min(args.steps, 10)))
     I = path.I
     del path
     torch.cuda.empty_cache()
@@ -461,6 +462,7 @@ def run_ours(args, rank, world, scene):
         "peaks": peaks,
         "project": proj,
         "bins": bins,
+        "step_trace": steps_trace,
         "workloads": others,
         "e2e": {"value": round(whole_job_rate(pixels, e2e, world) / 1e6, 2),
                 "unit": "Mpixel/s",
@@ -726,6 +728,60 @@ def time_projection(dev, flush, warmup, steps):
                        "height": s.height, "visible_pairs": visible,
                        "outputs": "radii, means2d, depths, conics, compensations, radii_float",
                        "l2": "flushed between launches"}}
+
+
+def time_steps_trace(path, flush, warmup, steps, max_steps=64):
+    """The per-pixel step trace (gs_rasterize_fwd_steps, gs_rasterize_bwd_steps)
+    on the step's scene, timed apart: the alternative to the mask trace that
+    the step uses.  max_steps records per pixel; pixels with more composites
+    fall back to the list walk in the backward."""
+    import torch
+
+    s, d, gsb = path.s, path.d, path.gs
+    K = max_steps
+
+    def fwd():
+        return gsb.gs_rasterize_fwd_steps(d["means2d"], d["conics"], d["colors"],
+                                          d["opacities"], None, None, s.width, s.height, 16,
+                                          path.offsets, path.ids, s.alpha_cutoff,
+                                          s.transmittance_threshold, K, d_status=path.status)
+
+    _, alpha, last, st = fwd()
+
+    def bwd():
+        return gsb.gs_rasterize_bwd_steps(d["means2d"], d["conics"], d["colors"],
+                                          d["opacities"], None, None, s.width, s.height, 16,
+                                          path.offsets, path.ids, s.alpha_cutoff, alpha, last,
+                                          st, d["grad_render_colors"], d["grad_render_alphas"],
+                                          d_status=path.status)
+
+    res = {}
+    for name, fn in (("fwd", fwd), ("bwd", bwd)):
+        for _ in range(warmup):
+            fn()
+            flush.zero_()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+            flush.zero_()
+        torch.cuda.synchronize()
+        res[name] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    gsb.check_status(path.status, "steps")
+    cnt = st[2]
+    over = int((cnt > K).sum())
+    rec = int(torch.clamp(cnt, max=K).sum(dtype=torch.int64))
+    out = {"kernels": "k_raster_fwd<.., steps>, k_raster_bwd_steps", "max_steps": K,
+           "fwd_ms": round(res["fwd"], 4), "bwd_ms": round(res["bwd"], 4),
+           "fallback_pixels": over, "records": rec,
+           "record_bytes": rec * 8,
+           "note": "per-pixel step trace, the alternative to the step's mask trace; "
+                   "timed apart, not part of the step"}
+    del st
+    return out
 
 
 def time_bins(path, max_list, flush, warmup, steps):

@@ -344,6 +344,56 @@ int gs_rasterize_bwd(const float* means2d, const float* conics,
                      float* grad_means2d_abs, const uint32_t* trace,
                      int32_t* d_status, void* stream);
 
+/*
+ * gs_rasterize_fwd_steps / gs_rasterize_bwd_steps -- the forward and
+ * backward over a per-pixel step trace, the trace buffers of rlx-metal 0.2.9,
+ * src/splat_training.rs, training_forward_metal_traced (per-pixel splat ids up
+ * to max_splat_steps), in place of gs_rasterize_fwd's per-entry masks.
+ *
+ * gs_rasterize_fwd_steps: gs_rasterize_fwd (same arguments, results and
+ * errors; no pair counts or mask trace) that also records, for every pixel
+ * p = (c * H + y) * W + x and its s-th composited pair front to back
+ * (s < max_steps):
+ *   step_pos int32 (max_steps, C, H, W): the pair's list position j
+ *   step_T float32 (max_steps, C, H, W): the transmittance T before it
+ *   step_count int32 (C, H, W): the pairs the pixel composited; it may exceed
+ *     max_steps, and then only the first max_steps are recorded.
+ * Records past step_count[p] are not written.
+ *
+ * gs_rasterize_bwd_steps: gs_rasterize_bwd's result (same gradients, same
+ * zeroing, any channel count, absgrad optional) from the step trace of
+ * gs_rasterize_fwd_steps on the same inputs: one thread per pixel walks the
+ * pixel's records from its last to its first, so no other list entry is
+ * revisited and T before each pair is read instead of recovered by a
+ * division; a pixel whose step_count exceeds max_steps walks its tile's list
+ * from its last id down instead, recovering T_before = T / (1 - alpha) as
+ * gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel does.  Each pair
+ * adds its terms with global atomics (an alternative to the mask-trace
+ * backward, whose per-entry reduction is cheaper; both are measured).
+ * Limits: max_steps >= 1 and max_steps * C * H * W < 2^40; otherwise as the
+ * forward and backward above.
+ */
+int gs_rasterize_fwd_steps(const float* means2d, const float* conics, const float* colors,
+                           const float* opacities, const float* backgrounds,
+                           const int32_t* masks, int C, int N, int channels, int width,
+                           int height, int tile_size, const int32_t* offsets,
+                           const int32_t* flatten_ids, int64_t n_isects, float alpha_cutoff,
+                           float transmittance_threshold, int max_steps, float* render_colors,
+                           float* render_alphas, int32_t* last_ids, int32_t* step_pos,
+                           float* step_T, int32_t* step_count, int32_t* d_status, void* stream);
+int gs_rasterize_bwd_steps(const float* means2d, const float* conics, const float* colors,
+                           const float* opacities, const float* backgrounds,
+                           const int32_t* masks, int C, int N, int channels, int width,
+                           int height, int tile_size, const int32_t* offsets,
+                           const int32_t* flatten_ids, int64_t n_isects, float alpha_cutoff,
+                           const float* render_alphas, const int32_t* last_ids, int max_steps,
+                           const int32_t* step_pos, const float* step_T,
+                           const int32_t* step_count, const float* grad_render_colors,
+                           const float* grad_render_alphas, float* grad_means2d,
+                           float* grad_conics, float* grad_colors, float* grad_opacities,
+                           float* grad_backgrounds, float* grad_means2d_abs, int32_t* d_status,
+                           void* stream);
+
 /* Bytes of workspace gs_sort_pairs needs for n pairs. */
 size_t gs_sort_workspace_size(int64_t n);
 

@@ -63,14 +63,14 @@ def _load(path):
     L.orc_tile_offsets.restype = I32
     L.orc_rasterize_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                     P, P, I64, F32, F32, P, I64, P, P, P, P, P, F32, F32,
-                                    P, P]
+                                    P, P, I32, P, P, P]
     L.orc_rasterize_fwd.restype = I32
     L.orc_rasterize_fwd_f64.argtypes = [P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                         P, P, I64, F64, F64, P, P, P]
     L.orc_rasterize_fwd_f64.restype = I32
     L.orc_rasterize_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I32, I32, I32, I32, I32, I32,
                                     P, P, I64, F32, P, P, P, P, P, I64, P, P, P, P, P, P, P,
-                                    F32, P, P]
+                                    F32, P, P, I32, P, P, P]
     L.orc_rasterize_bwd.restype = I32
     L.orc_bin_splats.argtypes = [P, P, I32, P, I64, I64, I32, I32, I32, I64, P, P]
     L.orc_bin_splats.restype = I64
@@ -154,7 +154,8 @@ def tile_offsets(keys, C, tile_width, tile_height):
 
 def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, transmittance_threshold,
-                  pixels=None, tie_rel=0.0, tie_rel_T=None, out=None, omp=False):
+                  pixels=None, tie_rel=0.0, tie_rel_T=None, out=None, omp=False,
+                  max_steps=0):
     """Forward compositing.  Returns dict(render_colors (C,H,W,ch),
     render_alphas (C,H,W,1), last_ids (C,H,W), stats [evaluated, composited,
     near-tie pixels], near_tie (C,H,W) uint8 (near-threshold decisions per
@@ -180,6 +181,10 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
     if "comp_hash" not in out:
         out["comp_hash"] = np.zeros((C, height, width), np.uint64)
     stats = np.zeros(3, np.int64)
+    if max_steps > 0:
+        out["step_pos"] = np.full((max_steps, C, height, width), -1, np.int32)
+        out["step_T"] = np.zeros((max_steps, C, height, width), np.float32)
+        out["step_count"] = np.zeros((C, height, width), np.int32)
     px = None if pixels is None else _c(pixels, np.int64)
     rc = lib(omp).orc_rasterize_fwd(
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
@@ -188,7 +193,8 @@ def rasterize_fwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         _ptr(px), 0 if px is None else px.size, _ptr(out["render_colors"]),
         _ptr(out["render_alphas"]), _ptr(out["last_ids"]), _ptr(stats), _ptr(out["near_tie"]),
         float(tie_rel), float(tie_rel if tie_rel_T is None else tie_rel_T),
-        _ptr(out["tie_splats"]), _ptr(out["comp_hash"]))
+        _ptr(out["tie_splats"]), _ptr(out["comp_hash"]), int(max_steps),
+        _ptr(out.get("step_pos")), _ptr(out.get("step_T")), _ptr(out.get("step_count")))
     if rc != 0:
         raise ValueError("oracle forward: bad arguments")
     out["stats"] = stats
@@ -223,11 +229,14 @@ def rasterize_fwd_f64(means2d, conics, colors, opacities, backgrounds, width, he
 def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width, height,
                   tile_size, offsets, flatten_ids, alpha_cutoff, render_alphas, last_ids,
                   grad_render_colors, grad_render_alphas, want_grad_backgrounds=None,
-                  absgrad=False, pixels=None, tie_rel=0.0, magnitudes=False, omp=False):
+                  absgrad=False, pixels=None, tie_rel=0.0, magnitudes=False, omp=False,
+                  steps=None):
     """Backward.  Returns dict(grad_means2d, grad_conics, grad_colors,
     grad_opacities, grad_backgrounds (or None), grad_means2d_abs (or None),
     near_tie (C,H,W) uint8, and with magnitudes=True mag_* arrays: per
-    gradient element the sum of |per-pair term|)."""
+    gradient element the sum of |per-pair term|).  steps: the forward's step
+    records (step_pos, step_T, step_count) from rasterize_fwd(max_steps=K);
+    pixels they hold entirely read T before each pair instead of dividing."""
     means2d = _c(means2d, np.float32)
     conics = _c(conics, np.float32)
     colors = _c(colors, np.float32)
@@ -255,6 +264,13 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
                tie_splats=np.zeros((C, N), np.uint8))
     px = None if pixels is None else _c(pixels, np.int64)
     mags = np.zeros((6 + ch) * C * N, np.float64) if magnitudes else None
+    if steps is not None:
+        st_pos, st_T, st_cnt = (_c(steps[0], np.int32), _c(steps[1], np.float32),
+                                _c(steps[2], np.int32))
+        K = st_pos.shape[0]
+    else:
+        st_pos = st_T = st_cnt = None
+        K = 0
     rc = lib(omp).orc_rasterize_bwd(
         _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
         _ptr(masks), C, N, ch, width, height, tile_size, TW, TH, _ptr(offsets),
@@ -263,7 +279,7 @@ def rasterize_bwd(means2d, conics, colors, opacities, backgrounds, masks, width,
         0 if px is None else px.size, _ptr(out["grad_means2d"]), _ptr(out["grad_conics"]),
         _ptr(out["grad_colors"]), _ptr(out["grad_opacities"]), _ptr(out["grad_backgrounds"]),
         _ptr(out["grad_means2d_abs"]), _ptr(out["near_tie"]), float(tie_rel), _ptr(mags),
-        _ptr(out["tie_splats"]))
+        _ptr(out["tie_splats"]), K, _ptr(st_pos), _ptr(st_T), _ptr(st_cnt))
     if rc != 0:
         raise ValueError("oracle backward: bad arguments")
     if magnitudes:

@@ -343,6 +343,12 @@ int64_t orc_bin_splats(const float* means2d, const float* radii, int elliptical,
 //     decision (T carries the accumulated error of every 1 - alpha, which is
 //     large relative to itself for alpha near 0.99, hence its own margin).
 //   tie_splats[g] = 1 for every splat g that took part in such a decision.
+//   step_pos / step_T (max_steps, C, H, W) and step_count (C, H, W), when
+//     step_pos is not null: the per-pixel step trace of rlx-metal's traced
+//     forward (splat_training.rs, training_forward_metal_traced): for the
+//     pixel's s-th composited pair (front to back, s < max_steps) its list
+//     position and the transmittance before it; step_count = the pairs the
+//     pixel composited (the records stop at max_steps).
 //   comp_hash[pixel] = a 64-bit FNV-1a hash of the list positions j the pixel
 //     composited, in order (h = (h ^ j) * 1099511628211 from 14695981039346656037):
 //     another implementation's decisions at a pixel can be compared with these
@@ -360,6 +366,11 @@ struct FwdArgs {
     const int32_t* flatten_ids;
     int64_t n_isects;
     float alpha_cutoff, transmittance_threshold;
+    // optional step records (see orc_rasterize_fwd)
+    int max_steps;
+    int32_t* step_pos;
+    float* step_T;
+    int32_t* step_count;
 };
 
 static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
@@ -403,6 +414,12 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
             float w = T * alpha;
             const float* col = a.colors + (int64_t)a.channels * g;
             for (int ch = 0; ch < a.channels; ++ch) rgb[ch] += w * col[ch];
+            if (a.step_pos != nullptr && composited < a.max_steps) {
+                int64_t o = composited * (a.C * a.height * (int64_t)a.width) +
+                            (c * a.height + y) * (int64_t)a.width + x;
+                a.step_pos[o] = (int32_t)j;
+                a.step_T[o] = T;  // before this pair
+            }
             T = T * (1.0f - alpha);
             last = (int32_t)j;
             ++composited;
@@ -429,6 +446,7 @@ static void fwd_pixel(const FwdArgs& a, int64_t c, int x, int y, float* out_rgb,
     }
     if (near_tie) near_tie[p] = (uint8_t)std::min(n_tie, 255);
     if (comp_hash) comp_hash[p] = hash;
+    if (a.step_count) a.step_count[p] = (int32_t)composited;
 }
 
 // Renders every pixel (pixels == nullptr) or only the listed flat pixel
@@ -443,12 +461,14 @@ int orc_rasterize_fwd(const float* means2d, const float* conics, const float* co
                       float transmittance_threshold, const int64_t* pixels, int64_t n_pixels,
                       float* render_colors, float* render_alphas, int32_t* last_ids,
                       int64_t* stats, uint8_t* near_tie, float tie_rel, float tie_rel_T,
-                      uint8_t* tie_splats, uint64_t* comp_hash) {
+                      uint8_t* tie_splats, uint64_t* comp_hash, int max_steps,
+                      int32_t* step_pos, float* step_T, int32_t* step_count) {
     if (channels < 1 || channels > kMaxChannels) return 1;
     FwdArgs a = {means2d,   conics,     colors,      opacities, backgrounds,
                  masks,     C,          N,           channels,  width,
                  height,    tile_size,  tile_width,  tile_height, offsets,
-                 flatten_ids, n_isects, alpha_cutoff, transmittance_threshold};
+                 flatten_ids, n_isects, alpha_cutoff, transmittance_threshold,
+                 max_steps, step_pos, step_T, step_count};
     if (pixels == nullptr) {
         // OpenMP build: rows of pixels handed out dynamically (list lengths,
         // and so the work per row, vary a lot)
@@ -556,6 +576,10 @@ int orc_rasterize_fwd_f64(const double* means2d, const double* conics, const dou
 // tie_rel of the cutoff (low 4 bits) and those whose raw alpha was within
 // tie_rel of the clamp (high 4 bits), each saturating at 15; tie_splats
 // (optional, per splat) marks the splats of those pairs.
+// step_pos / step_T / step_count (optional, the forward's step records for
+// max_steps): a pixel whose records hold all its pairs visits just those and
+// reads T before each instead of dividing (the trace-buffer backward of
+// rlx-metal's training step); other pixels walk their list as above.
 // magnitudes (optional, double) receives, per gradient element, the sum of
 // the absolute values of its per-pair terms, laid out as grad_means2d (2CN),
 // grad_conics (3CN), grad_colors (channels*CN), grad_opacities (CN): the
@@ -570,7 +594,9 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                       const int64_t* pixels, int64_t n_pixels, float* grad_means2d,
                       float* grad_conics, float* grad_colors, float* grad_opacities,
                       float* grad_backgrounds, float* grad_means2d_abs, uint8_t* near_tie,
-                      float tie_rel, double* magnitudes, uint8_t* tie_splats) {
+                      float tie_rel, double* magnitudes, uint8_t* tie_splats, int max_steps,
+                      const int32_t* step_pos, const float* step_T,
+                      const int32_t* step_count) {
     if (channels < 1 || channels > kMaxChannels) return 1;
     int64_t CN = C * N;
     std::vector<double> gm(2 * CN, 0.0), gq(3 * CN, 0.0), gc((size_t)channels * CN, 0.0),
@@ -608,7 +634,22 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
         }
         if (masks != nullptr && masks[t] == 0) continue;
         float px = (float)x + 0.5f, py = (float)y + 0.5f;
-        for (int64_t j = end - 1; j >= start; --j) {
+        // with a step trace holding all of this pixel's pairs, the recorded
+        // pairs are visited (last to first) and T before each is read;
+        // otherwise the list is walked and T before is recovered by division
+        const int32_t n_rec = step_count ? step_count[p] : -1;
+        const bool use_steps = step_count != nullptr && n_rec <= max_steps;
+        const int64_t iters = use_steps ? n_rec : end - start;
+        for (int64_t it = 0; it < iters; ++it) {
+            int64_t j;
+            float t_rec = 0.0f;
+            if (use_steps) {
+                int64_t o = (n_rec - 1 - it) * (C * HW) + p;
+                j = step_pos[o];
+                t_rec = step_T[o];
+            } else {
+                j = end - 1 - it;
+            }
             int32_t g = flatten_ids[j];
             float dx = means2d[2 * g] - px;
             float dy = means2d[2 * g + 1] - py;
@@ -628,7 +669,7 @@ int orc_rasterize_bwd(const float* means2d, const float* conics, const float* co
                 n_clamp_tie += clamp_tie ? 1 : 0;
             }
             if (!valid) continue;
-            float Tb = Tc / (1.0f - alpha);
+            float Tb = use_steps ? t_rec : Tc / (1.0f - alpha);
             float vis = Tb * alpha;
             const float* col = colors + (int64_t)channels * g;
             float dot = 0.0f;

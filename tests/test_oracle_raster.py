@@ -555,3 +555,85 @@ def test_composite_hash_lists_the_composited_positions():
     s.means2d[:] = 40.0  # nothing reaches any pixel of the tile it still lists
     out = _fwd(s, _setup(s))
     assert (out["comp_hash"] == _fnv([])).all()
+
+
+# ------------------------------------------------------------ step trace
+
+
+def test_step_records_golden():
+    # the golden two-splat pixel composites list positions 0 then 1, with T
+    # 1 before the front splat and 0.5 before the back one (exact)
+    s = _scene([[7.5, 7.5], [7.5, 7.5]], [[1, 0, 1], [1, 0, 1]], [[1, 0, 0], [0, 1, 0]],
+               [0.5, 0.5], [1.0, 2.0], [3.0, 3.0], 16, 16, bg=[0, 0, 1])
+    iso = _setup(s)
+    out = oracle.rasterize_fwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None,
+                               16, 16, 16, iso["offsets"], iso["ids"], CUT, THR, max_steps=4)
+    assert out["step_count"][0, 7, 7] == 2
+    assert out["step_pos"][:2, 0, 7, 7].tolist() == [0, 1]
+    assert out["step_T"][:2, 0, 7, 7].tolist() == [1.0, 0.5]
+    assert (out["step_pos"][2:, 0, 7, 7] == -1).all()  # records past the count: untouched
+
+
+def _fwd_steps(s, iso, K):
+    return oracle.rasterize_fwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None,
+                                s.width, s.height, s.tile_size, iso["offsets"], iso["ids"],
+                                s.alpha_cutoff, s.transmittance_threshold, max_steps=K)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_step_backward_matches_finite_differences(seed):
+    # the backward over the step records (T before each pair read, not
+    # recovered) against central differences of the double forward
+    s, iso = _fd_scene(seed, C=1, N=10, W=32, H=32, sigma=(1.5, 5.0), opacity=(0.3, 0.95))
+    rng = np.random.default_rng(seed + 20)
+    g_rgb = rng.standard_normal((1, 32, 32, 3)).astype(np.float32)
+    g_a = rng.standard_normal((1, 32, 32, 1)).astype(np.float32)
+    fwd = _fwd_steps(s, iso, 64)
+    assert fwd["step_count"].max() <= 64
+    got = oracle.rasterize_bwd(s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None,
+                               32, 32, 16, iso["offsets"], iso["ids"], s.alpha_cutoff,
+                               fwd["render_alphas"], fwd["last_ids"], g_rgb, g_a,
+                               steps=(fwd["step_pos"], fwd["step_T"], fwd["step_count"]))
+    for name, gname, h in [("means2d", "grad_means2d", 1e-5), ("opacities", "grad_opacities", 1e-6),
+                           ("colors", "grad_colors", 1e-5), ("conics", "grad_conics", 1e-6)]:
+        base = getattr(s, name).astype(np.float64)
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            hi, lo = base.copy(), base.copy()
+            hi[idx] += h
+            lo[idx] -= h
+            fd[idx] = (_loss_f64(s, iso, g_rgb, g_a, **{name: hi})[0]
+                       - _loss_f64(s, iso, g_rgb, g_a, **{name: lo})[0]) / (2 * h)
+        np.testing.assert_allclose(got[gname], fd, rtol=1e-3, atol=1e-5 * np.abs(fd).max(),
+                                   err_msg=gname)
+
+
+def test_step_backward_equals_walk_where_recovery_is_exact_and_falls_back():
+    # with every opacity <= 0.5, T stays >= 0.5^k well away from 0 and the
+    # division recovery loses nothing measurable: the two backwards agree to
+    # float rounding.  With max_steps = 1 every pixel with two or more pairs
+    # takes the walk: the result is the walk's, bit for bit, for those pixels
+    s = scenes.random_small(31, C=2, N=40, W=48, H=32, opacity=(0.05, 0.5))
+    iso = _setup(s)
+    rng = np.random.default_rng(3)
+    g_rgb = rng.standard_normal((2, 32, 48, 3)).astype(np.float32)
+    g_a = rng.standard_normal((2, 32, 48, 1)).astype(np.float32)
+    walk = None
+    for K in (64, 1):
+        fwd = _fwd_steps(s, iso, K)
+        args = (s.means2d, s.conics, s.colors, s.opacities, s.backgrounds, None, 48, 32, 16,
+                iso["offsets"], iso["ids"], s.alpha_cutoff, fwd["render_alphas"],
+                fwd["last_ids"], g_rgb, g_a)
+        walk = oracle.rasterize_bwd(*args)
+        st = oracle.rasterize_bwd(*args, steps=(fwd["step_pos"], fwd["step_T"],
+                                                fwd["step_count"]))
+        for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities",
+                  "grad_backgrounds"):
+            if K == 64:
+                np.testing.assert_allclose(st[k], walk[k], rtol=2e-5,
+                                           atol=2e-6 * np.abs(walk[k]).max(), err_msg=k)
+    # K = 1: pixels with one pair read its T (= 1, exact either way), the rest walk
+    multi = (fwd["step_count"] > 1)
+    assert multi.any()
+    for k in ("grad_means2d", "grad_conics", "grad_colors", "grad_opacities"):
+        np.testing.assert_allclose(st[k], walk[k], rtol=1e-6, atol=1e-9, err_msg=k)

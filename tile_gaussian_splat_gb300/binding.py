@@ -52,6 +52,10 @@ SIGNATURES = {
     "gs_sort_pairs_noalloc": (I32, [P, P, I64, I32, I32, P, P]),
     "gs_debug_sort_wait_timeout": (I32, [P, P, I64, I32, I32, P, SZ, P, P]),
     "gs_peak_probe": (I32, [I32, I32, I32, P, P, P]),
+    "gs_rasterize_fwd_steps": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I64,
+                                     F32, F32, I32, P, P, P, P, P, P, P, P]),
+    "gs_rasterize_bwd_steps": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, P, P, I64,
+                                     F32, P, P, I32, P, P, P, P, P, P, P, P, P, P, P, P, P]),
 }
 
 
@@ -387,3 +391,58 @@ def gs_peak_probe(kind, iters, blocks, out, stream=None):
     _check(lib().gs_peak_probe(kind, iters, blocks, _ptr(out), ct.byref(ops), _stream(stream)),
            "gs_peak_probe")
     return int(ops.value)
+
+
+def gs_rasterize_fwd_steps(means2d, conics, colors, opacities, backgrounds, masks, width, height,
+                           tile_size, offsets, flatten_ids, alpha_cutoff,
+                           transmittance_threshold, max_steps, d_status=None, stream=None):
+    """gs_rasterize_fwd that also records the per-pixel step trace.  Returns
+    (render_colors, render_alphas, last_ids, (step_pos, step_T, step_count))
+    with step_pos int32 / step_T float32 (max_steps, C, H, W) and step_count
+    int32 (C, H, W)."""
+    C, N = means2d.shape[0], means2d.shape[1]
+    ch = colors.shape[-1]
+    dev = means2d.device
+    rgb = _empty((C, height, width, ch), torch.float32, dev)
+    alpha = _empty((C, height, width, 1), torch.float32, dev)
+    last = _empty((C, height, width), torch.int32, dev)
+    pos = _empty((max_steps, C, height, width), torch.int32, dev)
+    tb = _empty((max_steps, C, height, width), torch.float32, dev)
+    cnt = _empty((C, height, width), torch.int32, dev)
+    _check(lib().gs_rasterize_fwd_steps(
+        _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
+        _ptr(masks), C, N, ch, width, height, tile_size, _ptr(offsets), _ptr(flatten_ids),
+        flatten_ids.numel(), alpha_cutoff, transmittance_threshold, max_steps, _ptr(rgb),
+        _ptr(alpha), _ptr(last), _ptr(pos), _ptr(tb), _ptr(cnt), _ptr(d_status),
+        _stream(stream)), "gs_rasterize_fwd_steps")
+    return rgb, alpha, last, (pos, tb, cnt)
+
+
+def gs_rasterize_bwd_steps(means2d, conics, colors, opacities, backgrounds, masks, width, height,
+                           tile_size, offsets, flatten_ids, alpha_cutoff, render_alphas,
+                           last_ids, steps, grad_render_colors, grad_render_alphas,
+                           absgrad=False, d_status=None, out=None, stream=None):
+    """The backward over a step trace `steps` = (step_pos, step_T, step_count)
+    from gs_rasterize_fwd_steps.  Returns the gradients as gs_rasterize_bwd."""
+    C, N = means2d.shape[0], means2d.shape[1]
+    ch = colors.shape[-1]
+    dev = means2d.device
+    pos, tb, cnt = steps
+    if out is None:
+        out = dict(grad_means2d=_empty((C, N, 2), torch.float32, dev),
+                   grad_conics=_empty((C, N, 3), torch.float32, dev),
+                   grad_colors=_empty((C, N, ch), torch.float32, dev),
+                   grad_opacities=_empty((C, N), torch.float32, dev),
+                   grad_backgrounds=None if backgrounds is None else
+                   _empty((C, ch), torch.float32, dev),
+                   grad_means2d_abs=_empty((C, N, 2), torch.float32, dev) if absgrad else None)
+    _check(lib().gs_rasterize_bwd_steps(
+        _ptr(means2d), _ptr(conics), _ptr(colors), _ptr(opacities), _ptr(backgrounds),
+        _ptr(masks), C, N, ch, width, height, tile_size, _ptr(offsets), _ptr(flatten_ids),
+        flatten_ids.numel(), alpha_cutoff, _ptr(render_alphas), _ptr(last_ids), pos.shape[0],
+        _ptr(pos), _ptr(tb), _ptr(cnt), _ptr(grad_render_colors), _ptr(grad_render_alphas),
+        _ptr(out["grad_means2d"]), _ptr(out["grad_conics"]), _ptr(out["grad_colors"]),
+        _ptr(out["grad_opacities"]), _ptr(out["grad_backgrounds"]),
+        _ptr(out["grad_means2d_abs"]), _ptr(d_status), _stream(stream)),
+        "gs_rasterize_bwd_steps")
+    return out

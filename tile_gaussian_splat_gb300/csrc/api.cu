@@ -377,7 +377,8 @@ int raster_fwd(const float* means2d, const float* conics, const float* colors,
                const int32_t* bin_counts, int bin_capacity, const int32_t* flatten_ids,
                int64_t n_isects, float alpha_cutoff, float transmittance_threshold,
                float* render_colors, float* render_alphas, int32_t* last_ids,
-               int32_t* pair_counts, uint32_t* trace, int32_t* d_status, void* stream) {
+               int32_t* pair_counts, uint32_t* trace, int32_t* d_status, void* stream,
+               const StepArgs* steps = nullptr) {
     if (!render_colors || !render_alphas || !last_ids) return GS_ERR_INVALID_ARG;
     if (trace && (reinterpret_cast<uintptr_t>(trace) & 15u)) return GS_ERR_INVALID_ARG;
     RasterArgs a{means2d, conics, colors, opacities, backgrounds, masks,
@@ -385,7 +386,7 @@ int raster_fwd(const float* means2d, const float* conics, const float* colors,
                  offsets, flatten_ids, n_isects, alpha_cutoff, transmittance_threshold,
                  channels, 0, 1, bin_counts, bin_capacity, d_status};
     launch_raster_fwd(a, render_colors, render_alphas, last_ids, pair_counts, trace,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), steps);
     return check_launch();
 }
 
@@ -398,7 +399,7 @@ int raster_bwd(const float* means2d, const float* conics, const float* colors,
                const float* grad_render_alphas, float* grad_means2d, float* grad_conics,
                float* grad_colors, float* grad_opacities, float* grad_backgrounds,
                float* grad_means2d_abs, const uint32_t* trace, int32_t* d_status,
-               void* stream) {
+               void* stream, const StepArgs* steps = nullptr) {
     if (!render_alphas || !last_ids || !grad_render_colors || !grad_render_alphas)
         return GS_ERR_INVALID_ARG;
     const int64_t CN = (int64_t)C * N;
@@ -426,7 +427,10 @@ int raster_bwd(const float* means2d, const float* conics, const float* colors,
     RasterGrads g{render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                   grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                   grad_means2d_abs};
-    launch_raster_bwd(a, g, trace, s);
+    if (steps)
+        launch_raster_bwd_steps(a, g, *steps, s);
+    else
+        launch_raster_bwd(a, g, trace, s);
     return check_launch();
 }
 
@@ -452,7 +456,6 @@ int gs_rasterize_fwd(const float* means2d, const float* conics, const float* col
                      float alpha_cutoff, float transmittance_threshold, float* render_colors,
                      float* render_alphas, int32_t* last_ids, int32_t* pair_counts,
                      uint32_t* trace, int32_t* d_status, void* stream) {
-    (void)d_status;
     if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
                         tile_size, offsets, flatten_ids, n_isects))
         return GS_ERR_INVALID_ARG;
@@ -471,7 +474,6 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
                      float* grad_means2d, float* grad_conics, float* grad_colors,
                      float* grad_opacities, float* grad_backgrounds, float* grad_means2d_abs,
                      const uint32_t* trace, int32_t* d_status, void* stream) {
-    (void)d_status;
     if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
                         tile_size, offsets, flatten_ids, n_isects))
         return GS_ERR_INVALID_ARG;
@@ -480,6 +482,57 @@ int gs_rasterize_bwd(const float* means2d, const float* conics, const float* col
                       render_alphas, last_ids, grad_render_colors, grad_render_alphas,
                       grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
                       grad_means2d_abs, trace, d_status, stream);
+}
+
+// The step-trace arrays: max_steps >= 1, pos/T of max_steps * C*H*W elements.
+static int steps_ok(int max_steps, int C, int width, int height, const void* pos, const void* T,
+                    const void* count) {
+    if (max_steps < 1 || !pos || !T || !count) return 0;
+    return (int64_t)max_steps * C * width * height < ((int64_t)1 << 40);
+}
+
+int gs_rasterize_fwd_steps(const float* means2d, const float* conics, const float* colors,
+                           const float* opacities, const float* backgrounds,
+                           const int32_t* masks, int C, int N, int channels, int width,
+                           int height, int tile_size, const int32_t* offsets,
+                           const int32_t* flatten_ids, int64_t n_isects, float alpha_cutoff,
+                           float transmittance_threshold, int max_steps, float* render_colors,
+                           float* render_alphas, int32_t* last_ids, int32_t* step_pos,
+                           float* step_T, int32_t* step_count, int32_t* d_status, void* stream) {
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects) ||
+        !steps_ok(max_steps, C, width, height, step_pos, step_T, step_count))
+        return GS_ERR_INVALID_ARG;
+    const StepArgs sa{step_pos, step_T, step_count, max_steps};
+    return raster_fwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
+                      transmittance_threshold, render_colors, render_alphas, last_ids, nullptr,
+                      nullptr, d_status, stream, &sa);
+}
+
+int gs_rasterize_bwd_steps(const float* means2d, const float* conics, const float* colors,
+                           const float* opacities, const float* backgrounds,
+                           const int32_t* masks, int C, int N, int channels, int width,
+                           int height, int tile_size, const int32_t* offsets,
+                           const int32_t* flatten_ids, int64_t n_isects, float alpha_cutoff,
+                           const float* render_alphas, const int32_t* last_ids, int max_steps,
+                           const int32_t* step_pos, const float* step_T,
+                           const int32_t* step_count, const float* grad_render_colors,
+                           const float* grad_render_alphas, float* grad_means2d,
+                           float* grad_conics, float* grad_colors, float* grad_opacities,
+                           float* grad_backgrounds, float* grad_means2d_abs, int32_t* d_status,
+                           void* stream) {
+    if (!raster_args_ok(means2d, conics, colors, opacities, C, N, channels, width, height,
+                        tile_size, offsets, flatten_ids, n_isects) ||
+        !steps_ok(max_steps, C, width, height, step_pos, step_T, step_count))
+        return GS_ERR_INVALID_ARG;
+    const StepArgs sa{const_cast<int32_t*>(step_pos), const_cast<float*>(step_T),
+                      const_cast<int32_t*>(step_count), max_steps};
+    return raster_bwd(means2d, conics, colors, opacities, backgrounds, masks, C, N, channels,
+                      width, height, offsets, nullptr, 0, flatten_ids, n_isects, alpha_cutoff,
+                      render_alphas, last_ids, grad_render_colors, grad_render_alphas,
+                      grad_means2d, grad_conics, grad_colors, grad_opacities, grad_backgrounds,
+                      grad_means2d_abs, nullptr, d_status, stream, &sa);
 }
 
 int gs_bin_splats(const float* means2d, const float* radii, int elliptical, const float* depths,

@@ -115,11 +115,21 @@ struct RasterArgs {
     int32_t* d_status;  // caller's status word or null
 };
 
+// Per-pixel step trace: pos int32 and T float32 (max_steps, C*H*W), count
+// int32 (C*H*W).
+struct StepArgs {
+    int32_t* pos;
+    float* T;
+    int32_t* count;
+    int max_steps;
+};
+
 // trace (may be null): per list entry 8 words, the tile pixels that composited it.
-// Runs one launch per chunk of up to 4 channels.
+// steps (may be null): the per-pixel step trace to record (then no trace or
+// pair counts).  Runs one launch per chunk of up to 4 channels.
 void launch_raster_fwd(RasterArgs a, float* render_colors, float* render_alphas,
                        int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
-                       cudaStream_t s);
+                       cudaStream_t s, const StepArgs* steps = nullptr);
 
 struct RasterGrads {
     const float* render_alphas;
@@ -136,6 +146,9 @@ struct RasterGrads {
 
 void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace,
                        cudaStream_t s);
+// The backward over a per-pixel step trace (one thread per pixel, all channels).
+void launch_raster_bwd_steps(RasterArgs a, const RasterGrads& g, const StepArgs& steps,
+                             cudaStream_t s);
 
 // ---- projection (project.cu)
 struct ProjectArgs {

@@ -424,6 +424,21 @@ __device__ __forceinline__ PixelSlot pixel_slot(const TileRange& tr) {
 
 // ------------------------------------------------------------------ forward
 
+// Per-pixel step trace (optional forward output, read by the per-pixel
+// backward): for pixel p and its s-th composited pair (front to back, s <
+// max_steps) the pair's list position pos[s * npix + p] and the
+// transmittance before it T[s * npix + p] (step-major, so neighbouring
+// pixels' records of one step are neighbours); count[p] = the pairs the
+// pixel composited, which may exceed max_steps (then the records stop at
+// max_steps and the backward re-walks that pixel's list).
+struct StepTrace {
+    int32_t* pos;
+    float* T;
+    int32_t* count;
+    int max_steps;
+    int64_t npix;
+};
+
 // *dst = v by lane 0 only, as one predicated store (written as a branch
 // around the store, the per-entry trace store made the forward 4 % slower).
 __device__ __forceinline__ void st_shared_lane0(uint32_t* dst, uint4 v, int lane) {
@@ -448,11 +463,11 @@ __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 // strip) with the packed f32x2 operations, whose per-component rounding is
 // that of the scalar operation, so results are bit for bit those of the
 // scalar code.
-template <int CH, bool COUNT, bool TRACE>
-__global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
+template <int CH, bool COUNT, bool TRACE, bool STEPS = false>
+__global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLOCKS)
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
                  int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts,
-                 uint32_t* __restrict__ trace) {
+                 uint32_t* __restrict__ trace, StepTrace stp = StepTrace{}) {
     constexpr int kBatch = kBatchFwd;
     constexpr int kPairs = kPPT / 2;
     __shared__ StageSmem<kBatch, false, true> st;
@@ -473,12 +488,29 @@ __global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
     // stays live across entries.  The pair counters keep an explicit flag.
     float cut[kPPT];
     bool done_c[COUNT ? kPPT : 1];
+    // step trace: records written per pixel, and the pixel's index
+    int32_t n_rec[STEPS ? kPPT : 1];
+    int64_t pix[STEPS ? kPPT : 1];
+    auto record = [&](int k, int32_t j, float t_before) {
+        if (STEPS) {
+            if (n_rec[k] < stp.max_steps) {
+                const int64_t o = (int64_t)n_rec[k] * stp.npix + pix[k];
+                stp.pos[o] = j;
+                stp.T[o] = t_before;
+            }
+            ++n_rec[k];
+        }
+    };
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         last[k] = -1;
         n_eval[k] = n_comp[k] = n_last[k] = 0;
         const bool outside = !(ps.x < a.width && ps.y0 + k < a.height);
         cut[k] = outside ? INFINITY : a.alpha_cutoff;
+        if (STEPS) {
+            n_rec[k] = 0;
+            pix[k] = ((int64_t)tr.c * a.height + ps.y0 + k) * a.width + ps.x;
+        }
         if (COUNT) done_c[k] = outside;
         py[k] = (float)(ps.y0 + k) + 0.5f;
     }
@@ -538,6 +570,11 @@ __global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
                             // a pair not taken adds exactly 0 (finite colours, T)
                             comp(aw, e) = took[k] ? alpha : 0.0f;
                         }
+                        if (STEPS) {
+#pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                if (took[2 * p + e]) record(2 * p + e, j, comp(T[p], e));
+                        }
                         const float2 w = __fmul2_rn(T[p], aw);
 #pragma unroll
                         for (int c = 0; c < CH; ++c)
@@ -577,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
                     for (int k = 0; k < kPPT; ++k) {
                         if (!took[k]) continue;
                         float& Tk = comp(T[k >> 1], k & 1);
+                        record(k, j, Tk);
                         const float w = Tk * alpha[k];
 #pragma unroll
                         for (int c = 0; c < CH; ++c) {
@@ -636,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, COUNT ? 12 : GS_FWD_MIN_BLOCKS)
             if (!a.first_chunk) continue;
             out_alpha[p] = 1.0f - Tk;
             out_last[p] = last[k];
+            if (STEPS) stp.count[p] = n_rec[k];
             if (COUNT) {
                 out_counts[3 * p] = n_eval[k];
                 out_counts[3 * p + 1] = n_comp[k];
@@ -1117,12 +1156,143 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     if (nslots) flush(nslots);
 }
 
+// ------------------------------------------------ per-pixel step-trace backward
+
+// The backward over the forward's per-pixel step trace (the trace buffers of
+// rlx-metal's traced training step, splat_training.rs): one thread per pixel
+// walks that pixel's recorded pairs from its last to its first -- no other
+// list entry is visited and the transmittance before each pair is read, not
+// recovered by division.  A pixel that composited more pairs than were
+// recorded walks its tile's list from its last id down instead, with the
+// recovery T_before = T / (1 - alpha) (gsplat 1.0.0, raster_backward.c,
+// gs_raster_backward_pixel).  Every channel is handled in one pass (colours
+// and upstream gradients read from global memory per pair); each pair adds
+// its terms with global atomics.
+constexpr int kStepThreads = kTile * kTile;
+
+template <bool ABS>
+__global__ void __launch_bounds__(kStepThreads)
+    k_raster_bwd_steps(RasterArgs a, RasterGrads gr, StepTrace stp) {
+    const TileRange tr = tile_range(a);
+    const int lx = threadIdx.x & (kTile - 1), ly = threadIdx.x / kTile;
+    const int x = tr.tx * kTile + lx, y = tr.ty * kTile + ly;
+    const bool inside = x < a.width && y < a.height;
+    const int nch = a.channels;
+    const int64_t p = inside ? ((int64_t)tr.c * a.height + y) * a.width + x : 0;
+    const float ra = inside ? gr.render_alphas[p] : 0.0f;
+    const float Tfinal = 1.0f - ra;
+    const float* bg = a.backgrounds ? a.backgrounds + (int64_t)tr.c * nch : nullptr;
+    const float* gp = gr.grad_render_colors + p * nch;
+    // dL/dbackground: sum over pixels of g (1 - render_alpha), per channel
+    if (gr.grad_backgrounds) {
+        const int lane = threadIdx.x & 31;
+        for (int c = 0; c < nch; ++c) {
+            float v = inside ? gp[c] * Tfinal : 0.0f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0 && v != 0.0f) atomicAdd(&gr.grad_backgrounds[(int64_t)tr.c * nch + c], v);
+        }
+    }
+    if (!inside || tr.masked || !(ra > 0.0f)) return;
+    const float px = (float)x + 0.5f, py = (float)y + 0.5f;
+    const int64_t CN = (int64_t)a.C * a.N;
+    // Q = g . rem - g_a T_after, from g . background - g_a (see k_raster_bwd)
+    float Q = -gr.grad_render_alphas[p];
+    if (bg)
+        for (int c = 0; c < nch; ++c) Q += gp[c] * bg[c];
+    // the terms of one pair; T_before given, T_after (Tc) the guard
+    auto pair = [&](int32_t g, float t_before, const PairEval& e, float dx, float al) {
+        const float* q = a.conics + 3 * (int64_t)g;
+        const float* col = a.colors + (int64_t)g * nch;
+        const float vis = t_before * al;
+        float gcol = 0.0f;
+        for (int c = 0; c < nch; ++c) {
+            const float t = gp[c] * vis;
+            if (t != 0.0f) atomicAdd(&gr.grad_colors[(int64_t)g * nch + c], t);
+            gcol += gp[c] * col[c];
+        }
+        const float g_alpha = t_before * (gcol - Q);
+        const float g_raw = al > 0.0f && e.raw < kAlphaClamp ? g_alpha : 0.0f;
+        const float g_s = -g_raw * e.raw;
+        if (g_s != 0.0f || g_raw != 0.0f) {
+            atomicAdd(&gr.grad_opacities[g], g_raw * e.resp);
+            const float gmx = g_s * (q[0] * dx + q[1] * e.dy);
+            const float gmy = g_s * (q[2] * e.dy + q[1] * dx);
+            atomicAdd(&gr.grad_means2d[2 * (int64_t)g], gmx);
+            atomicAdd(&gr.grad_means2d[2 * (int64_t)g + 1], gmy);
+            atomicAdd(&gr.grad_conics[3 * (int64_t)g], g_s * (0.5f * dx * dx));
+            atomicAdd(&gr.grad_conics[3 * (int64_t)g + 1], g_s * (dx * e.dy));
+            atomicAdd(&gr.grad_conics[3 * (int64_t)g + 2], g_s * (0.5f * e.dy * e.dy));
+            if (ABS) {
+                atomicAdd(&gr.grad_means2d_abs[2 * (int64_t)g], fabsf(gmx));
+                atomicAdd(&gr.grad_means2d_abs[2 * (int64_t)g + 1], fabsf(gmy));
+            }
+        }
+        Q = al * gcol + (1.0f - al) * Q;
+    };
+    auto eval_at = [&](int32_t g, float& dx) {
+        const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
+        const float* q = a.conics + 3 * (int64_t)g;
+        const ColumnTerms ct = column_terms(m.x, q[0], q[1], px);
+        dx = ct.dx;
+        return eval_pair(ct, m.y, q[2], a.opacities[g], py);
+    };
+    const int n = stp.count[p];
+    if (n <= stp.max_steps) {
+        // the recorded pairs, last to first; each was composited by the
+        // forward with these same operations, so only the T < 1 guard of the
+        // reverse walk remains to test
+        float Tc = Tfinal;
+        for (int s2 = n - 1; s2 >= 0; --s2) {
+            const int64_t o = (int64_t)s2 * stp.npix + p;
+            const int32_t j = stp.pos[o];
+            const float t_before = stp.T[o];
+            if (j < 0 || j >= a.n_isects) {  // only from a corrupted trace
+                GS_BOUNDS_REPORT(a.d_status);
+                continue;
+            }
+            const int32_t g = a.flatten_ids[j];
+            if ((uint64_t)g >= (uint64_t)CN) {
+                GS_BOUNDS_REPORT(a.d_status);
+                continue;
+            }
+            float dx;
+            const PairEval e = eval_at(g, dx);
+            const float al = Tc < 1.0f ? e.alpha : 0.0f;
+            pair(g, t_before, e, dx, al);
+            Tc = t_before;
+        }
+    } else {
+        // more pairs than records: the pixel's list walk, last id down
+        const int32_t last = gr.last_ids[p];
+        const int64_t hi = min((int64_t)last, tr.end - 1);
+        float Tc = Tfinal;
+        for (int64_t j = hi; j >= tr.start; --j) {
+            const int32_t g = a.flatten_ids[j];
+            if ((uint64_t)g >= (uint64_t)CN) {
+                GS_BOUNDS_REPORT(a.d_status);
+                continue;
+            }
+            float dx;
+            const PairEval e = eval_at(g, dx);
+            if (!(e.s >= 0.0f && e.alpha >= a.alpha_cutoff && Tc < 1.0f)) continue;
+            const float t_before = Tc / (1.0f - e.alpha);
+            pair(g, t_before, e, dx, e.alpha);
+            Tc = t_before;
+        }
+    }
+}
+
 template <int CH>
 void fwd_chunk(const RasterArgs& a, float* render_colors, float* render_alphas,
-               int32_t* last_ids, int32_t* pair_counts, uint32_t* trace, cudaStream_t s) {
+               int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
+               const StepTrace* steps, cudaStream_t s) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     const dim3 g((unsigned)tiles), b(kThreads);
-    if (pair_counts && trace)
+    if (steps)
+        k_raster_fwd<CH, false, false, true><<<g, b, 0, s>>>(a, render_colors, render_alphas,
+                                                            last_ids, nullptr, nullptr, *steps);
+    else if (pair_counts && trace)
         k_raster_fwd<CH, true, true><<<g, b, 0, s>>>(a, render_colors, render_alphas, last_ids,
                                                      pair_counts, trace);
     else if (pair_counts)
@@ -1162,22 +1332,42 @@ void bwd_chunk(const RasterArgs& a, const RasterGrads& g, const uint32_t* trace,
 // to the full gradient (the render_alpha term is added by the first chunk).
 void launch_raster_fwd(RasterArgs a, float* render_colors, float* render_alphas,
                        int32_t* last_ids, int32_t* pair_counts, uint32_t* trace,
-                       cudaStream_t s) {
+                       cudaStream_t s, const StepArgs* step_args) {
     const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
     if (tiles <= 0) return;
+    StepTrace stp{};
+    if (step_args)
+        stp = StepTrace{step_args->pos, step_args->T, step_args->count, step_args->max_steps,
+                        (int64_t)a.C * a.height * a.width};
     for (int off = 0; off < a.channels; off += 4) {
         a.ch_off = off;
         a.first_chunk = off == 0;
         const int ch = a.channels - off < 4 ? a.channels - off : 4;
         int32_t* pc = off == 0 ? pair_counts : nullptr;
         uint32_t* tr = off == 0 ? trace : nullptr;
+        const StepTrace* st = off == 0 && step_args ? &stp : nullptr;
         switch (ch) {
-            case 1: fwd_chunk<1>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
-            case 2: fwd_chunk<2>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
-            case 3: fwd_chunk<3>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
-            default: fwd_chunk<4>(a, render_colors, render_alphas, last_ids, pc, tr, s); break;
+            case 1: fwd_chunk<1>(a, render_colors, render_alphas, last_ids, pc, tr, st, s); break;
+            case 2: fwd_chunk<2>(a, render_colors, render_alphas, last_ids, pc, tr, st, s); break;
+            case 3: fwd_chunk<3>(a, render_colors, render_alphas, last_ids, pc, tr, st, s); break;
+            default: fwd_chunk<4>(a, render_colors, render_alphas, last_ids, pc, tr, st, s); break;
         }
     }
+}
+
+void launch_raster_bwd_steps(RasterArgs a, const RasterGrads& g, const StepArgs& step_args,
+                             cudaStream_t s) {
+    const int64_t tiles = (int64_t)a.C * a.tile_width * a.tile_height;
+    if (tiles <= 0) return;
+    a.ch_off = 0;
+    a.first_chunk = 1;
+    const StepTrace stp{step_args.pos, step_args.T, step_args.count, step_args.max_steps,
+                        (int64_t)a.C * a.height * a.width};
+    const dim3 gd((unsigned)tiles), b(kStepThreads);
+    if (g.grad_means2d_abs)
+        k_raster_bwd_steps<true><<<gd, b, 0, s>>>(a, g, stp);
+    else
+        k_raster_bwd_steps<false><<<gd, b, 0, s>>>(a, g, stp);
 }
 
 void launch_raster_bwd(RasterArgs a, const RasterGrads& g, const uint32_t* trace,
