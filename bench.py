@@ -401,9 +401,13 @@ def run_ours(args, rank, world, scene):
     path.run_e2e(3)
     e2e = max_over_ranks(path.run_e2e(max(5, min(args.steps, 20))), world, dev)
 
-    proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
-    bins = time_bins(path, max_list, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
-    steps_trace = time_steps_trace(path, flush, max(args.warmup, 3), max(5, min(args.steps, 10)))
+    proj = bins = steps_trace = None
+    if not args.main_only:
+        proj = time_projection(dev, flush, max(args.warmup, 3), max(5, min(args.steps, 20)))
+        bins = time_bins(path, max_list, flush, max(args.warmup, 3),
+                         max(5, min(args.steps, 20)))
+        steps_trace = time_steps_trace(path, flush, max(args.warmup, 3),
+                                       max(5, min(args.steps, 10)))
     I = path.I
     del path
     torch.cuda.empty_cache()
@@ -416,10 +420,10 @@ def run_ours(args, rank, world, scene):
 
     if rank != 0:
         return None
-    proj.update(achieved_gbs=round(proj["bytes"] / (proj["ms"] * 1e-3) / 1e9, 1))
-    proj["frac"] = round(proj["achieved_gbs"] / hbm_peak, 4)
-    bins.update(achieved_gbs=round(bins["bytes"] / (bins["ms"] * 1e-3) / 1e9, 1))
-    bins["frac"] = round(bins["achieved_gbs"] / hbm_peak, 4)
+    for side in (proj, bins):
+        if side is not None:
+            side["achieved_gbs"] = round(side["bytes"] / (side["ms"] * 1e-3) / 1e9, 1)
+            side["frac"] = round(side["achieved_gbs"] / hbm_peak, 4)
     st = stage_ms.mean(axis=0)
     clk = clocks.summary()
     stages = stage_report(s, I, st, work, peaks, hbm_peak)
@@ -933,7 +937,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--main-only", action="store_true",
-                    help="skip the workload 2/4/5 lines (profiling runs)")
+                    help="time the step alone: no projection, bin-list, step-trace or "
+                         "workload 2/4/5 lines (profiling runs)")
     ap.add_argument("--workload", type=int, default=3, choices=[2, 3, 4],
                     help="3 is the measured workload; 2 and 4 serve profiling")
     args = ap.parse_args()
