@@ -111,9 +111,12 @@ def _walked_splats(s, offsets, flatten_ids, pixels, lasts):
 
 
 def _bwd_case(s, masks=None, absgrad=True, seed=1, nudges=1):
-    """Oracle and GPU backward on the same (oracle) forward state; splats in
-    the walked part of any pixel that still has a near-tie pair are left
-    out."""
+    """Oracle and GPU backward on the same (oracle) forward state.  The GPU
+    backward re-decides every pair with the GPU's arithmetic, which is the
+    GPU forward's: at the pixels flagged near a decision, the GPU forward's
+    composited positions (from its trace) are compared with the oracle's,
+    and the walked part of a pixel where they differ (or with a pair near
+    the 0.99 clamp) is left out."""
     iso, ref, rb, g_rgb, g_a = _oracle_bwd_state(s, masks, absgrad, seed, nudges)
     d = scene_to_dev(s)
     # the GPU backward gets the oracle's forward state, so it is compared alone
@@ -123,8 +126,12 @@ def _bwd_case(s, masks=None, absgrad=True, seed=1, nudges=1):
                               to_dev(ref["render_alphas"]), to_dev(ref["last_ids"]),
                               to_dev(g_rgb), to_dev(g_a), absgrad=absgrad)
     torch.cuda.synchronize()
-    tie_pix = np.nonzero(rb["near_tie"].reshape(-1))[0]
-    excluded = _walked_splats(s, iso["offsets"], iso["flatten_ids"], tie_pix, [ref["last_ids"]])
+    f, tr = _gpu_fwd_with_trace(s, d, masks=masks)
+    excl_pix, flagged, flipped = flipped_pixels(ref, rb, tr, f, s.width, s.height)
+    log_parity(kind="decisions", flagged_pixels=flagged, flipped_pixels=flipped,
+               left_out_pixels=int(excl_pix.size))
+    excluded = _walked_splats(s, iso["offsets"], iso["flatten_ids"], excl_pix,
+                              [ref["last_ids"], f["last_ids"].cpu().numpy()])
     return rb, got, excluded
 
 
