@@ -40,7 +40,8 @@ struct FillSmem {
 
 __global__ void __launch_bounds__(kFillThreads)
     k_bin_fill(const float* __restrict__ means2d, const float* __restrict__ radii, int elliptical,
-               int64_t CN, int N, float ts, int tile_width, int tile_height, int capacity,
+               int64_t CN, int N, float ts, float inv_ts, int tile_width, int tile_height,
+               int capacity,
                int32_t* __restrict__ bins, int32_t* __restrict__ counts) {
     __shared__ FillSmem sm;
     const int tid = threadIdx.x;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(kFillThreads)
             } else {
                 rx = ry = radii[i];
             }
-            const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+            const Rect r = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
             cnt[u] = (r.x1 - r.x0) * (r.y1 - r.y0);
             sm.x0[slot] = r.x0;
             sm.y0[slot] = r.y0;
@@ -207,7 +208,8 @@ int launch_bin_splats(const float* means2d, const float* radii, int elliptical,
     if (CN > 0) {
         const int64_t chunks = (CN + kFillSplats - 1) / kFillSplats;
         k_bin_fill<<<(unsigned)chunks, kFillThreads, 0, s>>>(
-            means2d, radii, elliptical, CN, N, (float)tile_size, tile_width, tile_height,
+            means2d, radii, elliptical, CN, N, (float)tile_size, exact_tile_inverse(tile_size),
+            tile_width, tile_height,
             capacity, bins, counts);
     }
     const int smem = bin_sort_smem_bytes(capacity);

@@ -153,15 +153,24 @@ __device__ __forceinline__ int clamp_to_grid(float v, int maximum) {
     return (int)v;
 }
 
+// v / ts in IEEE single precision.  When ts is a power of two its
+// reciprocal is exact and v * (1 / ts) is the correctly rounded value of the
+// same real number as v / ts, so the multiply gives the division's bits
+// (subnormal, infinite and NaN results included); inv_ts > 0 selects it and
+// is passed only for such ts (exact_tile_inverse).
+__device__ __forceinline__ float div_tile(float v, float ts, float inv_ts) {
+    return inv_ts > 0.0f ? __fmul_rn(v, inv_ts) : __fdiv_rn(v, ts);
+}
+
 __device__ __forceinline__ Rect splat_rect(float mx, float my, float rx, float ry, float ts,
-                                           int tile_width, int tile_height) {
+                                           float inv_ts, int tile_width, int tile_height) {
     Rect r = {0, 0, 0, 0};
     if (!(isfinite(mx) && isfinite(my) && isfinite(rx) && isfinite(ry))) return r;
     if (rx <= 0.0f || ry <= 0.0f) return r;
-    r.x0 = clamp_to_grid(floorf(__fdiv_rn(__fsub_rn(mx, rx), ts)), tile_width);
-    r.y0 = clamp_to_grid(floorf(__fdiv_rn(__fsub_rn(my, ry), ts)), tile_height);
-    r.x1 = clamp_to_grid(ceilf(__fdiv_rn(__fadd_rn(mx, rx), ts)), tile_width);
-    r.y1 = clamp_to_grid(ceilf(__fdiv_rn(__fadd_rn(my, ry), ts)), tile_height);
+    r.x0 = clamp_to_grid(floorf(div_tile(__fsub_rn(mx, rx), ts, inv_ts)), tile_width);
+    r.y0 = clamp_to_grid(floorf(div_tile(__fsub_rn(my, ry), ts, inv_ts)), tile_height);
+    r.x1 = clamp_to_grid(ceilf(div_tile(__fadd_rn(mx, rx), ts, inv_ts)), tile_width);
+    r.y1 = clamp_to_grid(ceilf(div_tile(__fadd_rn(my, ry), ts, inv_ts)), tile_height);
     return r;
 }
 

@@ -55,6 +55,12 @@ void launch_onesweep_u32_widen(const uint32_t* keys_in, const int32_t* vals_in,
                                LookbackScratch lb, int32_t* abort_flag, int32_t* d_status,
                                cudaStream_t s);
 
+// 1 / tile_size when tile_size is a power of two (then exact, and the tile
+// bounds may multiply by it instead of dividing), else 0.
+inline float exact_tile_inverse(int tile_size) {
+    return tile_size > 0 && (tile_size & (tile_size - 1)) == 0 ? 1.0f / (float)tile_size : 0.0f;
+}
+
 // ---- isect.cu
 constexpr int kIsectThreads = 256;
 constexpr int kEmitChunk = 2 * kIsectThreads;  // splats per emit block

@@ -38,8 +38,9 @@ constexpr int kThreads = kIsectThreads;
 
 __global__ void __launch_bounds__(kThreads)
     k_isect_count(const float* __restrict__ means2d, const float* __restrict__ radii,
-                  int elliptical, int64_t CN, float ts, int tile_width, int tile_height,
-                  int32_t* __restrict__ tiles_per_gauss, unsigned long long* __restrict__ total) {
+                  int elliptical, int64_t CN, float ts, float inv_ts, int tile_width,
+                  int tile_height, int32_t* __restrict__ tiles_per_gauss,
+                  unsigned long long* __restrict__ total) {
     __shared__ int64_t scratch[32];
     int64_t local = 0;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(kThreads)
         } else {
             rx = ry = radii[i];
         }
-        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
         const int cnt = (r.x1 - r.x0) * (r.y1 - r.y0);
         if (tiles_per_gauss) tiles_per_gauss[i] = cnt;
         local += cnt;
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     k_rect_hist(const float* __restrict__ means2d, const float* __restrict__ radii,
                 int elliptical, const uint32_t* __restrict__ dbits, int64_t CN, float ts,
-                int tile_width, int tile_height, int4* __restrict__ rects,
+                float inv_ts, int tile_width, int tile_height, int4* __restrict__ rects,
                 uint32_t* __restrict__ hist) {
     constexpr int kW = kThreads / kWarp;
     // one private histogram per warp and digit; a digit shared by the whole
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads)
             } else {
                 rx = ry = radii[i];
             }
-            const Rect rc = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+            const Rect rc = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
             rects[i] = make_int4(rc.x0, rc.y0, rc.x1, rc.y1);
             key = dbits[i];
         }
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kThreads)
     k_isect_emit(const float* __restrict__ means2d, const float* __restrict__ radii, int elliptical,
                  const float* __restrict__ depths, const int4* __restrict__ rects,
                  const int32_t* __restrict__ order, int64_t CN,
-                 float ts, int tile_width, int tile_height, int N, int tile_bits,
+                 float ts, float inv_ts, int tile_width, int tile_height, int N, int tile_bits,
                  uint64_t* __restrict__ keys, uint32_t* __restrict__ keys32,
                  int32_t* __restrict__ ids, int64_t capacity,
                  int32_t* __restrict__ tiles_per_gauss, uint64_t* __restrict__ lookback,
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kThreads)
                 } else {
                     rx = ry = radii[s];
                 }
-                r = splat_rect(m.x, m.y, rx, ry, ts, tile_width, tile_height);
+                r = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
             }
             cnt[u] = (r.x1 - r.x0) * (r.y1 - r.y0);
             sm.x0[slot] = r.x0;
@@ -318,14 +319,12 @@ __device__ __forceinline__ int64_t flat_tile(uint64_t key, int C, int64_t per_ca
 
 // Tile ids of positions i - 1 and i (position n is the end: every tile
 // after the last key starts there) -> offsets of the tiles in between.
-__device__ __forceinline__ void range_step(int64_t i, int64_t n, uint64_t prev_key,
-                                           uint64_t key, int C, int64_t per_camera,
-                                           int tile_bits, int32_t* __restrict__ offsets,
-                                           int32_t* d_status) {
-    const int64_t ntiles = (int64_t)C * per_camera;
-    bool ok_cur = true, ok_prev = true;
-    const int64_t cur = i < n ? flat_tile(key, C, per_camera, tile_bits, &ok_cur) : ntiles;
-    const int64_t prev = i > 0 ? flat_tile(prev_key, C, per_camera, tile_bits, &ok_prev) : -1;
+// Tile ids of positions i - 1 (prev) and i (cur; position n is the end:
+// every tile after the last key starts there) -> offsets of the tiles in
+// between.  ok_* say whether the key lies inside the grid.
+__device__ __forceinline__ void range_step(int64_t i, int64_t cur, bool ok_cur, int64_t prev,
+                                           bool ok_prev, int64_t ntiles,
+                                           int32_t* __restrict__ offsets, int32_t* d_status) {
     if (!ok_cur) {
         report(d_status, GS_ERR_KEY_OUT_OF_GRID);
         return;
@@ -369,12 +368,20 @@ __global__ void __launch_bounds__(kThreads)
         // complete whenever this one has a position <= n)
         uint64_t before = __shfl_up_sync(0xffffffffu, k[3], 1);
         if (lane == 0 && p0 > 0 && p0 <= n) before = keys[p0 - 1];
+        const int64_t ntiles = (int64_t)C * per_camera;
+        // each key's tile id is worked out once and serves as the next
+        // position's predecessor
+        bool ok_prev = true;
+        int64_t prev = p0 > 0 ? flat_tile(before, C, per_camera, tile_bits, &ok_prev) : -1;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t i = p0 + u;
             if (i > n) break;
-            range_step(i, n, u == 0 ? before : k[u - 1], k[u], C, per_camera, tile_bits,
-                       offsets, d_status);
+            bool ok_cur = true;
+            const int64_t cur = i < n ? flat_tile(k[u], C, per_camera, tile_bits, &ok_cur) : ntiles;
+            range_step(i, cur, ok_cur, prev, ok_prev, ntiles, offsets, d_status);
+            prev = cur;
+            ok_prev = ok_cur;
         }
     }
 }
@@ -401,8 +408,9 @@ void launch_isect_count(const float* means2d, const float* radii, int elliptical
                         unsigned long long* total, cudaStream_t s) {
     if (CN <= 0) return;
     k_isect_count<<<grid_for(CN, 4), kThreads, 0, s>>>(means2d, radii, elliptical, CN,
-                                                       (float)tile_size, tile_width, tile_height,
-                                                       tiles_per_gauss, total);
+                                                       (float)tile_size,
+                                                       exact_tile_inverse(tile_size), tile_width,
+                                                       tile_height, tiles_per_gauss, total);
 }
 
 void launch_publish_total(const unsigned long long* total, unsigned long long* host_word,
@@ -415,8 +423,9 @@ void launch_rect_hist(const float* means2d, const float* radii, int elliptical,
                       int tile_height, int4* rects, uint32_t* hist, cudaStream_t s) {
     if (CN <= 0) return;
     k_rect_hist<<<grid_for(CN, 4), kThreads, 0, s>>>(means2d, radii, elliptical, dbits, CN,
-                                                     (float)tile_size, tile_width, tile_height,
-                                                     rects, hist);
+                                                     (float)tile_size,
+                                                     exact_tile_inverse(tile_size), tile_width,
+                                                     tile_height, rects, hist);
 }
 
 void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
@@ -430,12 +439,14 @@ void launch_isect_emit(const float* means2d, const float* radii, int elliptical,
     const ErrorSink err{abort_flag, d_status};
     if (keys)
         k_isect_emit<true><<<(unsigned)chunks, kThreads, 0, s>>>(
-            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size, tile_width,
+            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size,
+            exact_tile_inverse(tile_size), tile_width,
             tile_height, N, tile_bits, keys, nullptr, ids, capacity, tiles_per_gauss, lb.words,
             lb.ticket, up_hist, up_passes, err);
     else
         k_isect_emit<false><<<(unsigned)chunks, kThreads, 0, s>>>(
-            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size, tile_width,
+            means2d, radii, elliptical, depths, rects, order, CN, (float)tile_size,
+            exact_tile_inverse(tile_size), tile_width,
             tile_height, N, tile_bits, nullptr, keys32, ids, capacity, tiles_per_gauss,
             lb.words, lb.ticket, up_hist, up_passes, err);
 }
