@@ -231,3 +231,21 @@ def test_tile_offsets_errors_inside_long_lists(pos):
         st = gs.new_status(DEV)
         gs.gs_tile_offsets(keys, C, TW, TH, d_status=st)
         assert int(st.item()) == code, (code, pos)
+
+
+@pytest.mark.parametrize("ts", [1, 8, 10, 13, 32])
+def test_tile_sizes_power_of_two_and_not(ts):
+    # the bounds divide by the tile size; for powers of two the kernels
+    # multiply by the exact reciprocal instead (the same correctly rounded
+    # value), for other sizes they divide: both bit-exact to the oracle's
+    # float division, including means +- radii on exact tile edges and
+    # quarter-pixel offsets
+    s = scenes.random_small(40 + ts, C=2, N=5000, W=203, H=117, tile_size=ts,
+                            sigma=(0.3, 9.0))
+    rng = np.random.default_rng(ts)
+    edge = rng.integers(0, 2 * s.N, 500)
+    m = s.means2d.reshape(-1, 2)
+    r = s.radii.reshape(-1, 2)
+    m[edge % s.N] = (rng.integers(0, 12, (500, 2)) * ts + r[edge % s.N]).astype(np.float32)
+    m[edge[:250] % s.N] += np.float32(0.25)
+    _check_isect(s)
