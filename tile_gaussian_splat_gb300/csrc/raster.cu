@@ -20,14 +20,18 @@
 // pixels have stopped; the block ends once every pixel has stopped.
 //
 // Backward (gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel): the
-// list is walked from the tile's largest last_id down to its start.  For
-// each entry every thread evaluates alpha for its 4 pixels; the valid
-// (pixel, entry) pairs of the warp are then packed onto consecutive lanes,
-// which run the gradient recurrence for them with the per-pixel state
-// (T, T_after, rem, upstream gradients) kept in shared memory.  Each lane's
-// terms for the entry go to a per-warp shared buffer; every 4 entries the
-// warp sums the buffer column-wise (one lane per (entry, field)) and adds
-// the sums to the gradients with one atomic each.
+// list is walked back to front from the largest last_id.  Without a trace,
+// the block stages batches as above and every thread evaluates alpha for its
+// 4 pixels; with the forward's trace, each warp walks the list on its own
+// (from its own pixels' largest last_id), reads its trace words of 32
+// entries at a time and stages only the entries it composited, in a buffer
+// of its own, so the tile's two warps never wait for each other.  For each
+// entry the valid (pixel, entry) pairs of the warp are packed onto
+// consecutive lanes, which run the gradient recurrence for them with the
+// per-pixel state (T, Q, upstream gradients) kept in shared memory.  Each
+// lane's terms for the entry go to a per-warp shared buffer; every
+// 32 / fields entries the warp sums the buffer column-wise (one lane per
+// (entry, field)) and adds the sums to the gradients with one atomic each.
 #include <cstdint>
 #include <type_traits>
 
@@ -722,6 +726,14 @@ struct BwdWarpSmem {
     int32_t red_gid[kRed];
 };
 
+// One warp's staged entries (trace-driven backward).
+struct BwdStage {
+    float4 mo[kWarp];   // mx, my, opacity, list position (int bits)
+    float4 q[kWarp];    // a, b, c, flatten id (int bits)
+    float4 col[kWarp];  // up to 4 channels of the launch's chunk
+    uint4 tr[kWarp];    // the warp's trace words
+};
+
 // A lane's share of every flush: field f of buffered entry e, where
 // (e, f) = (lane / F, lane mod F) never changes, so the gradient array, its
 // stride per splat and the shared-memory row are worked out once per thread.
@@ -804,7 +816,8 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     using G = GradLayout<CH>;
     constexpr int F = CH + (ABS ? 8 : 6);
     constexpr int kBatch = kBatchBwd;
-    __shared__ StageSmem<kBatch, TRACE, false> st;
+    __shared__ StageSmem<kBatch, false, false> st;
+    __shared__ BwdStage wst[TRACE ? kWarps : 1];
     __shared__ BwdWarpSmem<CH, F> ws[kWarps];
     __shared__ float s_bg[kWarps][4];
     __shared__ int s_jmax;
@@ -876,118 +889,175 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     }
     if (tr.masked || tr.start == tr.end) return;
     const int warp_max = __reduce_max_sync(0xffffffffu, my_max);
-    if (lane == 0) atomicMax(&s_jmax, warp_max);
-    __syncthreads();
-    const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
     const unsigned lt = lanemask_lt();
     const int x_tile = tr.tx * kTile;
     const int y_tile = tr.ty * kTile;
     const FlushTask task = flush_task<CH, F>(w, a, gr, lane);
     int nslots = 0;
-    for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
-        const int64_t b0 = max(tr.start, b1 - kBatch);
-        stage_batch<true, TRACE, kBatch, CH>(a, box, b0, b1, trace, st);
-        const int nw = st.nw[warp];
-        for (int ii = 0; ii < nw; ++ii) {
-            const int i = st.idx[warp][ii];
-            const float4 mo = st.mo[i];  // mx, my, opacity, list position
-            const int32_t j = __float_as_int(mo.w);
-            // warp-uniform; with a trace it never holds (a composited pair
-            // has j <= its pixel's last id <= warp_max), so it is not tested
-            if (!TRACE && j > warp_max) continue;
-            const float4 q = st.q[i];    // a, b, c, flatten id
-            // 1. which pixels of the warp have a valid pair with this entry
-            //    (the sync orders the previous entry's list reads first)
-            __syncwarp();
-            int count = 0;
-            if (TRACE) {
-                const uint4 m4 = st.tr[i][warp];
-                const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
+    // steps 1-3 for one staged entry (m4: the warp's trace words of it)
+    auto entry = [&](const float4 mo, const float4 q, const float4 col, const uint4 m4) {
+        const int32_t j = __float_as_int(mo.w);
+        // 1. which pixels of the warp have a valid pair with this entry
+        //    (the sync orders the previous entry's list reads first)
+        __syncwarp();
+        int count = 0;
+        if (TRACE) {
+            const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    if ((m[k] >> lane) & 1u)
-                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
-                    count += __popc(m[k]);
-                }
-            } else {
-                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+            for (int k = 0; k < kPPT; ++k) {
+                if ((m[k] >> lane) & 1u)
+                    w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                count += __popc(m[k]);
+            }
+        } else {
+            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                    // T < 1 depends on pairs still being run; the lane that
-                    // runs this pair tests it
-                    const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
-                                       e.alpha >= a.alpha_cutoff && last[k] >= j;
-                    const unsigned m = __ballot_sync(0xffffffffu, valid);
-                    if (valid) w.list[count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
-                    count += __popc(m);
+            for (int k = 0; k < kPPT; ++k) {
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                // T < 1 depends on pairs still being run; the lane that
+                // runs this pair tests it
+                const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
+                                   e.alpha >= a.alpha_cutoff && last[k] >= j;
+                const unsigned m = __ballot_sync(0xffffffffu, valid);
+                if (valid) w.list[count + __popc(m & lt)] = (int16_t)(k * kWarp + lane);
+                count += __popc(m);
+            }
+        }
+        if (count == 0) return;  // warp-uniform
+        __syncwarp();
+        // 2. the packed pairs, one per lane
+        float v[F];
+#pragma unroll
+        for (int f = 0; f < F; ++f) v[f] = 0.0f;
+        for (int L = lane; L < count; L += kWarp) {
+            const int p = w.list[L];
+            const int ol = p & 31;
+            const float4 g4 = w.g4[p];
+            const float pyv = CH < 4 ? g4.w
+                                     : (float)(y_tile + ((warp * kWarp + ol) / kTile) * kPPT +
+                                               (p >> 5)) + 0.5f;
+            const ColumnTerms ct =
+                column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
+            const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, pyv);
+            const float dx = ct.dx;
+            const float2 tq = w.tq[p];
+            const float Tc = tq.x, Q = tq.y;
+            // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
+            // cutoff and last_id >= j (from the trace, or tested while
+            // packing), so alpha is finite and, clamped, below 1; the
+            // T < 1 guard depends on the walk and is tested here.  A pair
+            // failing it adds nothing and leaves the pixel's state as it
+            // was: it runs with alpha 0 and no alpha gradient (no branch
+            // around the pair's work)
+            const bool ok = Tc < 1.0f;
+            const float al = ok ? e.alpha : 0.0f;
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
+            const float colv[4] = {col.x, col.y, col.z, col.w};
+            const float one_m = 1.0f - al;
+            const float Tb = __fdividef(Tc, one_m);
+            const float vis = Tb * al;
+            float gcol = 0.0f;  // g . color
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const float gcc = gv[c];
+                v[c] += gcc * vis;
+                gcol += gcc * colv[c];
+            }
+            const float g_alpha = Tb * (gcol - Q);
+            const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
+            v[G::kOp] += g_raw * e.resp;
+            const float g_s = -g_raw * e.raw;
+            const float gmx = g_s * (q.x * dx + q.y * e.dy);
+            const float gmy = g_s * (q.z * e.dy + q.y * dx);
+            v[G::kMx] += gmx;
+            v[G::kMy] += gmy;
+            v[G::kQa] += g_s * (0.5f * dx * dx);
+            v[G::kQb] += g_s * (dx * e.dy);
+            v[G::kQc] += g_s * (0.5f * e.dy * e.dy);
+            if (ABS) {
+                v[G::kAx] += fabsf(gmx);
+                v[G::kAy] += fabsf(gmy);
+            }
+            w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
+        }
+        // 3. this entry's terms into the warp's reduction buffer
+#pragma unroll
+        for (int f = 0; f < F; ++f) reinterpret_cast<float*>(w.red[nslots][f])[lane] = v[f];
+        if (lane == 0) w.red_gid[nslots] = __float_as_int(q.w);
+        if (++nslots == BwdWarpSmem<CH, F>::kRed) {
+            flush_reduction<CH, F>(w, nslots, task, lane);
+            nslots = 0;
+        }
+    };
+    if constexpr (TRACE) {
+        // Each warp walks the list on its own, from its own largest last id:
+        // per chunk of 32 entries every lane reads the warp's trace words of
+        // one entry, and the entries the warp composited are staged in the
+        // warp's own buffer -- no block barrier, so the tile's two warps never
+        // wait for each other.
+        BwdStage& sw = wst[warp];
+        const int64_t CN = (int64_t)a.C * a.N;
+        const int64_t wend = min(tr.end, (int64_t)warp_max + 1);
+        // the trace words and flatten id of a chunk's entry are read one
+        // chunk ahead, while the warp works through the previous chunk
+        auto fetch = [&](int64_t b1, uint4& m4, int64_t& g) {
+            const int64_t j = b1 - 1 - lane;
+            m4 = make_uint4(0u, 0u, 0u, 0u);
+            g = -1;
+            if (j >= tr.start) {
+                m4 = reinterpret_cast<const uint4*>(trace + j * kTraceWords)[warp];
+                if ((m4.x | m4.y | m4.z | m4.w) != 0u) {
+                    g = a.flatten_ids[j];
+                    if ((uint64_t)g >= (uint64_t)CN) {
+                        GS_BOUNDS_REPORT(a.d_status);
+                        g = -1;
+                    }
                 }
             }
-            if (count == 0) continue;  // warp-uniform
-            __syncwarp();
-            // 2. the packed pairs, one per lane
-            float v[F];
-#pragma unroll
-            for (int f = 0; f < F; ++f) v[f] = 0.0f;
-            const float4 col = st.col[i];
-            for (int L = lane; L < count; L += kWarp) {
-                const int p = w.list[L];
-                const int ol = p & 31;
-                const float4 g4 = w.g4[p];
-                const float pyv = CH < 4 ? g4.w
-                                         : (float)(y_tile + ((warp * kWarp + ol) / kTile) * kPPT +
-                                                   (p >> 5)) + 0.5f;
-                const ColumnTerms ct =
-                    column_terms(mo.x, q.x, q.y, (float)(x_tile + (ol & (kTile - 1))) + 0.5f);
-                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, pyv);
-                const float dx = ct.dx;
-                const float2 tq = w.tq[p];
-                const float Tc = tq.x, Q = tq.y;
-                // the packed pairs satisfy render_alpha > 0, s >= 0, alpha >=
-                // cutoff and last_id >= j (from the trace, or tested while
-                // packing), so alpha is finite and, clamped, below 1; the
-                // T < 1 guard depends on the walk and is tested here.  A pair
-                // failing it adds nothing and leaves the pixel's state as it
-                // was: it runs with alpha 0 and no alpha gradient (no branch
-                // around the pair's work)
-                const bool ok = Tc < 1.0f;
-                const float al = ok ? e.alpha : 0.0f;
-                const float gv[4] = {g4.x, g4.y, g4.z, g4.w};
-                const float colv[4] = {col.x, col.y, col.z, col.w};
-                const float one_m = 1.0f - al;
-                const float Tb = __fdividef(Tc, one_m);
-                const float vis = Tb * al;
-                float gcol = 0.0f;  // g . color
-#pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    const float gcc = gv[c];
-                    v[c] += gcc * vis;
-                    gcol += gcc * colv[c];
-                }
-                const float g_alpha = Tb * (gcol - Q);
-                const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
-                v[G::kOp] += g_raw * e.resp;
-                const float g_s = -g_raw * e.raw;
-                const float gmx = g_s * (q.x * dx + q.y * e.dy);
-                const float gmy = g_s * (q.z * e.dy + q.y * dx);
-                v[G::kMx] += gmx;
-                v[G::kMy] += gmy;
-                v[G::kQa] += g_s * (0.5f * dx * dx);
-                v[G::kQb] += g_s * (dx * e.dy);
-                v[G::kQc] += g_s * (0.5f * e.dy * e.dy);
-                if (ABS) {
-                    v[G::kAx] += fabsf(gmx);
-                    v[G::kAy] += fabsf(gmy);
-                }
-                w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
+        };
+        uint4 m4n;
+        int64_t gn;
+        fetch(wend, m4n, gn);
+        for (int64_t b1 = wend; b1 > tr.start; b1 -= kWarp) {
+            const int64_t j = b1 - 1 - lane;
+            const uint4 m4 = m4n;
+            const int64_t g = gn;
+            const unsigned ball = __ballot_sync(0xffffffffu, g >= 0);
+            if (ball == 0u) {
+                fetch(b1 - kWarp, m4n, gn);
+                continue;
             }
-            // 3. this entry's terms into the warp's reduction buffer
-#pragma unroll
-            for (int f = 0; f < F; ++f) reinterpret_cast<float*>(w.red[nslots][f])[lane] = v[f];
-            if (lane == 0) w.red_gid[nslots] = __float_as_int(q.w);
-            if (++nslots == BwdWarpSmem<CH, F>::kRed) {
-                flush_reduction<CH, F>(w, nslots, task, lane);
-                nslots = 0;
+            __syncwarp();  // the previous chunk's reads of the buffer are done
+            if (g >= 0) {
+                const int pos = __popc(ball & lt);
+                const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
+                const float* qq = a.conics + 3 * g;
+                const float* cc = a.colors + g * a.channels + a.ch_off;
+                sw.mo[pos] = make_float4(m.x, m.y, a.opacities[g], __int_as_float((int32_t)j));
+                sw.q[pos] = make_float4(qq[0], qq[1], qq[2], __int_as_float((int32_t)g));
+                sw.col[pos] = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
+                                          CH > 3 ? cc[3] : 0.0f);
+                sw.tr[pos] = m4;
+            }
+            fetch(b1 - kWarp, m4n, gn);
+            __syncwarp();
+            const int n = __popc(ball);
+            for (int i = 0; i < n; ++i) entry(sw.mo[i], sw.q[i], sw.col[i], sw.tr[i]);
+        }
+    } else {
+        if (lane == 0) atomicMax(&s_jmax, warp_max);
+        __syncthreads();
+        const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
+        for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
+            const int64_t b0 = max(tr.start, b1 - kBatch);
+            stage_batch<true, false, kBatch, CH>(a, box, b0, b1, trace, st);
+            const int nw = st.nw[warp];
+            for (int ii = 0; ii < nw; ++ii) {
+                const int i = st.idx[warp][ii];
+                const float4 mo = st.mo[i];
+                // warp-uniform
+                if (__float_as_int(mo.w) > warp_max) continue;
+                entry(mo, st.q[i], st.col[i], make_uint4(0u, 0u, 0u, 0u));
             }
         }
     }
