@@ -273,8 +273,9 @@ int gs_rasterize_bwd_bins(const float* means2d, const float* conics,
  *   are skipped unevaluated and not counted).
  *   trace uint32 (n_isects, 8) or NULL, 16-byte aligned: per list entry, a
  *   256-bit mask of the tile's pixels that composited it (the forward's
- *   decisions, for gs_rasterize_bwd).  Words of entries past the point where
- *   every pixel of the tile had stopped are not written.  Bit layout: word
+ *   decisions, for gs_rasterize_bwd).  Words 4h .. 4h + 3 (tile rows
+ *   8h .. 8h + 7) of entries past the point where every pixel of those rows
+ *   had stopped are not written.  Bit layout: word
  *   w (0..7), bit l covers tile pixel column (32 (w / 4) + l) % 16, row
  *   4 ((32 (w / 4) + l) / 16) + w % 4.
  * Supported: 1 <= channels <= GS_MAX_CHANNELS, tile_size == 16;

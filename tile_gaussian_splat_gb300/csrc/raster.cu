@@ -2,36 +2,36 @@
 // 16x16 tile, 4 pixels per thread in a vertical strip (thread t owns column
 // t % 16 and rows 4 (t / 16) .. 4 (t / 16) + 3 of the tile).
 //
-// Shared by both kernels:
-//  * The tile's sorted list is staged through shared memory in batches of 128
-//    records gathered through flatten_ids.  While staging, an entry whose
-//    splat cannot reach the alpha cutoff at any pixel centre of the tile is
-//    dropped (exact minimum of the quadratic form over the tile's
-//    pixel-centre rectangle, with a margin that covers the rounding of the
-//    per-pixel evaluation and of exp); such an entry is skipped by every
-//    pixel anyway, so results are unchanged.
-//  * A record read from shared memory serves the thread's 4 pixels, and the
-//    dx-only terms of the quadratic form (a dx dx, b dx) are computed once
-//    per entry in the per-pixel formula's own rounding order.
+// Each warp of a tile's block walks the tile's list on its own, 32 entries
+// at a time, with no block barrier, so the tile's two warps never wait for
+// each other:
+//  * The entries are gathered through flatten_ids into a shared buffer of the
+//    warp's own.  An entry whose splat cannot reach the alpha cutoff at any
+//    pixel centre of the warp's 8 rows is dropped while gathering (exact
+//    minimum of the quadratic form over the pixel-centre rectangle, with a
+//    margin that covers the rounding of the per-pixel evaluation and of
+//    exp); such an entry is skipped by every pixel of the warp anyway, so
+//    results are unchanged.
+//  * A staged entry serves the thread's 4 pixels, and the dx-only terms of
+//    the quadratic form (a dx dx, b dx) are computed once per entry in the
+//    per-pixel formula's own rounding order.
 //  * alpha comes from the same inline code in both kernels, so the backward
 //    makes exactly the forward's skip/composite decisions.
 //
-// Forward: per-pixel state in registers; a warp skips a batch when all its
-// pixels have stopped; the block ends once every pixel has stopped.
+// Forward: front to back, per-pixel state in registers; a warp ends once all
+// its pixels have stopped.  With a trace, the warp records for every entry it
+// gathered which of its pixels composited it.
 //
-// Backward (gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel): the
-// list is walked back to front from the largest last_id.  Without a trace,
-// the block stages batches as above and every thread evaluates alpha for its
-// 4 pixels; with the forward's trace, each warp walks the list on its own
-// (from its own pixels' largest last_id), reads its trace words of 32
-// entries at a time and stages only the entries it composited, in a buffer
-// of its own, so the tile's two warps never wait for each other.  For each
-// entry the valid (pixel, entry) pairs of the warp are packed onto
-// consecutive lanes, which run the gradient recurrence for them with the
-// per-pixel state (T, Q, upstream gradients) kept in shared memory.  Each
-// lane's terms for the entry go to a per-warp shared buffer; every
-// 32 / fields entries the warp sums the buffer column-wise (one lane per
-// (entry, field)) and adds the sums to the gradients with one atomic each.
+// Backward (gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel): back
+// to front, each warp from its own pixels' largest last_id.  With the
+// forward's trace only the entries the warp composited are staged; without,
+// every thread re-evaluates alpha for its 4 pixels.  For each entry the
+// valid (pixel, entry) pairs of the warp are packed onto consecutive lanes,
+// which run the gradient recurrence for them with the per-pixel state (T, Q,
+// upstream gradients) kept in shared memory.  Each lane's terms for the
+// entry go to a per-warp shared buffer; every 32 / fields entries the warp
+// sums the buffer column-wise (one lane per (entry, field)) and adds the
+// sums to the gradients with one atomic each.
 #include <cstdint>
 #include <type_traits>
 
@@ -54,8 +54,6 @@ constexpr int kTile = 16;
 constexpr int kPPT = 4;                          // pixels per thread
 constexpr int kThreads = kTile * kTile / kPPT;   // 64
 constexpr int kWarps = kThreads / kWarp;         // 2
-constexpr int kBatchFwd = 2 * kThreads;          // records staged per batch (forward)
-constexpr int kBatchBwd = kThreads;              // records staged per batch (backward)
 constexpr int kWarpPix = kWarp * kPPT;           // pixels per warp (128)
 constexpr float kAlphaClamp = 0.99f;
 
@@ -274,147 +272,6 @@ __device__ __forceinline__ bool cannot_reach(const TileBox& t, float mx, float m
 constexpr int kTraceWords = kWarps * kPPT;  // 8 -> 256 pixels
 static_assert(kPPT == 4, "a warp's trace words of one entry are one uint4");
 
-template <int BATCH, bool TRACE_IN, bool FAST>
-struct StageSmem {
-    static constexpr int kPerThread = BATCH / kThreads;  // candidates per thread
-    float4 mo[BATCH];   // mx, my, opacity, list position (int bits)
-    float4 q[BATCH];    // a, b, c, backward: flatten id (int bits)
-    float4 qf[FAST ? BATCH : 1];  // forward: a/2, b, c/2, fast form (0 no, 1 yes,
-                                  // 2 yes without clamp)
-    float4 col[BATCH];  // up to 4 channels of the launch's chunk
-    uint4 tr[TRACE_IN ? BATCH : 1][kWarps];  // trace words (backward with a trace)
-    uint8_t idx[kWarps][BATCH];  // per warp: staged slots that can reach its pixels
-    int32_t nw[kWarps];          // per warp: length of idx
-    int32_t cnt[1 + kWarps][kPerThread * kWarps];
-};
-
-// Stages the entries [lo, hi) of the tile's list that can reach the cutoff
-// at some pixel of the tile, in processing order (ascending positions, or
-// descending when REVERSE), packed from slot 0; with TRACE_IN also their
-// trace words.  For each warp, st.idx[w][0 .. st.nw[w]) lists (in the same
-// order) the staged slots whose splat can reach one of that warp's pixels --
-// with TRACE_IN, exactly those some pixel of the warp composited.
-// Returns how many were staged.  Contains two __syncthreads.  A flatten id
-// outside [0, C*N) (only from corrupted input) is dropped.
-template <bool REVERSE, bool TRACE_IN, int BATCH, int CH>
-__device__ __forceinline__ int stage_batch(const RasterArgs& a, const TileBox (&box)[kWarps],
-                                           int64_t lo, int64_t hi,
-                                           const uint32_t* __restrict__ trace,
-                                           StageSmem<BATCH, TRACE_IN, !REVERSE>& st) {
-    constexpr int kPerThread = StageSmem<BATCH, TRACE_IN, !REVERSE>::kPerThread;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = (int)(hi - lo);
-    const int64_t CN = (int64_t)a.C * a.N;
-    float4 mo[kPerThread], q[kPerThread];
-    int32_t gid[kPerThread];
-    int64_t jj[kPerThread];
-    uint4 tw[TRACE_IN ? kPerThread : 1][kWarps];
-    unsigned ball[kPerThread][1 + kWarps];
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-        const int i = r * kThreads + tid;
-        bool reach[kWarps];
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) reach[w] = false;
-        if (i < n) {
-            jj[r] = REVERSE ? hi - 1 - i : lo + i;
-            const int64_t g = a.flatten_ids[jj[r]];
-            const bool valid_id = (uint64_t)g < (uint64_t)CN;
-            if (!valid_id) GS_BOUNDS_REPORT(a.d_status);
-            bool any = valid_id;
-            if (TRACE_IN && valid_id) {
-                // the forward's masks say exactly which warps composited it;
-                // an entry none of them composited needs no splat data
-                const uint4* t = reinterpret_cast<const uint4*>(trace + jj[r] * kTraceWords);
-                any = false;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    tw[r][w] = t[w];
-                    reach[w] = (tw[r][w].x | tw[r][w].y | tw[r][w].z | tw[r][w].w) != 0u;
-                    any |= reach[w];
-                }
-            }
-            if (any) {
-                const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
-                const float* qq = a.conics + 3 * g;
-                mo[r] = make_float4(m.x, m.y, a.opacities[g], 0.0f);
-                q[r] = make_float4(qq[0], qq[1], qq[2], 0.0f);
-                gid[r] = (int32_t)g;
-                if (!TRACE_IN) {
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w)
-                        reach[w] =
-                            !cannot_reach(box[w], m.x, m.y, q[r].x, q[r].y, q[r].z, mo[r].z);
-                }
-            }
-        }
-        bool keep = false;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) keep |= reach[w];
-        ball[r][0] = __ballot_sync(0xffffffffu, keep);
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) ball[r][1 + w] = __ballot_sync(0xffffffffu, reach[w]);
-        if (lane == 0)
-#pragma unroll
-            for (int l = 0; l <= kWarps; ++l) st.cnt[l][r * kWarps + warp] = __popc(ball[r][l]);
-    }
-    __syncthreads();
-    int total[1 + kWarps];
-#pragma unroll
-    for (int l = 0; l <= kWarps; ++l) {
-        total[l] = 0;
-#pragma unroll
-        for (int k = 0; k < kPerThread * kWarps; ++k) total[l] += st.cnt[l][k];
-    }
-    const unsigned lt = lanemask_lt();
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-        int base[1 + kWarps];
-#pragma unroll
-        for (int l = 0; l <= kWarps; ++l) {
-            base[l] = 0;
-            for (int k = 0; k < r * kWarps + warp; ++k) base[l] += st.cnt[l][k];
-        }
-        if ((ball[r][0] >> lane) & 1u) {
-            const int pos = base[0] + __popc(ball[r][0] & lt);
-            const float* cc = a.colors + (int64_t)gid[r] * a.channels + a.ch_off;
-            const float4 col = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
-                                           CH > 3 ? cc[3] : 0.0f);
-            float4 f;
-            bool fast = fast_terms(mo[r].x, mo[r].y, q[r].x, q[r].y, q[r].z, mo[r].z, f);
-            fast = fast && fabsf(col.x) < 3.0e38f && fabsf(col.y) < 3.0e38f &&
-                   fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
-            // 2: fast form, and o <= 0.98 so o exp(-s) (s >= 0) never reaches the
-            // 0.99 clamp, whatever the exponential's 2^-22 rounding
-            if (!REVERSE) {
-                st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
-                                         __int_as_float((int32_t)jj[r]));
-                st.q[pos] = q[r];
-                f.w = fast ? (mo[r].z <= 0.98f ? 2.0f : 1.0f) : 0.0f;
-                st.qf[pos] = f;
-            } else {
-                st.mo[pos] = make_float4(mo[r].x, mo[r].y, mo[r].z,
-                                         __int_as_float((int32_t)jj[r]));
-                st.q[pos] = make_float4(q[r].x, q[r].y, q[r].z, __int_as_float(gid[r]));
-            }
-            st.col[pos] = col;
-            if (TRACE_IN) {
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) st.tr[pos][w] = tw[r][w];
-            }
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w)
-                if ((ball[r][1 + w] >> lane) & 1u)
-                    st.idx[w][base[1 + w] + __popc(ball[r][1 + w] & lt)] = (uint8_t)pos;
-        }
-    }
-    if (tid == 0)
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) st.nw[w] = total[1 + w];
-    __syncthreads();
-    return total[0];
-}
-
 struct PixelSlot {
     int x, y0;  // column and first row of the thread's strip
 };
@@ -441,6 +298,15 @@ struct StepTrace {
     int32_t* count;
     int max_steps;
     int64_t npix;
+};
+
+// One warp's staged entries (forward).
+struct FwdStage {
+    float4 mo[kWarp];   // mx, my, opacity, list position (int bits)
+    float4 q[kWarp];    // a, b, c
+    float4 qf[kWarp];   // a/2, b, c/2, fast form (0 no, 1 yes, 2 yes without clamp)
+    float4 col[kWarp];  // up to 4 channels of the launch's chunk
+    uint4 tr[kWarp];    // the warp's trace words
 };
 
 // *dst = v by lane 0 only, as one predicated store (written as a branch
@@ -472,16 +338,11 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
     k_raster_fwd(RasterArgs a, float* __restrict__ out_rgb, float* __restrict__ out_alpha,
                  int32_t* __restrict__ out_last, int32_t* __restrict__ out_counts,
                  uint32_t* __restrict__ trace, StepTrace stp = StepTrace{}) {
-    constexpr int kBatch = kBatchFwd;
     constexpr int kPairs = kPPT / 2;
-    __shared__ StageSmem<kBatch, false, true> st;
-    __shared__ __align__(16) uint32_t s_trace[TRACE ? kBatch : 1][kTraceWords];
+    __shared__ FwdStage fst[kWarps];
     const TileRange tr = tile_range(a);
-    TileBox box[kWarps];
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) box[w] = warp_box(a, tr, w);
     const PixelSlot ps = pixel_slot(tr);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float px = (float)ps.x + 0.5f;
     float2 T[kPairs], acc[kPairs][4], npy[kPairs];
     float py[kPPT];
@@ -495,16 +356,6 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
     // step trace: records written per pixel, and the pixel's index
     int32_t n_rec[STEPS ? kPPT : 1];
     int64_t pix[STEPS ? kPPT : 1];
-    auto record = [&](int k, int32_t j, float t_before) {
-        if (STEPS) {
-            if (n_rec[k] < stp.max_steps) {
-                const int64_t o = (int64_t)n_rec[k] * stp.npix + pix[k];
-                stp.pos[o] = j;
-                stp.T[o] = t_before;
-            }
-            ++n_rec[k];
-        }
-    };
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
         last[k] = -1;
@@ -518,6 +369,16 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
         if (COUNT) done_c[k] = outside;
         py[k] = (float)(ps.y0 + k) + 0.5f;
     }
+    auto record = [&](int k, int32_t j, float t_before) {
+        if (STEPS) {
+            if (n_rec[k] < stp.max_steps) {
+                const int64_t o = (int64_t)n_rec[k] * stp.npix + pix[k];
+                stp.pos[o] = j;
+                stp.T[o] = t_before;
+            }
+            ++n_rec[k];
+        }
+    };
     auto stopped = [&](int k) { return COUNT ? done_c[k] : cut[k] == INFINITY; };
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) {
@@ -527,24 +388,69 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
         npy[p] = make_float2(-py[2 * p], -py[2 * p + 1]);
     }
     const float2 one = splat2(1.0f), minus_one = splat2(-1.0f);
-    for (int64_t b0 = tr.start; b0 < tr.end; b0 += kBatch) {
+    // Each warp walks the tile's list on its own, 32 entries at a time: lane
+    // l gathers entry b0 + l and tests it against the warp's own pixel box;
+    // the entries that can reach one of the warp's pixels are staged, in
+    // order, in the warp's own buffer.  No block barrier: a warp whose
+    // pixels have all stopped ends without waiting for the other.
+    FwdStage& sw = fst[warp];
+    const TileBox wb = warp_box(a, tr, warp);
+    const int64_t CN = (int64_t)a.C * a.N;
+    const unsigned lt = lanemask_lt();
+    for (int64_t b0 = tr.start; b0 < tr.end; b0 += kWarp) {
         bool all_done = true;
 #pragma unroll
         for (int k = 0; k < kPPT; ++k) all_done &= stopped(k);
-        if (__syncthreads_count(all_done) == kThreads) break;
-        const int n_raw = (int)min((int64_t)kBatch, tr.end - b0);
+        if (__all_sync(0xffffffffu, all_done)) break;
+        const int n_raw = (int)min((int64_t)kWarp, tr.end - b0);
         const int32_t b0_32 = (int32_t)b0;  // list positions are below 2^31
-        if (TRACE)
-            for (int i = tid; i < kBatch * kTraceWords; i += kThreads) (&s_trace[0][0])[i] = 0u;
-        stage_batch<false, false, kBatch, CH>(a, box, b0, b0 + n_raw, nullptr, st);
-        if (!__all_sync(0xffffffffu, all_done)) {
-            const int nw = st.nw[warp];
-            for (int ii = 0; ii < nw; ++ii) {
-                const int i = st.idx[warp][ii];
-                const float4 mo = st.mo[i];
+        const int64_t jl = b0 + lane;
+        bool reach = false;
+        float2 m = make_float2(0.0f, 0.0f);
+        float op = 0.0f, qa = 0.0f, qb = 0.0f, qc = 0.0f;
+        int64_t g = 0;
+        if (lane < n_raw) {
+            g = a.flatten_ids[jl];
+            if ((uint64_t)g < (uint64_t)CN) {
+                m = reinterpret_cast<const float2*>(a.means2d)[g];
+                const float* qq = a.conics + 3 * g;
+                qa = qq[0];
+                qb = qq[1];
+                qc = qq[2];
+                op = a.opacities[g];
+                reach = !cannot_reach(wb, m.x, m.y, qa, qb, qc, op);
+            } else {
+                GS_BOUNDS_REPORT(a.d_status);
+            }
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, reach);
+        __syncwarp();  // the previous chunk's reads of the buffer are done
+        if (TRACE) sw.tr[lane] = make_uint4(0u, 0u, 0u, 0u);
+        if (reach) {
+            const int pos = __popc(ball & lt);
+            const float* cc = a.colors + g * a.channels + a.ch_off;
+            const float4 col = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
+                                           CH > 3 ? cc[3] : 0.0f);
+            float4 f;
+            bool fast = fast_terms(m.x, m.y, qa, qb, qc, op, f);
+            fast = fast && fabsf(col.x) < 3.0e38f && fabsf(col.y) < 3.0e38f &&
+                   fabsf(col.z) < 3.0e38f && fabsf(col.w) < 3.0e38f;
+            // 2: fast form, and o <= 0.98 so o exp(-s) (s >= 0) never reaches
+            // the 0.99 clamp, whatever the exponential's 2^-22 rounding
+            f.w = fast ? (op <= 0.98f ? 2.0f : 1.0f) : 0.0f;
+            sw.mo[pos] = make_float4(m.x, m.y, op, __int_as_float((int32_t)jl));
+            sw.q[pos] = make_float4(qa, qb, qc, 0.0f);
+            sw.qf[pos] = f;
+            sw.col[pos] = col;
+        }
+        __syncwarp();
+        {
+            const int nw = __popc(ball);
+            for (int i = 0; i < nw; ++i) {
+                const float4 mo = sw.mo[i];
                 const int32_t j = __float_as_int(mo.w);
-                const float4 h = st.qf[i];  // a/2, b, c/2, fast-form flag
-                const float4 col = st.col[i];
+                const float4 h = sw.qf[i];  // a/2, b, c/2, fast-form flag
+                const float4 col = sw.col[i];
                 const float colv[4] = {col.x, col.y, col.z, col.w};
                 bool took[kPPT];
                 // fast form (warp-uniform): branch-free compositing
@@ -604,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
                 } else if (h.w != 0.0f) {
                     fast_pairs(std::integral_constant<bool, true>{});
                 } else {  // exact-order form, with the s >= 0 test
-                    const float4 q = st.q[i];
+                    const float4 q = sw.q[i];
                     const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
                     float alpha[kPPT];
 #pragma unroll
@@ -643,10 +549,10 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
                                                 __ballot_sync(0xffffffffu, took[1]),
                                                 __ballot_sync(0xffffffffu, took[2]),
                                                 __ballot_sync(0xffffffffu, took[3]));
-                    st_shared_lane0(&s_trace[j - b0_32][warp * kPPT], m4, lane);
+                    st_shared_lane0(&sw.tr[j - b0_32].x, m4, lane);
                 }
-                // leave the batch early once every pixel of the warp has stopped
-                if ((ii & 15) == 15) {
+                // leave the chunk early once every pixel of the warp has stopped
+                if ((i & 15) == 15) {
                     bool d = true;
 #pragma unroll
                     for (int k = 0; k < kPPT; ++k) d &= stopped(k);
@@ -655,10 +561,9 @@ __global__ void __launch_bounds__(kThreads, COUNT || STEPS ? 12 : GS_FWD_MIN_BLO
             }
         }
         if (TRACE) {
-            __syncthreads();
-            uint4* dst = reinterpret_cast<uint4*>(trace + b0 * kTraceWords);
-            const uint4* src = reinterpret_cast<const uint4*>(&s_trace[0][0]);
-            for (int i = tid; i < n_raw * (kTraceWords / 4); i += kThreads) dst[i] = src[i];
+            __syncwarp();
+            if (lane < n_raw)
+                reinterpret_cast<uint4*>(trace + jl * kTraceWords)[warp] = sw.tr[lane];
         }
     }
     float bg[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -733,6 +638,86 @@ struct BwdStage {
     float4 col[kWarp];  // up to 4 channels of the launch's chunk
     uint4 tr[kWarp];    // the warp's trace words
 };
+
+// One warp's walk of its tile's list from position wend - 1 down to the
+// tile's start, 32 entries at a time (lane l takes entry b1 - 1 - l).  An
+// entry is staged -- in walk order, in the warp's own buffer -- when the
+// warp has work with it: with the forward's trace, when the warp's trace
+// words of it are not all zero; without, when its splat can reach one of
+// the warp's pixels.  The flatten id (and the trace words) of a chunk's
+// entry are read one chunk ahead, while the warp works through the current
+// chunk.  entry(mo, q, col, m4) then runs on the whole warp for each staged
+// entry in order: mo = (mx, my, opacity, list position), q = (a, b, c,
+// flatten id), col = the chunk's up to 4 colour channels (none when CH is
+// 0), m4 = the warp's trace words.  A flatten id outside [0, C*N) (only from
+// corrupted input) is reported and the entry dropped.
+template <int CH, bool TRACE, typename Entry>
+__device__ __forceinline__ void walk_back(const RasterArgs& a, const TileRange& tr,
+                                          const TileBox& wb, const uint32_t* __restrict__ trace,
+                                          int64_t wend, BwdStage& sw, Entry&& entry) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = lanemask_lt();
+    const int64_t CN = (int64_t)a.C * a.N;
+    auto fetch = [&](int64_t b1, uint4& m4, int64_t& g) {
+        const int64_t j = b1 - 1 - lane;
+        m4 = make_uint4(0u, 0u, 0u, 0u);
+        g = -1;
+        if (j >= tr.start) {
+            bool want = true;
+            if (TRACE) {
+                m4 = reinterpret_cast<const uint4*>(trace + j * kTraceWords)[warp];
+                want = (m4.x | m4.y | m4.z | m4.w) != 0u;
+            }
+            if (want) {
+                g = a.flatten_ids[j];
+                if ((uint64_t)g >= (uint64_t)CN) {
+                    GS_BOUNDS_REPORT(a.d_status);
+                    g = -1;
+                }
+            }
+        }
+    };
+    uint4 m4n;
+    int64_t gn;
+    fetch(wend, m4n, gn);
+    for (int64_t b1 = wend; b1 > tr.start; b1 -= kWarp) {
+        const int64_t j = b1 - 1 - lane;
+        const uint4 m4 = m4n;
+        const int64_t g = gn;
+        bool take = g >= 0;
+        float4 mo = make_float4(0.0f, 0.0f, 0.0f, 0.0f), q = mo;
+        if (take) {
+            const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
+            const float* qq = a.conics + 3 * g;
+            mo = make_float4(m.x, m.y, a.opacities[g], __int_as_float((int32_t)j));
+            q = make_float4(qq[0], qq[1], qq[2], __int_as_float((int32_t)g));
+            if (!TRACE) take = !cannot_reach(wb, mo.x, mo.y, q.x, q.y, q.z, mo.z);
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, take);
+        if (ball == 0u) {
+            fetch(b1 - kWarp, m4n, gn);
+            continue;
+        }
+        __syncwarp();  // the previous chunk's reads of the buffer are done
+        if (take) {
+            const int pos = __popc(ball & lt);
+            float4 col = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (CH > 0) {
+                const float* cc = a.colors + g * a.channels + a.ch_off;
+                col = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
+                                  CH > 3 ? cc[3] : 0.0f);
+            }
+            sw.mo[pos] = mo;
+            sw.q[pos] = q;
+            sw.col[pos] = col;
+            sw.tr[pos] = m4;
+        }
+        fetch(b1 - kWarp, m4n, gn);
+        __syncwarp();
+        const int n = __popc(ball);
+        for (int i = 0; i < n; ++i) entry(sw.mo[i], sw.q[i], sw.col[i], sw.tr[i]);
+    }
+}
 
 // A lane's share of every flush: field f of buffered entry e, where
 // (e, f) = (lane / F, lane mod F) never changes, so the gradient array, its
@@ -815,16 +800,10 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     k_raster_bwd(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
     using G = GradLayout<CH>;
     constexpr int F = CH + (ABS ? 8 : 6);
-    constexpr int kBatch = kBatchBwd;
-    __shared__ StageSmem<kBatch, false, false> st;
-    __shared__ BwdStage wst[TRACE ? kWarps : 1];
+    __shared__ BwdStage wst[kWarps];
     __shared__ BwdWarpSmem<CH, F> ws[kWarps];
     __shared__ float s_bg[kWarps][4];
-    __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
-    TileBox box[kWarps];
-#pragma unroll
-    for (int k = 0; k < kWarps; ++k) box[k] = warp_box(a, tr, k);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     BwdWarpSmem<CH, F>& w = ws[warp];
     const PixelSlot ps = pixel_slot(tr);
@@ -872,7 +851,6 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         w.tq[k * kWarp + lane] = make_float2(Tc, Q);
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
-    if (tid == 0) s_jmax = -1;
     if (gr.grad_backgrounds) {
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
@@ -989,78 +967,9 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
             nslots = 0;
         }
     };
-    if constexpr (TRACE) {
-        // Each warp walks the list on its own, from its own largest last id:
-        // per chunk of 32 entries every lane reads the warp's trace words of
-        // one entry, and the entries the warp composited are staged in the
-        // warp's own buffer -- no block barrier, so the tile's two warps never
-        // wait for each other.
-        BwdStage& sw = wst[warp];
-        const int64_t CN = (int64_t)a.C * a.N;
-        const int64_t wend = min(tr.end, (int64_t)warp_max + 1);
-        // the trace words and flatten id of a chunk's entry are read one
-        // chunk ahead, while the warp works through the previous chunk
-        auto fetch = [&](int64_t b1, uint4& m4, int64_t& g) {
-            const int64_t j = b1 - 1 - lane;
-            m4 = make_uint4(0u, 0u, 0u, 0u);
-            g = -1;
-            if (j >= tr.start) {
-                m4 = reinterpret_cast<const uint4*>(trace + j * kTraceWords)[warp];
-                if ((m4.x | m4.y | m4.z | m4.w) != 0u) {
-                    g = a.flatten_ids[j];
-                    if ((uint64_t)g >= (uint64_t)CN) {
-                        GS_BOUNDS_REPORT(a.d_status);
-                        g = -1;
-                    }
-                }
-            }
-        };
-        uint4 m4n;
-        int64_t gn;
-        fetch(wend, m4n, gn);
-        for (int64_t b1 = wend; b1 > tr.start; b1 -= kWarp) {
-            const int64_t j = b1 - 1 - lane;
-            const uint4 m4 = m4n;
-            const int64_t g = gn;
-            const unsigned ball = __ballot_sync(0xffffffffu, g >= 0);
-            if (ball == 0u) {
-                fetch(b1 - kWarp, m4n, gn);
-                continue;
-            }
-            __syncwarp();  // the previous chunk's reads of the buffer are done
-            if (g >= 0) {
-                const int pos = __popc(ball & lt);
-                const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
-                const float* qq = a.conics + 3 * g;
-                const float* cc = a.colors + g * a.channels + a.ch_off;
-                sw.mo[pos] = make_float4(m.x, m.y, a.opacities[g], __int_as_float((int32_t)j));
-                sw.q[pos] = make_float4(qq[0], qq[1], qq[2], __int_as_float((int32_t)g));
-                sw.col[pos] = make_float4(cc[0], CH > 1 ? cc[1] : 0.0f, CH > 2 ? cc[2] : 0.0f,
-                                          CH > 3 ? cc[3] : 0.0f);
-                sw.tr[pos] = m4;
-            }
-            fetch(b1 - kWarp, m4n, gn);
-            __syncwarp();
-            const int n = __popc(ball);
-            for (int i = 0; i < n; ++i) entry(sw.mo[i], sw.q[i], sw.col[i], sw.tr[i]);
-        }
-    } else {
-        if (lane == 0) atomicMax(&s_jmax, warp_max);
-        __syncthreads();
-        const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
-        for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
-            const int64_t b0 = max(tr.start, b1 - kBatch);
-            stage_batch<true, false, kBatch, CH>(a, box, b0, b1, trace, st);
-            const int nw = st.nw[warp];
-            for (int ii = 0; ii < nw; ++ii) {
-                const int i = st.idx[warp][ii];
-                const float4 mo = st.mo[i];
-                // warp-uniform
-                if (__float_as_int(mo.w) > warp_max) continue;
-                entry(mo, st.q[i], st.col[i], make_uint4(0u, 0u, 0u, 0u));
-            }
-        }
-    }
+    // each warp walks the list on its own, from its own pixels' largest last id
+    walk_back<CH, TRACE>(a, tr, warp_box(a, tr, warp), trace,
+                         min(tr.end, (int64_t)warp_max + 1), wst[warp], entry);
     if (nslots) flush_reduction<CH, F>(w, nslots, task, lane);
 }
 
@@ -1086,16 +995,11 @@ struct AbsWarpSmem {
 template <bool TRACE>
 __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
     k_raster_bwd_absgrad(RasterArgs a, RasterGrads gr, const uint32_t* __restrict__ trace) {
-    constexpr int kBatch = kBatchBwd;
     constexpr int kRed = AbsWarpSmem::kRed;
-    __shared__ StageSmem<kBatch, TRACE, false> st;
+    __shared__ BwdStage wst[kWarps];
     __shared__ AbsWarpSmem ws[kWarps];
-    __shared__ int s_jmax;
     const TileRange tr = tile_range(a);
-    TileBox box[kWarps];
-#pragma unroll
-    for (int k = 0; k < kWarps; ++k) box[k] = warp_box(a, tr, k);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     AbsWarpSmem& w = ws[warp];
     const PixelSlot ps = pixel_slot(tr);
     const float px = (float)ps.x + 0.5f;
@@ -1122,13 +1026,9 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         w.tq[k * kWarp + lane] = make_float2(1.0f - ra[k], Q);
         if (ra[k] > 0.0f && last[k] > my_max) my_max = last[k];
     }
-    if (tid == 0) s_jmax = -1;
-    __syncthreads();
+    __syncwarp();
     if (tr.masked || tr.start == tr.end) return;  // block-uniform
     const int warp_max = __reduce_max_sync(0xffffffffu, my_max);
-    if (lane == 0) atomicMax(&s_jmax, warp_max);
-    __syncthreads();
-    const int64_t walk_end = min(tr.end, (int64_t)s_jmax + 1);
     const unsigned lt = lanemask_lt();
     const int x_tile = tr.tx * kTile;
     const int y_tile = tr.ty * kTile;
@@ -1152,77 +1052,69 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
         __syncwarp();
     };
     int nslots = 0;
-    for (int64_t b1 = walk_end; b1 > tr.start; b1 -= kBatch) {
-        const int64_t b0 = max(tr.start, b1 - kBatch);
-        stage_batch<true, TRACE, kBatch, 1>(a, box, b0, b1, trace, st);
-        const int nw = st.nw[warp];
-        for (int ii = 0; ii < nw; ++ii) {
-            const int i = st.idx[warp][ii];
-            const float4 mo = st.mo[i];  // mx, my, opacity, list position
-            const int32_t j = __float_as_int(mo.w);
-            if (!TRACE && j > warp_max) continue;  // warp-uniform
-            const float4 q = st.q[i];            // a, b, c, flatten id
-            const int32_t gid = __float_as_int(q.w);
-            __syncwarp();
-            int count = 0;
-            if (TRACE) {
-                const uint4 m4 = st.tr[i][warp];
-                const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
+    auto entry = [&](const float4 mo, const float4 q, const float4, const uint4 m4) {
+        const int32_t j = __float_as_int(mo.w);
+        const int32_t gid = __float_as_int(q.w);
+        __syncwarp();
+        int count = 0;
+        if (TRACE) {
+            const unsigned m[kPPT] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    if ((m[k] >> lane) & 1u)
-                        w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
-                    count += __popc(m[k]);
-                }
-            } else {
-                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
+            for (int k = 0; k < kPPT; ++k) {
+                if ((m[k] >> lane) & 1u)
+                    w.list[count + __popc(m[k] & lt)] = (int16_t)(k * kWarp + lane);
+                count += __popc(m[k]);
+            }
+        } else {
+            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, px);
 #pragma unroll
-                for (int k = 0; k < kPPT; ++k) {
-                    const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
-                    const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
-                                       e.alpha >= a.alpha_cutoff && last[k] >= j;
-                    const unsigned mk = __ballot_sync(0xffffffffu, valid);
-                    if (valid) w.list[count + __popc(mk & lt)] = (int16_t)(k * kWarp + lane);
-                    count += __popc(mk);
-                }
-            }
-            if (count == 0) continue;  // warp-uniform
-            __syncwarp();
-            float va = 0.0f, vb = 0.0f;
-            const float* const col = a.colors + (int64_t)gid * nch;
-            for (int L = lane; L < count; L += kWarp) {
-                const int p = w.list[L];
-                const int ol = p & 31;
-                const int xx = x_tile + (ol & (kTile - 1));
-                const int yy = y_tile + ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
-                const ColumnTerms ct = column_terms(mo.x, q.x, q.y, (float)xx + 0.5f);
-                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)yy + 0.5f);
-                const float2 tq = w.tq[p];
-                const float Tc = tq.x, Q = tq.y;
-                const bool ok = Tc < 1.0f;  // as in the chunks' pair loop
-                const float al = ok ? e.alpha : 0.0f;
-                const float one_m = 1.0f - al;
-                const float Tb = __fdividef(Tc, one_m);
-                const float* gp =
-                    gr.grad_render_colors + (((int64_t)tr.c * a.height + yy) * a.width + xx) * nch;
-                float gcol = 0.0f;  // g . color over every channel
-                for (int c = 0; c < nch; ++c) gcol += gp[c] * col[c];
-                const float g_alpha = Tb * (gcol - Q);
-                const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
-                const float g_s = -g_raw * e.raw;
-                va += fabsf(g_s * (q.x * ct.dx + q.y * e.dy));
-                vb += fabsf(g_s * (q.z * e.dy + q.y * ct.dx));
-                w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
-            }
-            reinterpret_cast<float*>(w.red[nslots][0])[lane] = va;
-            reinterpret_cast<float*>(w.red[nslots][1])[lane] = vb;
-            if (lane == 0) w.red_gid[nslots] = gid;
-            if (++nslots == kRed) {
-                flush(nslots);
-                nslots = 0;
+            for (int k = 0; k < kPPT; ++k) {
+                const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, py[k]);
+                const bool valid = ra[k] > 0.0f && e.s >= 0.0f &&
+                                   e.alpha >= a.alpha_cutoff && last[k] >= j;
+                const unsigned mk = __ballot_sync(0xffffffffu, valid);
+                if (valid) w.list[count + __popc(mk & lt)] = (int16_t)(k * kWarp + lane);
+                count += __popc(mk);
             }
         }
-    }
+        if (count == 0) return;  // warp-uniform
+        __syncwarp();
+        float va = 0.0f, vb = 0.0f;
+        const float* const col = a.colors + (int64_t)gid * nch;
+        for (int L = lane; L < count; L += kWarp) {
+            const int p = w.list[L];
+            const int ol = p & 31;
+            const int xx = x_tile + (ol & (kTile - 1));
+            const int yy = y_tile + ((warp * kWarp + ol) / kTile) * kPPT + (p >> 5);
+            const ColumnTerms ct = column_terms(mo.x, q.x, q.y, (float)xx + 0.5f);
+            const PairEval e = eval_pair(ct, mo.y, q.z, mo.z, (float)yy + 0.5f);
+            const float2 tq = w.tq[p];
+            const float Tc = tq.x, Q = tq.y;
+            const bool ok = Tc < 1.0f;  // as in the chunks' pair loop
+            const float al = ok ? e.alpha : 0.0f;
+            const float one_m = 1.0f - al;
+            const float Tb = __fdividef(Tc, one_m);
+            const float* gp =
+                gr.grad_render_colors + (((int64_t)tr.c * a.height + yy) * a.width + xx) * nch;
+            float gcol = 0.0f;  // g . color over every channel
+            for (int c = 0; c < nch; ++c) gcol += gp[c] * col[c];
+            const float g_alpha = Tb * (gcol - Q);
+            const float g_raw = ok && e.raw < kAlphaClamp ? g_alpha : 0.0f;
+            const float g_s = -g_raw * e.raw;
+            va += fabsf(g_s * (q.x * ct.dx + q.y * e.dy));
+            vb += fabsf(g_s * (q.z * e.dy + q.y * ct.dx));
+            w.tq[p] = make_float2(Tb, al * gcol + one_m * Q);
+        }
+        reinterpret_cast<float*>(w.red[nslots][0])[lane] = va;
+        reinterpret_cast<float*>(w.red[nslots][1])[lane] = vb;
+        if (lane == 0) w.red_gid[nslots] = gid;
+        if (++nslots == kRed) {
+            flush(nslots);
+            nslots = 0;
+        }
+    };
+    walk_back<0, TRACE>(a, tr, warp_box(a, tr, warp), trace, min(tr.end, (int64_t)warp_max + 1),
+                        wst[warp], entry);
     if (nslots) flush(nslots);
 }
 
