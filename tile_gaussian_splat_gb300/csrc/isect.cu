@@ -8,12 +8,12 @@
 //                  visits splats in depth order, gathers one sector per splat)
 //                  and the histograms of the four 8-bit digits of the depth
 //                  bits for the depth sort.
-//   k_isect_emit   one thread per splat of a 256-splat chunk taken in ticket
-//                  order; a block scan of the counts plus a decoupled
+//   k_isect_emit   two splats per thread of a 512-splat chunk taken in
+//                  ticket order; a block scan of the counts plus a decoupled
 //                  look-back over earlier chunks gives each splat's first
-//                  output slot; then the block's whole run of keys is written
-//                  cooperatively (every thread finds the key's splat by a
-//                  binary search over the block's prefix sums), so stores are
+//                  output slot; then each warp writes the keys of its 64
+//                  splats 32 consecutive keys at a time (a key's splat comes
+//                  from the round's splat-start bits), so stores are
 //                  coalesced whatever the per-splat counts are.  Optionally
 //                  also histograms the 8-bit digits of the key's upper word
 //                  for the radix passes that follow.
@@ -142,6 +142,8 @@ struct EmitSmem {
     uint32_t upper[kEmitSplats];  // camera << tile_bits
     uint32_t dbits[kEmitSplats];
     int32_t sid[kEmitSplats];
+    float rw[kEmitSplats];      // 1 / rect width
+    int16_t owner[kThreads / kWarp][kWarp];  // per warp: splat slot starting at R + i
     uint32_t hist[4][256];
     int64_t scratch[32];
     int64_t base;
@@ -244,6 +246,7 @@ __global__ void __launch_bounds__(kThreads)
             sm.x0[slot] = r.x0;
             sm.y0[slot] = r.y0;
             sm.w[slot] = r.x1 - r.x0;
+            sm.rw[slot] = __frcp_rn((float)(r.x1 - r.x0));
             sm.upper[slot] = (uint32_t)((uint64_t)(s / N) << tile_bits);
             if (WIDE) sm.dbits[slot] = __float_as_uint(depths[s]);
             sm.sid[slot] = (int32_t)s;
@@ -267,26 +270,55 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     const int64_t base = sm.base;
-    const int total = (int)chunk_total;
-    const int rounds = (total + kThreads - 1) / kThreads;
-    for (int r = 0; r < rounds; ++r) {
-        const int q = r * kThreads + tid;
-        const bool valid = q < total;
+    // Each warp writes the keys of its own 64 splats (slots 64 w .. 64 w + 63,
+    // two per lane), 32 consecutive keys per round: a key's splat is the last
+    // one starting at or before it, found from the round's start bits (each
+    // splat starting in the round marks its offset and leaves its slot in
+    // the warp's table) and, before the first start, the previous round's
+    // last splat.
+    const int lane = tid & 31, warp = tid >> 5;
+    const int s_first = 2 * kWarp * warp;
+    const int wstart = s_first == 0 ? 0 : sm.incl[s_first - 1];
+    const int wend = sm.incl[s_first + 2 * kWarp - 1];
+    int start[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) start[u] = sm.incl[2 * tid + u] - cnt[u];
+    int carry = 0;
+    for (int R = wstart; R < wend; R += kWarp) {
+        unsigned mine = 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int off = start[u] - R;
+            if (cnt[u] > 0 && off >= 0 && off < kWarp) {
+                mine |= 1u << off;
+                sm.owner[warp][off] = (int16_t)(2 * tid + u);
+            }
+        }
+        const unsigned starts = __reduce_or_sync(0xffffffffu, mine);
+        __syncwarp();
+        const unsigned upto = starts & (0xffffffffu >> (31 - lane));
+        const int o = upto ? sm.owner[warp][31 - __clz(upto)] : carry;
+        carry = starts ? sm.owner[warp][31 - __clz(starts)] : carry;
+        __syncwarp();  // the table is read before the next round writes it
+        const int q = R + lane;
+        const bool valid = q < wend;
         uint32_t upper = 0;
         if (valid) {
-            // owner: first o with incl[o] > q
-            int lo = 0, hi = kEmitSplats - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (sm.incl[mid] > q) hi = mid;
-                else lo = mid + 1;
-            }
-            const int o = lo;
             const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
             const int w = sm.w[o];
-            const int dy = li / w;
+            // li / w from the reciprocal: li < 2^23, so the product is within
+            // 1 of the quotient and one step either way corrects it
+            int dy = __float2int_rz((float)li * sm.rw[o]);
+            int rem = li - dy * w;
+            if (rem < 0) {
+                --dy;
+                rem += w;
+            } else if (rem >= w) {
+                ++dy;
+                rem -= w;
+            }
             const int ty = sm.y0[o] + dy;
-            const int tx = sm.x0[o] + (li - dy * w);
+            const int tx = sm.x0[o] + rem;
             upper = sm.upper[o] | (uint32_t)(ty * tile_width + tx);
             const int64_t pos = base + q;
             if (pos < capacity) {
@@ -317,8 +349,6 @@ __device__ __forceinline__ int64_t flat_tile(uint64_t key, int C, int64_t per_ca
     return (int64_t)cam * per_camera + (int64_t)tile;
 }
 
-// Tile ids of positions i - 1 and i (position n is the end: every tile
-// after the last key starts there) -> offsets of the tiles in between.
 // Tile ids of positions i - 1 (prev) and i (cur; position n is the end:
 // every tile after the last key starts there) -> offsets of the tiles in
 // between.  ok_* say whether the key lies inside the grid.
