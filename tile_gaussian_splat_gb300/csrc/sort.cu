@@ -7,7 +7,11 @@
 // Per pass, each 256-thread block:
 //   1. takes a virtual block id from an atomic ticket (so a block only ever
 //      waits on blocks that are already running);
-//   2. loads its tile of keys warp-striped (coalesced) into registers;
+//   2. loads its tile of keys warp-striped (coalesced) into registers, and
+//      starts one bulk copy (TMA, cp.async.bulk) of the tile's values into
+//      shared memory, which is waited for only when the tile is reordered
+//      (bulk-copying the keys too measured 2 % slower: they are needed in
+//      registers at once, and the copy adds a shared-memory round trip);
 //   3. ranks each key among equal digits of its warp (bit-sliced ballots +
 //      popc), keeping input order (stability);
 //   4. publishes its 256 digit counts, then walks back over predecessors'
@@ -41,6 +45,7 @@ __host__ __device__ __forceinline__ uint32_t digit_mask(int shift, int end_bit) 
 }
 
 constexpr int kHistPasses = 4;  // digit passes per histogram launch
+constexpr int kBulkPolls = 1 << 20;  // bounded try_wait rounds for a tile's bulk copies
 
 template <typename K>
 __global__ void __launch_bounds__(kThreads) k_digit_hist(const K* __restrict__ keys, int64_t n,
@@ -82,10 +87,43 @@ __global__ void __launch_bounds__(kThreads) k_digit_hist(const K* __restrict__ k
     }
 }
 
+// How a tile of `count` elements at src splits for a bulk copy: `head`
+// elements before the first 16-byte boundary, a `body` of whole 16-byte
+// units, the rest after it; `shift` places the body on a 16-byte boundary
+// of the destination (dst[shift + j] receives src[j]).
+struct TileCopy {
+    int shift, head, body;
+};
+
+template <typename T>
+__device__ __forceinline__ TileCopy plan_copy(const T* src, int count) {
+    constexpr int kPer = 16 / (int)sizeof(T);
+    const int mis = (int)((reinterpret_cast<uintptr_t>(src) & 15u) / sizeof(T));
+    TileCopy c;
+    c.head = mis == 0 ? 0 : kPer - mis;
+    if (c.head > count) c.head = count;
+    c.body = (count - c.head) / kPer * kPer;
+    c.shift = (kPer - c.head % kPer) % kPer;
+    return c;
+}
+
+// The ends the bulk copy leaves (head and tail, under 16 bytes each), one
+// element per thread: threads 0 .. head - 1 and 16 .. 16 + tail - 1.
+template <typename T>
+__device__ __forceinline__ void copy_ends(T* dst, const T* src, const TileCopy& c, int count,
+                                          int tid) {
+    const int tail = count - c.head - c.body;
+    if (tid < c.head) dst[tid] = src[tid];
+    const int t = tid - 16;
+    if (t >= 0 && t < tail) dst[c.head + c.body + t] = src[c.head + c.body + t];
+}
+
 template <typename K, int ITEMS>
 struct OnesweepSmem {
-    K keys[kThreads * ITEMS];
-    int32_t vals[kThreads * ITEMS];
+    K keys[kThreads * ITEMS];                             // the tile, reordered
+    alignas(16) int32_t stage_vals[kThreads * ITEMS + 4];  // the tile's values as loaded
+    int32_t vals[kThreads * ITEMS];                    // reordered values
+    uint64_t bar;                                      // completes the bulk copies
     uint32_t warp_count[kWarps][256];  // per-warp digit counts, then warp prefixes
     uint32_t local_start[256];         // first slot of each digit in the tile
     int64_t out_base[256];             // output index of slot 0 of each digit
@@ -106,26 +144,40 @@ __global__ void __launch_bounds__(kThreads, 4)
                const uint32_t* __restrict__ wide_low = nullptr) {
     __shared__ OnesweepSmem<K, ITEMS> sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) sm.blk = atomicAdd(ticket, 1u);
+    if (tid == 0) {
+        sm.blk = atomicAdd(ticket, 1u);
+        mbar_init(&sm.bar, 1);
+    }
     for (int i = tid; i < kWarps * 256; i += kThreads) (&sm.warp_count[0][0])[i] = 0;
     __syncthreads();
     const int64_t blk = sm.blk;
     const int64_t tile_base = blk * (kThreads * ITEMS);
-    const int64_t warp_base = tile_base + (int64_t)warp * (kWarp * ITEMS);
+    const int warp_local = warp * (kWarp * ITEMS);
+    const int64_t warp_base = tile_base + warp_local;
+
+    // 2. the tile's values into shared memory while the keys are ranked: the
+    //    16-byte aligned middle by one bulk copy, the ragged ends (under 16
+    //    bytes each) by plain loads; value j lands at stage_vals[shift + j].
+    //    The keys come straight into registers, warp-striped.
+    // (no keys for a virtual block past the end: a test of the timeout path
+    // starts the tickets late)
+    const int64_t left = n - tile_base;
+    const int tile_n = left <= 0 ? 0 : (left < kThreads * ITEMS ? (int)left : kThreads * ITEMS);
+    const TileCopy vc = IOTA ? TileCopy{0, 0, 0} : plan_copy(vals_in + tile_base, tile_n);
+    const uint32_t tx = (uint32_t)(vc.body * 4);
+    if (tid == 0 && tx) {
+        mbar_expect_tx(&sm.bar, tx);
+        bulk_to_shared(sm.stage_vals + vc.shift + vc.head, vals_in + tile_base + vc.head, tx,
+                       &sm.bar);
+    }
+    if (!IOTA) copy_ends(sm.stage_vals + vc.shift, vals_in + tile_base, vc, tile_n, tid);
 
     K key[ITEMS];
-    int32_t val[ITEMS];
     uint32_t rank[ITEMS];
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
-        const int64_t idx = warp_base + i * kWarp + lane;
-        if (idx < n) {
-            key[i] = keys_in[idx];
-            val[i] = IOTA ? (int32_t)idx : vals_in[idx];
-        } else {
-            key[i] = K(0);
-            val[i] = 0;
-        }
+        const int local = warp_local + i * kWarp + lane;
+        key[i] = local < tile_n ? keys_in[tile_base + local] : K(0);
     }
 
     // 3. rank within the warp, in element order (i, then lane): for each
@@ -199,8 +251,16 @@ __global__ void __launch_bounds__(kThreads, 4)
     int64_t tile_count;
     const int64_t lstart = block_exclusive_scan<kThreads>(total, sm.scratch_b, &tile_count);
     sm.local_start[d] = (uint32_t)lstart;
+    // the values' bulk copy has had the ranking and the look-back to land
+    const bool ok = tx == 0 || mbar_wait(&sm.bar, 0, kBulkPolls);
     sm.out_base[d] = bucket_start + excl - lstart;
-    __syncthreads();
+    if (__syncthreads_or(!ok)) {
+        // the copy never completed: report, give it one more bounded wait
+        // (it writes this block's shared memory), and stop
+        if (tid == 0) err.raise(GS_ERR_TIMEOUT);
+        mbar_wait(&sm.bar, 0, kBulkPolls);
+        return;
+    }
 
     // 5. reorder by digit in shared memory, then write out bucket runs
 #pragma unroll
@@ -208,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, 4)
         if (warp_base + i * kWarp + lane < n) {
             const uint32_t dd = digit_of(key[i], shift, dmask);
             const uint32_t pos = sm.local_start[dd] + sm.warp_count[warp][dd] + rank[i];
+            const int local = warp_local + i * kWarp + lane;
             sm.keys[pos] = key[i];
-            sm.vals[pos] = val[i];
+            sm.vals[pos] = IOTA ? (int32_t)(tile_base + local) : sm.stage_vals[vc.shift + local];
         }
     }
     __syncthreads();
