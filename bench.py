@@ -457,6 +457,7 @@ def run_ours(args, rank, world, scene):
         "data": "synthetic (seeded workload 3 generator)",
         "config": workload_config(s, I, max_list, world),
         "msplat_isect_per_s": round(I / (isect_ms * 1e-3) / 1e6, 1),
+        "msplat_per_s": round(s.C * s.N / (ms * 1e-3) / 1e6, 1),
         "mpixel_per_s_fwd": stages["raster_fwd"]["mpix_s"],
         "mpixel_per_s_bwd": stages["raster_bwd"]["mpix_s"],
         "stages": stages,
@@ -531,7 +532,8 @@ def method_bytes(s, I):
 def isect_summary(s, I, st, hbm_peak):
     """Intersect + sort + ranges as one stage, under both byte models."""
     ms = float(st[0] + st[1] + st[2])
-    out = {"ms": round(ms, 4), "msplat_isect_per_s": round(I / (ms * 1e-3) / 1e6, 1)}
+    out = {"ms": round(ms, 4), "msplat_isect_per_s": round(I / (ms * 1e-3) / 1e6, 1),
+           "msplat_per_s": round(s.C * s.N / (ms * 1e-3) / 1e6, 1)}
     for name, model in (("impl", impl_bytes(s, I)), ("method", method_bytes(s, I))):
         b = sum(model.values())
         gbs = b / (ms * 1e-3) / 1e9
