@@ -181,6 +181,35 @@ def test_sort_pairs(n, distinct, begin, end):
         np.testing.assert_array_equal(v.cpu().numpy(), rv)
 
 
+@pytest.mark.parametrize("koff,voff", [(0, 0), (1, 1), (0, 2), (1, 3)])
+@pytest.mark.parametrize("n", [5, 2048 * 3 + 7, 100_003])
+def test_sort_pairs_unaligned_buffers(n, koff, voff):
+    # the radix passes bring each tile's values in by a bulk copy of their
+    # 16-byte aligned middle plus plain loads of the ragged ends: keys 8 bytes
+    # and values 4, 8 or 12 bytes past a 16-byte boundary sort exactly as
+    # aligned ones, and the elements beside the slices stay untouched
+    rng = np.random.default_rng(n + 7 * koff + voff)
+    pool = rng.integers(0, 2**63, max(n // 3, 1), dtype=np.uint64)
+    keys = rng.choice(pool, n).astype(np.uint64)
+    vals = np.arange(n, dtype=np.int32)
+    kbuf = torch.full((n + 2,), -7, dtype=torch.int64, device=DEV)
+    vbuf = torch.full((n + 4,), -7, dtype=torch.int32, device=DEV)
+    k = kbuf[koff:koff + n]
+    v = vbuf[voff:voff + n]
+    k.copy_(torch.from_numpy(keys.view(np.int64).copy()))
+    v.copy_(torch.from_numpy(vals.copy()))
+    assert (k.data_ptr() % 16 != 0) == (koff == 1) and (v.data_ptr() % 16) == 4 * voff
+    st = gs.new_status(DEV)
+    gs.gs_sort_pairs(k, v, 0, 64, d_status=st)
+    gs.check_status(st)
+    perm = np.argsort(keys, kind="stable")
+    np.testing.assert_array_equal(u64(k), keys[perm])
+    np.testing.assert_array_equal(v.cpu().numpy(), vals[perm])
+    kb, vb = kbuf.cpu().numpy(), vbuf.cpu().numpy()
+    assert (np.delete(kb, np.arange(koff, koff + n)) == -7).all()
+    assert (np.delete(vb, np.arange(voff, voff + n)) == -7).all()
+
+
 def test_repeat_runs_bit_identical():
     # races in the scan/sort would show up as run-to-run differences
     s = scenes.workload2()
