@@ -325,9 +325,9 @@ __device__ __forceinline__ void st_shared_lane0(uint32_t* dst, uint4 v, int lane
 __device__ __forceinline__ float& comp(float2& v, int i) { return i ? v.y : v.x; }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 
-// At most 72 registers, so 14 blocks (28 warps) fit on an SM: measured 3.5 %
-// faster than 12 blocks at 80 registers despite a few spilled bytes.  With
-// the pair counters (a diagnostic) 80 registers, 12 blocks.
+// At most 72 registers, so 14 blocks (28 warps) fit on an SM: measured
+// faster than 12 blocks at 80 registers and than 16 at 64.  With the pair
+// counters (a diagnostic) 80 registers, 12 blocks.
 //
 // A thread's 4 pixels are handled as two pairs (rows 0-1 and 2-3 of its
 // strip) with the packed f32x2 operations, whose per-component rounding is
