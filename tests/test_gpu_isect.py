@@ -50,6 +50,28 @@ def test_random_multi_camera_ragged(seed):
     assert n > 3 * 3072
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_emission_long_runs_and_empty_splats(seed):
+    # the emission hands each warp 64 consecutive splats (in depth order) and
+    # writes their keys 32 at a time, a key's splat found from the round's
+    # splat-start bits or carried over from the previous round: splats of
+    # hundreds of tiles (many rounds with no start), long stretches of splats
+    # off screen (no keys), and single-tile splats side by side, in a
+    # depth order that mixes them, must give the oracle's keys bit for bit
+    s = scenes.random_small(30 + seed, C=2, N=3000, W=640, H=360, sigma=(0.5, 2.0))
+    rng = np.random.default_rng(seed)
+    kind = rng.integers(0, 10, (s.C, s.N))
+    big = kind == 0            # about 10 %: radii of 60-200 px
+    gone = (kind >= 1) & (kind <= 4)  # about 40 %: entirely off screen
+    s.radii[big] = rng.uniform(60.0, 200.0, (int(big.sum()), 2)).astype(np.float32)
+    s.means2d[gone] = np.float32(-1000.0)
+    # runs of equal depth so that long stretches of one kind meet in the order
+    s.depths[:] = np.where(big, 1.0, np.where(gone, 2.0, 3.0)).astype(np.float32)
+    s.depths[:, ::97] = np.float32(2.5)
+    n = _check_isect(s)
+    assert n > 10 * 3072
+
+
 def test_equal_depths_keep_splat_order():
     # many equal depths and equal keys: the sort must be stable
     s = scenes.random_small(7, C=2, N=20000, W=256, H=256, sigma=(0.5, 6.0))
