@@ -399,7 +399,10 @@ def run_ours(args, rank, world, scene):
     # end to end through host buffers (pipelined: see Path.run_e2e)
     h2d, d2h = path.setup_e2e()
     path.run_e2e(3)
-    e2e = max_over_ranks(path.run_e2e(max(5, min(args.steps, 20))), world, dev)
+    # the median of three runs: host-side copies see other traffic on the
+    # host's memory now and then, which a single run can catch
+    e2e_runs = sorted(path.run_e2e(max(5, min(args.steps, 20))) for _ in range(3))
+    e2e = max_over_ranks(e2e_runs[1], world, dev)
 
     proj = bins = steps_trace = None
     if not args.main_only:
@@ -472,9 +475,10 @@ def run_ours(args, rank, world, scene):
         "e2e": {"value": round(whole_job_rate(pixels, e2e, world) / 1e6, 2),
                 "unit": "Mpixel/s",
                 "note": "pinned host inputs -> image + gradients on the host; uploads and "
-                        "downloads overlapped with the previous/next step",
+                        "downloads overlapped with the previous/next step; median of 3 runs",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e, 3)},
+                "ms_per_step": round(e2e, 3),
+                "runs_ms_per_step": [round(x, 3) for x in e2e_runs]},
         "gpu_launches": args.steps * launches_per_step(s),
         "clocks": clk,
         "wall_s_timed": round(t_wall, 3),
