@@ -42,22 +42,35 @@ __global__ void __launch_bounds__(kThreads)
                   int tile_height, int32_t* __restrict__ tiles_per_gauss,
                   unsigned long long* __restrict__ total) {
     __shared__ int64_t scratch[32];
+    constexpr int U = 4;  // splats per thread and round, their loads issued together
     int64_t local = 0;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < CN; i += stride) {
-        const float2 m = reinterpret_cast<const float2*>(means2d)[i];
-        float rx, ry;
-        if (elliptical) {
-            const float2 r = reinterpret_cast<const float2*>(radii)[i];
-            rx = r.x;
-            ry = r.y;
-        } else {
-            rx = ry = radii[i];
+    for (int64_t i0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; i0 < CN; i0 += U * stride) {
+        float2 m[U], r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + u * stride;
+            m[u] = make_float2(0.0f, 0.0f);
+            r[u] = make_float2(0.0f, 0.0f);
+            if (i < CN) {
+                m[u] = reinterpret_cast<const float2*>(means2d)[i];
+                if (elliptical) {
+                    r[u] = reinterpret_cast<const float2*>(radii)[i];
+                } else {
+                    r[u].x = r[u].y = radii[i];
+                }
+            }
         }
-        const Rect r = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
-        const int cnt = (r.x1 - r.x0) * (r.y1 - r.y0);
-        if (tiles_per_gauss) tiles_per_gauss[i] = cnt;
-        local += cnt;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i >= CN) break;
+            const Rect rc = splat_rect(m[u].x, m[u].y, r[u].x, r[u].y, ts, inv_ts, tile_width,
+                                       tile_height);
+            const int cnt = (rc.x1 - rc.x0) * (rc.y1 - rc.y0);
+            if (tiles_per_gauss) tiles_per_gauss[i] = cnt;
+            local += cnt;
+        }
     }
     int64_t sum;
     block_exclusive_scan<kThreads>(local, scratch, &sum);
