@@ -91,34 +91,48 @@ __global__ void __launch_bounds__(kThreads)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t begin = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    const int64_t rounds = (CN + stride - 1) / stride;  // same trip count in every lane
+    constexpr int U = 2;  // splats per thread and round, their loads issued together
+    // same trip count in every lane
+    const int64_t rounds = (CN + U * stride - 1) / (U * stride);
     for (int64_t r = 0; r < rounds; ++r) {
-        const int64_t i = begin + r * stride;
-        const bool valid = i < CN;
-        uint32_t key = 0;
-        if (valid) {
-            const float2 m = reinterpret_cast<const float2*>(means2d)[i];
-            float rx, ry;
-            if (elliptical) {
-                const float2 rr = reinterpret_cast<const float2*>(radii)[i];
-                rx = rr.x;
-                ry = rr.y;
-            } else {
-                rx = ry = radii[i];
-            }
-            const Rect rc = splat_rect(m.x, m.y, rx, ry, ts, inv_ts, tile_width, tile_height);
-            rects[i] = make_int4(rc.x0, rc.y0, rc.x1, rc.y1);
-            key = dbits[i];
-        }
-        const bool full = __all_sync(0xffffffffu, valid);
+        float2 m[U], rr[U];
+        uint32_t key[U];
+        bool valid[U];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const uint32_t d = (key >> (8 * p)) & 0xffu;
-            const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
-            if (full && __all_sync(0xffffffffu, d == d0)) {
-                if (lane == 0) sh[warp][p][d] += 32u;
-            } else if (valid) {
-                atomicAdd(&sh[warp][p][d], 1u);
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = begin + (r * U + u) * stride;
+            valid[u] = i < CN;
+            m[u] = make_float2(0.0f, 0.0f);
+            rr[u] = make_float2(0.0f, 0.0f);
+            key[u] = 0;
+            if (valid[u]) {
+                m[u] = reinterpret_cast<const float2*>(means2d)[i];
+                if (elliptical) {
+                    rr[u] = reinterpret_cast<const float2*>(radii)[i];
+                } else {
+                    rr[u].x = rr[u].y = radii[i];
+                }
+                key[u] = dbits[i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = begin + (r * U + u) * stride;
+            if (valid[u]) {
+                const Rect rc = splat_rect(m[u].x, m[u].y, rr[u].x, rr[u].y, ts, inv_ts,
+                                           tile_width, tile_height);
+                rects[i] = make_int4(rc.x0, rc.y0, rc.x1, rc.y1);
+            }
+            const bool full = __all_sync(0xffffffffu, valid[u]);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t d = (key[u] >> (8 * p)) & 0xffu;
+                const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+                if (full && __all_sync(0xffffffffu, d == d0)) {
+                    if (lane == 0) sh[warp][p][d] += 32u;
+                } else if (valid[u]) {
+                    atomicAdd(&sh[warp][p][d], 1u);
+                }
             }
         }
     }
