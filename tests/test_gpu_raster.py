@@ -186,6 +186,19 @@ def test_backward_ragged_with_background(seed, W, H, C):
                                rtol=1e-4, atol=1e-3)
 
 
+def test_many_cameras():
+    # 37 small cameras (3 x 2 tiles each, the last row and column ragged):
+    # tile -> camera indexing, per-camera backgrounds and their gradients,
+    # and the keys' camera bits (6 of them) through the forward and backward
+    s = scenes.random_small(12, C=37, N=300, W=40, H=24, sigma=(0.5, 6.0))
+    iso, ref = _oracle_forward(s)
+    compare_forward(ref, gpu_forward(s, scene_to_dev(s)), s)
+    rb, got, excluded = _bwd_case(s)
+    _compare_grads(rb, got, excluded)
+    np.testing.assert_allclose(got["grad_backgrounds"].cpu().numpy(), rb["grad_backgrounds"],
+                               rtol=1e-4, atol=1e-3)
+
+
 def test_backward_masks_and_dense_stack():
     s = scenes.random_small(6, C=1, N=6000, W=64, H=64, sigma=(3.0, 12.0), opacity=(0.5, 0.99))
     masks = np.array([[[1, 0, 1, 1], [1, 1, 0, 1], [1, 1, 1, 1], [0, 1, 1, 1]]], np.int32)
