@@ -824,7 +824,8 @@ def time_bins(path, max_list, flush, warmup, steps):
     nb = s.C * s.tile_width * s.tile_height
     # fill: mean + radii per splat, one 4-byte id per intersection; sort: read
     # the id, gather 4 bytes of depth, write every slot (ids and -1s)
-    return {"kernels": "k_bin_fill, k_bin_sort", "ms": round(ms, 4), "capacity": M,
+    return {"kernels": "k_bin_fill, k_bin_merge (+ k_bin_merge_large above 2048 per bin)",
+            "ms": round(ms, 4), "capacity": M,
             "bytes": s.C * s.N * 16 + path.I * (4 + 4 + 4) + nb * M * 4,
             "note": "alternative to emit + sort + ranges; not part of the step"}
 

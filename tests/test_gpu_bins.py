@@ -33,7 +33,14 @@ def _ties_scene():
 def _scene(kind):
     return {"w1": scenes.workload1, "w2": scenes.workload2, "ties": _ties_scene,
             "cams": lambda: scenes.random_small(3, C=3, N=800, W=90, H=70,
-                                                sigma=(0.5, 12.0))}[kind]()
+                                                sigma=(0.5, 12.0)),
+            # bins of 2-3.4k entries beside smaller ones: both merge kernels
+            "mid": lambda: scenes.random_small(6, C=2, N=9000, W=400, H=300,
+                                               sigma=(0.5, 60.0)),
+            # every bin about 15k entries: the bitonic network of the largest
+            # capacities
+            "big": lambda: scenes.random_small(5, C=1, N=15000, W=64, H=48,
+                                               sigma=(30.0, 60.0))}[kind]()
 
 
 def _gpu_bins(s, d, M, status=None):
@@ -43,7 +50,7 @@ def _gpu_bins(s, d, M, status=None):
     return bins.cpu().numpy(), counts.cpu().numpy()
 
 
-@pytest.mark.parametrize("kind", ["w1", "w2", "ties", "cams"])
+@pytest.mark.parametrize("kind", ["w1", "w2", "ties", "cams", "mid", "big"])
 def test_bins_bit_exact(kind):
     s = _scene(kind)
     _, _, largest = oracle.bin_splats(s.means2d, s.radii, s.depths, s.tile_size, s.tile_width,
@@ -58,11 +65,13 @@ def test_bins_bit_exact(kind):
     np.testing.assert_array_equal(b, rb)
 
 
-def test_bins_overflow():
-    s = _scene("cams")
+@pytest.mark.parametrize("kind", ["cams", "mid"])
+def test_bins_overflow(kind):
+    s = _scene(kind)
     _, rc, largest = oracle.bin_splats(s.means2d, s.radii, s.depths, s.tile_size, s.tile_width,
                                        s.tile_height, 1)
-    M = max(1, largest // 3)
+    # "mid": a capacity above 2048, so that the bins it cuts are the larger ones
+    M = max(1, largest // 3) if kind == "cams" else largest * 2 // 3
     full, _, _ = oracle.bin_splats(s.means2d, s.radii, s.depths, s.tile_size, s.tile_width,
                                    s.tile_height, largest)
     st = gs.new_status(DEV)

@@ -10,11 +10,18 @@
 //               each appends its splat to the tile's bin with one atomic on
 //               the tile's counter.  The order inside a bin is the order the
 //               atomics happened to take.
-//   k_bin_sort  one block per bin: its entries, keyed (depth bits << 32 |
-//               splat index), are sorted by a bitonic network (short strides
-//               in registers with warp shuffles, long ones in shared memory),
-//               written back in order and followed by -1s.  The result does
-//               not depend on the append order.
+//   k_bin_merge one block per bin of at most kSmallBin entries (every bin when
+//               the capacity allows no more): its entries, keyed (depth bits
+//               << 32 | splat index), are merge-sorted in shared memory --
+//               64-entry chunks in registers with warp shuffles, then runs
+//               merged pairwise, each entry placed by a binary search in the
+//               partner run -- written back in order and followed by -1s.
+//   k_bin_merge_large  the same for the larger bins, 1024 threads, a few
+//               blocks per SM walking the bins in turn (the small ones
+//               skipped); above kMergeMaxCapacity (two key buffers no longer
+//               fit in shared memory) a bitonic network on one power-of-two
+//               buffer instead.
+//   The result does not depend on the append order.
 #include <cstdint>
 
 #include "gs_device.cuh"
@@ -26,7 +33,12 @@ namespace {
 
 constexpr int kFillThreads = 256;
 constexpr int kFillSplats = 2 * kFillThreads;
-constexpr int kBinSortThreads = 256;
+constexpr int kBinSortThreads = 256;       // k_bin_merge
+constexpr int kLargeBinThreads = 1024;     // k_bin_merge_large
+constexpr int kSmallBin = 2048;            // entries of the largest bin k_bin_merge sorts
+// Largest capacity merge-sorted by k_bin_merge_large (two buffers of 64-bit
+// keys in shared memory); above it a bitonic network on one buffer.
+constexpr int kMergeMaxCapacity = 14336;
 
 struct FillSmem {
     int32_t incl[kFillSplats];  // inclusive prefix of pair counts in the chunk
@@ -79,20 +91,36 @@ __global__ void __launch_bounds__(kFillThreads)
     sm.incl[2 * tid + 1] = (int32_t)(excl + cnt[0] + cnt[1]);
     __syncthreads();
     const int total = (int)chunk_total;
-    for (int q = tid; q < total; q += kFillThreads) {
-        int lo = 0, hi = kFillSplats - 1;  // owner: first o with incl[o] > q
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sm.incl[mid] > q) hi = mid;
-            else lo = mid + 1;
+    // four pairs per thread and round: their owner searches and atomics are
+    // issued together, so the atomics' returns overlap
+    constexpr int U = 4;
+    for (int q0 = tid; q0 < total; q0 += U * kFillThreads) {
+        int64_t t[U];
+        int32_t id[U], k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = q0 + u * kFillThreads;
+            t[u] = -1;
+            if (q < total) {
+                int lo = 0, hi = kFillSplats - 1;  // owner: first o with incl[o] > q
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (sm.incl[mid] > q) hi = mid;
+                    else lo = mid + 1;
+                }
+                const int o = lo;
+                const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
+                const int dy = li / sm.w[o];
+                t[u] = sm.tile0[o] + (int64_t)(sm.y0[o] + dy) * tile_width + sm.x0[o] +
+                       (li - dy * sm.w[o]);
+                id[u] = sm.sid[o];
+            }
         }
-        const int o = lo;
-        const int li = q - (o == 0 ? 0 : sm.incl[o - 1]);
-        const int dy = li / sm.w[o];
-        const int64_t t = sm.tile0[o] + (int64_t)(sm.y0[o] + dy) * tile_width + sm.x0[o] +
-                          (li - dy * sm.w[o]);
-        const int k = atomicAdd(&counts[t], 1);
-        if (k < capacity) bins[t * capacity + k] = sm.sid[o];
+#pragma unroll
+        for (int u = 0; u < U; ++u) k[u] = t[u] >= 0 ? atomicAdd(&counts[t[u]], 1) : capacity;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (k[u] < capacity) bins[t[u] * capacity + k[u]] = id[u];
     }
 }
 
@@ -130,74 +158,186 @@ __device__ __forceinline__ void chunk_stages(uint64_t& x0, uint64_t& x1, int bas
     }
 }
 
-// Bitonic sort of a bin's keys in shared memory over n2 = the next power of
-// two (at least 64) of the bin's entry count, padded with all-ones keys that
-// sort last.  Strides below 64 run in registers with warp shuffles on
-// 64-element chunks; only the longer strides go through shared memory with
-// a block barrier.
-__global__ void __launch_bounds__(kBinSortThreads)
-    k_bin_sort(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
-               int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
-               int32_t* d_status) {
-    extern __shared__ uint64_t keys[];
-    constexpr int kW = kBinSortThreads / kWarp;
-    const int64_t b = blockIdx.x;
-    if (b >= nbins) return;
+// Number of entries of the sorted run[0 .. n) below x (its lower bound).
+__device__ __forceinline__ int count_below(const uint64_t* run, int n, uint64_t x) {
+    int lo = 0;
+    while (n > 0) {
+        const int half = n >> 1;
+        if (run[lo + half] < x) {
+            lo += half + 1;
+            n -= half + 1;
+        } else {
+            n = half;
+        }
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint64_t bin_key(const uint32_t* depth_bits, const int32_t* bin, int k) {
+    const uint32_t id = (uint32_t)bin[k];
+    return ((uint64_t)depth_bits[id] << 32) | id;
+}
+
+// Merge sort of bin[0 .. cnt) (cnt >= 2) by key, in place, through the two
+// shared-memory buffers src and dst of at least cnt keys each.  Keys are
+// unique (a splat covers a tile once), so an entry's place in a merged run is
+// its place in its own run plus the number of the partner run's entries below
+// it.  Ends with a block barrier.
+template <int THREADS>
+__device__ void merge_sort_bin(const uint32_t* __restrict__ depth_bits, int32_t* bin, int cnt,
+                               uint64_t* src, uint64_t* dst) {
+    constexpr int kW = THREADS / kWarp;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int total = counts[b];
-    if (total > capacity && tid == 0) report(d_status, GS_ERR_CAPACITY);
-    const int cnt = total < capacity ? total : capacity;
-    int32_t* bin = bins + b * capacity;
-    int n2 = 64;
-    while (n2 < cnt) n2 <<= 1;
-    if (cnt > 1) {
-        for (int k = tid; k < n2; k += kBinSortThreads) {
-            uint64_t key = ~0ull;
-            if (k < cnt) {
-                const uint32_t id = (uint32_t)bin[k];
-                key = ((uint64_t)depth_bits[id] << 32) | id;
-            }
-            keys[k] = key;
+    for (int c = warp; c * 64 < cnt; c += kW) {
+        const int i0 = c * 64 + lane, i1 = i0 + 32;
+        uint64_t x0 = i0 < cnt ? bin_key(depth_bits, bin, i0) : ~0ull;  // padding sorts last
+        uint64_t x1 = i1 < cnt ? bin_key(depth_bits, bin, i1) : ~0ull;
+        chunk_stages(x0, x1, 0, 2, 64, lane);  // all levels up to 64, ascending
+        if (i0 < cnt) src[i0] = x0;
+        if (i1 < cnt) src[i1] = x1;
+    }
+    __syncthreads();
+    for (int L = 64; L < cnt; L <<= 1) {
+        for (int i = tid; i < cnt; i += THREADS) {
+            const uint64_t x = src[i];
+            const int start = i & ~(L - 1);       // this run
+            const int pair = start & ~(2 * L - 1);  // the merged run
+            const bool left = start == pair;
+            const int p0 = left ? start + L : pair;  // the partner run [p0, p1)
+            const int p1 = left ? min(start + 2 * L, cnt) : start;
+            const int below = p1 > p0 ? count_below(src + p0, p1 - p0, x) : 0;
+            dst[pair + (i - start) + below] = x;
         }
         __syncthreads();
-        for (int size = 2; size <= n2; size <<= 1) {
-            // shared-memory stages of this level (strides >= 64)
-            for (int stride = size >> 1; stride >= 64; stride >>= 1) {
-                for (int p = tid; p < (n2 >> 1); p += kBinSortThreads) {
-                    const int lo = ((p / stride) * 2 * stride) + (p % stride);
-                    const int hi = lo + stride;
-                    const bool ascending = (lo & size) == 0;
-                    const uint64_t x = keys[lo], y = keys[hi];
-                    if ((x > y) == ascending) {
-                        keys[lo] = y;
-                        keys[hi] = x;
-                    }
+        uint64_t* t = src;
+        src = dst;
+        dst = t;
+    }
+    for (int k = tid; k < cnt; k += THREADS) bin[k] = (int32_t)(uint32_t)src[k];
+    __syncthreads();
+}
+
+// Bitonic sort of bin[0 .. cnt) (cnt >= 2) by key over n2 = the next power
+// of two (at least 64) of cnt, padded with all-ones keys that sort last, in
+// one shared-memory buffer of n2 keys.  Strides below 64 run in registers
+// with warp shuffles on 64-element chunks; only the longer strides go
+// through shared memory with a block barrier.  Ends with a block barrier.
+template <int THREADS>
+__device__ void bitonic_sort_bin(const uint32_t* __restrict__ depth_bits, int32_t* bin, int cnt,
+                                 uint64_t* keys) {
+    constexpr int kW = THREADS / kWarp;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int n2 = 64;
+    while (n2 < cnt) n2 <<= 1;
+    for (int k = tid; k < n2; k += THREADS) keys[k] = k < cnt ? bin_key(depth_bits, bin, k) : ~0ull;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride >= 64; stride >>= 1) {
+            for (int p = tid; p < (n2 >> 1); p += THREADS) {
+                const int lo = ((p / stride) * 2 * stride) + (p % stride);
+                const int hi = lo + stride;
+                const bool ascending = (lo & size) == 0;
+                const uint64_t x = keys[lo], y = keys[hi];
+                if ((x > y) == ascending) {
+                    keys[lo] = y;
+                    keys[hi] = x;
                 }
-                __syncthreads();
-            }
-            // the rest in registers: all levels up to 64 at once, then per level
-            const int size_lo = size <= 64 ? 2 : size, size_hi = size <= 64 ? 64 : size;
-            for (int c = warp; c < n2 / 64; c += kW) {
-                uint64_t x0 = keys[c * 64 + lane], x1 = keys[c * 64 + lane + 32];
-                chunk_stages(x0, x1, c * 64, size_lo, size_hi, lane);
-                keys[c * 64 + lane] = x0;
-                keys[c * 64 + lane + 32] = x1;
             }
             __syncthreads();
-            if (size < 64) size = 64;  // levels 2..64 are done
         }
-        for (int k = tid; k < cnt; k += kBinSortThreads) bin[k] = (int32_t)(uint32_t)keys[k];
+        // the rest in registers: all levels up to 64 at once, then per level
+        const int size_lo = size <= 64 ? 2 : size, size_hi = size <= 64 ? 64 : size;
+        for (int c = warp; c < n2 / 64; c += kW) {
+            uint64_t x0 = keys[c * 64 + lane], x1 = keys[c * 64 + lane + 32];
+            chunk_stages(x0, x1, c * 64, size_lo, size_hi, lane);
+            keys[c * 64 + lane] = x0;
+            keys[c * 64 + lane + 32] = x1;
+        }
+        __syncthreads();
+        if (size < 64) size = 64;  // levels 2..64 are done
     }
-    for (int k = cnt + tid; k < capacity; k += kBinSortThreads) bin[k] = -1;
+    for (int k = tid; k < cnt; k += THREADS) bin[k] = (int32_t)(uint32_t)keys[k];
+    __syncthreads();
+}
+
+// Bin b's entry count (reporting an overflow) and its -1 tail.
+template <int THREADS>
+__device__ __forceinline__ int bin_entries(int64_t b, int capacity, const int32_t* counts,
+                                           int32_t* d_status) {
+    const int total = counts[b];
+    if (total > capacity && threadIdx.x == 0) report(d_status, GS_ERR_CAPACITY);
+    return total < capacity ? total : capacity;
+}
+
+template <int THREADS>
+__device__ __forceinline__ void fill_tail(int32_t* bin, int cnt, int capacity) {
+    for (int k = cnt + (int)threadIdx.x; k < capacity; k += THREADS) bin[k] = -1;
+}
+
+// One block per bin; bins of more than kSmallBin entries are left to
+// k_bin_merge_large.  Shared memory: two buffers of min(capacity, kSmallBin)
+// keys, rounded up to 64.
+__global__ void __launch_bounds__(kBinSortThreads)
+    k_bin_merge(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
+                int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
+                int32_t* d_status) {
+    extern __shared__ uint64_t keys[];
+    const int64_t b = blockIdx.x;
+    if (b >= nbins) return;
+    const int cnt = bin_entries<kBinSortThreads>(b, capacity, counts, d_status);
+    if (cnt > kSmallBin) return;
+    int32_t* bin = bins + b * capacity;
+    const int stride = ((capacity < kSmallBin ? capacity : kSmallBin) + 63) & ~63;
+    if (cnt > 1) merge_sort_bin<kBinSortThreads>(depth_bits, bin, cnt, keys, keys + stride);
+    fill_tail<kBinSortThreads>(bin, cnt, capacity);
+}
+
+// Bins of more than kSmallBin entries, walked in turn by a grid of a few
+// blocks per SM.  MERGE: two buffers of capacity keys (rounded up to 64);
+// otherwise one power-of-two buffer for the bitonic network.
+template <bool MERGE>
+__global__ void __launch_bounds__(kLargeBinThreads)
+    k_bin_merge_large(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
+                      int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
+                      int32_t* d_status) {
+    extern __shared__ uint64_t keys[];
+    for (int64_t b = blockIdx.x; b < nbins; b += gridDim.x) {
+        const int cnt = bin_entries<kLargeBinThreads>(b, capacity, counts, d_status);
+        if (cnt <= kSmallBin) continue;
+        int32_t* bin = bins + b * capacity;
+        if (MERGE)
+            merge_sort_bin<kLargeBinThreads>(depth_bits, bin, cnt, keys,
+                                             keys + ((capacity + 63) & ~63));
+        else
+            bitonic_sort_bin<kLargeBinThreads>(depth_bits, bin, cnt, keys);
+        fill_tail<kLargeBinThreads>(bin, cnt, capacity);
+    }
 }
 
 }  // namespace
 
-int bin_sort_smem_bytes(int capacity) {
+namespace {
+
+int large_smem_bytes(int capacity) {
+    if (capacity <= kMergeMaxCapacity) return 2 * ((capacity + 63) & ~63) * 8;
     int n2 = 64;
     while (n2 < capacity) n2 <<= 1;
-    return n2 * (int)sizeof(uint64_t);
+    return n2 * 8;
 }
+
+template <typename K>
+int launch_sized(K kern, unsigned grid, int threads, int smem, cudaStream_t s,
+                 const uint32_t* depth_bits, int64_t nbins, int capacity, int32_t* bins,
+                 const int32_t* counts, int32_t* d_status) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+        return GS_ERR_CUDA;
+    kern<<<grid, threads, smem, s>>>(depth_bits, nbins, capacity, bins, counts, d_status);
+    return GS_OK;
+}
+
+}  // namespace
 
 int launch_bin_splats(const float* means2d, const float* radii, int elliptical,
                       const float* depths, int C, int N, int tile_size, int tile_width,
@@ -209,17 +349,29 @@ int launch_bin_splats(const float* means2d, const float* radii, int elliptical,
         const int64_t chunks = (CN + kFillSplats - 1) / kFillSplats;
         k_bin_fill<<<(unsigned)chunks, kFillThreads, 0, s>>>(
             means2d, radii, elliptical, CN, N, (float)tile_size, exact_tile_inverse(tile_size),
-            tile_width, tile_height,
-            capacity, bins, counts);
+            tile_width, tile_height, capacity, bins, counts);
     }
-    const int smem = bin_sort_smem_bytes(capacity);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(k_bin_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    const uint32_t* depth_bits = reinterpret_cast<const uint32_t*>(depths);
+    const int small = 2 * (((capacity < kSmallBin ? capacity : kSmallBin) + 63) & ~63) * 8;
+    int rc = launch_sized(k_bin_merge, (unsigned)nbins, kBinSortThreads, small, s, depth_bits,
+                          nbins, capacity, bins, counts, d_status);
+    if (rc != GS_OK || capacity <= kSmallBin) return rc;
+    // the larger bins: a grid of as many blocks as fit on the GPU at once
+    const int large = large_smem_bytes(capacity);
+    const bool merge = capacity <= kMergeMaxCapacity;
+    auto* kern = merge ? k_bin_merge_large<true> : k_bin_merge_large<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, large) !=
+        cudaSuccess)
+        return GS_ERR_CUDA;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLargeBinThreads, large) !=
             cudaSuccess)
         return GS_ERR_CUDA;
-    k_bin_sort<<<(unsigned)nbins, kBinSortThreads, smem, s>>>(
-        reinterpret_cast<const uint32_t*>(depths), nbins, capacity, bins, counts, d_status);
-    return GS_OK;
+    const int64_t grid = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    return launch_sized(kern, (unsigned)(grid < nbins ? grid : nbins), kLargeBinThreads, large,
+                        s, depth_bits, nbins, capacity, bins, counts, d_status);
 }
 
 }  // namespace gs
