@@ -16,11 +16,13 @@
 //               64-entry chunks in registers with warp shuffles, then runs
 //               merged pairwise, each entry placed by a binary search in the
 //               partner run -- written back in order and followed by -1s.
-//   k_bin_merge_large  the same for the larger bins, 1024 threads, a few
-//               blocks per SM walking the bins in turn (the small ones
-//               skipped); above kMergeMaxCapacity (two key buffers no longer
-//               fit in shared memory) a bitonic network on one power-of-two
-//               buffer instead.
+//   k_bin_merge_large  the larger bins, 1024 threads, as many blocks as fit
+//               on the GPU walking the bins in turn (the small ones skipped):
+//               runs of eight sorted in registers, then merged pairwise with
+//               each thread writing several consecutive entries from one
+//               binary search (merge path); above kMergeMaxCapacity (two key
+//               buffers no longer fit in shared memory) a bitonic network on
+//               one power-of-two buffer instead.
 //   The result does not depend on the append order.
 #include <cstdint>
 
@@ -217,6 +219,89 @@ __device__ void merge_sort_bin(const uint32_t* __restrict__ depth_bits, int32_t*
     __syncthreads();
 }
 
+// Compare-exchange of two registers: a gets the smaller key.
+__device__ __forceinline__ void order2(uint64_t& a, uint64_t& b) {
+    const uint64_t lo = a < b ? a : b, hi = a < b ? b : a;
+    a = lo;
+    b = hi;
+}
+
+// Batcher's odd-even merge sort of eight keys held in registers (19
+// compare-exchanges).
+__device__ __forceinline__ void sort8(uint64_t (&v)[8]) {
+    order2(v[0], v[1]); order2(v[2], v[3]); order2(v[4], v[5]); order2(v[6], v[7]);
+    order2(v[0], v[2]); order2(v[1], v[3]); order2(v[4], v[6]); order2(v[5], v[7]);
+    order2(v[1], v[2]); order2(v[5], v[6]);
+    order2(v[0], v[4]); order2(v[1], v[5]); order2(v[2], v[6]); order2(v[3], v[7]);
+    order2(v[2], v[4]); order2(v[3], v[5]);
+    order2(v[1], v[2]); order2(v[3], v[4]); order2(v[5], v[6]);
+}
+
+// The same sort for long bins, where a thread has several entries per
+// merge: runs of eight are sorted in registers; then runs of 8, 16, ... are
+// merged pairwise, each thread writing E consecutive entries of the merged
+// runs -- it finds where its first entry's diagonal crosses the two runs by
+// binary search (the merge path) and merges sequentially from there.  E is
+// odd (so a warp's 8-byte stores spread over the banks) and large enough
+// that one pass of the block covers the bin (cnt <= THREADS * E).  Buffers
+// of at least cnt keys rounded up to 8.  Ends with a block barrier.
+template <int THREADS>
+__device__ void merge_path_sort_bin(const uint32_t* __restrict__ depth_bits, int32_t* bin,
+                                    int cnt, uint64_t* src, uint64_t* dst) {
+    const int tid = threadIdx.x;
+    const int E = max(7, (cnt + THREADS - 1) / THREADS) | 1;
+    for (int r = tid; r * 8 < cnt; r += THREADS) {
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = r * 8 + j < cnt ? bin_key(depth_bits, bin, r * 8 + j) : ~0ull;  // padding last
+        sort8(v);
+        ulonglong2* out = reinterpret_cast<ulonglong2*>(src + r * 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[j] = make_ulonglong2(v[2 * j], v[2 * j + 1]);
+    }
+    __syncthreads();
+    for (int L = 8; L < cnt; L <<= 1) {
+        for (int o0 = tid * E; o0 < cnt; o0 += THREADS * E) {
+            const int o1 = min(o0 + E, cnt);
+            int o = o0;
+            while (o < o1) {  // a step may cross into the next pair of runs
+                const int pair = o & ~(2 * L - 1);
+                const int la = min(L, cnt - pair);             // run A = src[pair, +la)
+                const int lb = max(0, min(L, cnt - pair - L));  // run B right after it
+                const int seg = min(o1, pair + la + lb);
+                const uint64_t* A = src + pair;
+                const uint64_t* B = A + la;
+                const int d = o - pair;  // entries of the merged run before o
+                int lo = max(0, d - lb), hi = min(d, la);
+                while (lo < hi) {  // entries of A among those d
+                    const int mid = (lo + hi) >> 1;
+                    if (A[mid] < B[d - 1 - mid]) lo = mid + 1;
+                    else hi = mid;
+                }
+                int ia = lo, ib = d - lo;
+                uint64_t va = ia < la ? A[ia] : ~0ull, vb = ib < lb ? B[ib] : ~0ull;
+                for (; o < seg; ++o) {
+                    const bool ta = va < vb;
+                    dst[o] = ta ? va : vb;
+                    ia += ta;
+                    ib += !ta;
+                    const bool more = ta ? ia < la : ib < lb;
+                    const uint64_t x = more ? (ta ? A[ia] : B[ib]) : ~0ull;
+                    va = ta ? x : va;
+                    vb = ta ? vb : x;
+                }
+            }
+        }
+        __syncthreads();
+        uint64_t* t = src;
+        src = dst;
+        dst = t;
+    }
+    for (int k = tid; k < cnt; k += THREADS) bin[k] = (int32_t)(uint32_t)src[k];
+    __syncthreads();
+}
+
 // Bitonic sort of bin[0 .. cnt) (cnt >= 2) by key over n2 = the next power
 // of two (at least 64) of cnt, padded with all-ones keys that sort last, in
 // one shared-memory buffer of n2 keys.  Strides below 64 run in registers
@@ -281,7 +366,7 @@ __global__ void __launch_bounds__(kBinSortThreads)
     k_bin_merge(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
                 int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
                 int32_t* d_status) {
-    extern __shared__ uint64_t keys[];
+    extern __shared__ __align__(16) uint64_t keys[];
     const int64_t b = blockIdx.x;
     if (b >= nbins) return;
     const int cnt = bin_entries<kBinSortThreads>(b, capacity, counts, d_status);
@@ -300,14 +385,14 @@ __global__ void __launch_bounds__(kLargeBinThreads)
     k_bin_merge_large(const uint32_t* __restrict__ depth_bits, int64_t nbins, int capacity,
                       int32_t* __restrict__ bins, const int32_t* __restrict__ counts,
                       int32_t* d_status) {
-    extern __shared__ uint64_t keys[];
+    extern __shared__ __align__(16) uint64_t keys[];
     for (int64_t b = blockIdx.x; b < nbins; b += gridDim.x) {
         const int cnt = bin_entries<kLargeBinThreads>(b, capacity, counts, d_status);
         if (cnt <= kSmallBin) continue;
         int32_t* bin = bins + b * capacity;
         if (MERGE)
-            merge_sort_bin<kLargeBinThreads>(depth_bits, bin, cnt, keys,
-                                             keys + ((capacity + 63) & ~63));
+            merge_path_sort_bin<kLargeBinThreads>(depth_bits, bin, cnt, keys,
+                                                  keys + ((capacity + 63) & ~63));
         else
             bitonic_sort_bin<kLargeBinThreads>(depth_bits, bin, cnt, keys);
         fill_tail<kLargeBinThreads>(bin, cnt, capacity);
