@@ -1121,22 +1121,35 @@ __global__ void __launch_bounds__(kThreads, GS_BWD_MIN_BLOCKS)
 // ------------------------------------------------ per-pixel step-trace backward
 
 // The backward over the forward's per-pixel step trace (the trace buffers of
-// rlx-metal's traced training step, splat_training.rs): one thread per pixel
-// walks that pixel's recorded pairs from its last to its first -- no other
-// list entry is visited and the transmittance before each pair is read, not
-// recovered by division.  A pixel that composited more pairs than were
-// recorded walks its tile's list from its last id down instead, with the
-// recovery T_before = T / (1 - alpha) (gsplat 1.0.0, raster_backward.c,
+// rlx-metal's traced training step, splat_training.rs): each pixel walks its
+// recorded pairs from its last to its first -- no other list entry is
+// visited and the transmittance before each pair is read, not recovered by
+// division.  A pixel that composited more pairs than were recorded walks its
+// tile's list from its last id down instead, with the recovery T_before =
+// T / (1 - alpha) (gsplat 1.0.0, raster_backward.c,
 // gs_raster_backward_pixel).  Every channel is handled in one pass (colours
-// and upstream gradients read from global memory per pair); each pair adds
-// its terms with global atomics.
+// and upstream gradients read from global memory per pair).
+//
+// One thread per pixel, and the 32 pixels of a warp (two rows of the tile)
+// move through their tile's list together: each round takes the largest
+// list position any lane still has to visit (its next record, or its next
+// entry in the fallback walk), so the lanes at that position all hold the
+// same splat; they run their pair, and the warp sums each gradient term over
+// its lanes before one atomic per field (a lone lane adds its own terms).
 constexpr int kStepThreads = kTile * kTile;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
 template <bool ABS>
 __global__ void __launch_bounds__(kStepThreads)
     k_raster_bwd_steps(RasterArgs a, RasterGrads gr, StepTrace stp) {
     const TileRange tr = tile_range(a);
     const int lx = threadIdx.x & (kTile - 1), ly = threadIdx.x / kTile;
+    const int lane = threadIdx.x & 31;
     const int x = tr.tx * kTile + lx, y = tr.ty * kTile + ly;
     const bool inside = x < a.width && y < a.height;
     const int nch = a.channels;
@@ -1147,99 +1160,129 @@ __global__ void __launch_bounds__(kStepThreads)
     const float* gp = gr.grad_render_colors + p * nch;
     // dL/dbackground: sum over pixels of g (1 - render_alpha), per channel
     if (gr.grad_backgrounds) {
-        const int lane = threadIdx.x & 31;
         for (int c = 0; c < nch; ++c) {
-            float v = inside ? gp[c] * Tfinal : 0.0f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            const float v = warp_sum(inside ? gp[c] * Tfinal : 0.0f);
             if (lane == 0 && v != 0.0f) atomicAdd(&gr.grad_backgrounds[(int64_t)tr.c * nch + c], v);
         }
     }
-    if (!inside || tr.masked || !(ra > 0.0f)) return;
+    const bool live = inside && !tr.masked && ra > 0.0f;
     const float px = (float)x + 0.5f, py = (float)y + 0.5f;
     const int64_t CN = (int64_t)a.C * a.N;
     // Q = g . rem - g_a T_after, from g . background - g_a (see k_raster_bwd)
-    float Q = -gr.grad_render_alphas[p];
-    if (bg)
-        for (int c = 0; c < nch; ++c) Q += gp[c] * bg[c];
-    // the terms of one pair; T_before given, T_after (Tc) the guard
-    auto pair = [&](int32_t g, float t_before, const PairEval& e, float dx, float al) {
-        const float* q = a.conics + 3 * (int64_t)g;
-        const float* col = a.colors + (int64_t)g * nch;
-        const float vis = t_before * al;
-        float gcol = 0.0f;
-        for (int c = 0; c < nch; ++c) {
-            const float t = gp[c] * vis;
-            if (t != 0.0f) atomicAdd(&gr.grad_colors[(int64_t)g * nch + c], t);
-            gcol += gp[c] * col[c];
-        }
-        const float g_alpha = t_before * (gcol - Q);
-        const float g_raw = al > 0.0f && e.raw < kAlphaClamp ? g_alpha : 0.0f;
-        const float g_s = -g_raw * e.raw;
-        if (g_s != 0.0f || g_raw != 0.0f) {
-            atomicAdd(&gr.grad_opacities[g], g_raw * e.resp);
-            const float gmx = g_s * (q[0] * dx + q[1] * e.dy);
-            const float gmy = g_s * (q[2] * e.dy + q[1] * dx);
-            atomicAdd(&gr.grad_means2d[2 * (int64_t)g], gmx);
-            atomicAdd(&gr.grad_means2d[2 * (int64_t)g + 1], gmy);
-            atomicAdd(&gr.grad_conics[3 * (int64_t)g], g_s * (0.5f * dx * dx));
-            atomicAdd(&gr.grad_conics[3 * (int64_t)g + 1], g_s * (dx * e.dy));
-            atomicAdd(&gr.grad_conics[3 * (int64_t)g + 2], g_s * (0.5f * e.dy * e.dy));
-            if (ABS) {
-                atomicAdd(&gr.grad_means2d_abs[2 * (int64_t)g], fabsf(gmx));
-                atomicAdd(&gr.grad_means2d_abs[2 * (int64_t)g + 1], fabsf(gmy));
-            }
-        }
-        Q = al * gcol + (1.0f - al) * Q;
-    };
-    auto eval_at = [&](int32_t g, float& dx) {
-        const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
-        const float* q = a.conics + 3 * (int64_t)g;
-        const ColumnTerms ct = column_terms(m.x, q[0], q[1], px);
-        dx = ct.dx;
-        return eval_pair(ct, m.y, q[2], a.opacities[g], py);
-    };
-    const int n = stp.count[p];
-    if (n <= stp.max_steps) {
-        // the recorded pairs, last to first; each was composited by the
-        // forward with these same operations, so only the T < 1 guard of the
-        // reverse walk remains to test
-        float Tc = Tfinal;
-        for (int s2 = n - 1; s2 >= 0; --s2) {
-            const int64_t o = (int64_t)s2 * stp.npix + p;
+    float Q = 0.0f;
+    if (live) {
+        Q = -gr.grad_render_alphas[p];
+        if (bg)
+            for (int c = 0; c < nch; ++c) Q += gp[c] * bg[c];
+    }
+    const int n = live ? stp.count[p] : 0;
+    // rec: the records hold every pair of the pixel; else the list walk
+    const bool rec = n <= stp.max_steps;
+    // the lane's next list position to visit (-1: none left) and, from a
+    // record, the transmittance before that pair
+    int32_t cur = -1;
+    float t_rec = 0.0f;
+    int s_next = n - 1;  // next record to read
+    auto next_record = [&]() {
+        cur = -1;
+        while (s_next >= 0) {
+            const int64_t o = (int64_t)s_next * stp.npix + p;
+            --s_next;
             const int32_t j = stp.pos[o];
-            const float t_before = stp.T[o];
             if (j < 0 || j >= a.n_isects) {  // only from a corrupted trace
                 GS_BOUNDS_REPORT(a.d_status);
                 continue;
             }
-            const int32_t g = a.flatten_ids[j];
-            if ((uint64_t)g >= (uint64_t)CN) {
-                GS_BOUNDS_REPORT(a.d_status);
-                continue;
-            }
-            float dx;
-            const PairEval e = eval_at(g, dx);
-            const float al = Tc < 1.0f ? e.alpha : 0.0f;
-            pair(g, t_before, e, dx, al);
-            Tc = t_before;
+            cur = j;
+            t_rec = stp.T[o];
+            return;
         }
-    } else {
-        // more pairs than records: the pixel's list walk, last id down
-        const int32_t last = gr.last_ids[p];
-        const int64_t hi = min((int64_t)last, tr.end - 1);
-        float Tc = Tfinal;
-        for (int64_t j = hi; j >= tr.start; --j) {
-            const int32_t g = a.flatten_ids[j];
-            if ((uint64_t)g >= (uint64_t)CN) {
-                GS_BOUNDS_REPORT(a.d_status);
-                continue;
+    };
+    if (live) {
+        if (rec) {
+            next_record();
+        } else {
+            const int64_t hi = min((int64_t)gr.last_ids[p], tr.end - 1);
+            cur = hi >= tr.start ? (int32_t)hi : -1;
+        }
+    }
+    float Tc = Tfinal;
+    while (true) {
+        const int32_t j = __reduce_max_sync(0xffffffffu, cur);
+        if (j < 0) break;
+        const bool mine = cur == j;
+        // the entry's splat, the same for every lane
+        const int32_t g = a.flatten_ids[j];
+        const bool g_ok = (uint64_t)g < (uint64_t)CN;
+        if (!g_ok && lane == 0) GS_BOUNDS_REPORT(a.d_status);
+        bool take = false;
+        float t_before = 0.0f, al = 0.0f, dx = 0.0f;
+        PairEval e{0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        float q0 = 0.0f, q1 = 0.0f, q2 = 0.0f;
+        if (g_ok) {
+            const float2 m = reinterpret_cast<const float2*>(a.means2d)[g];
+            const float* q = a.conics + 3 * (int64_t)g;
+            q0 = q[0];
+            q1 = q[1];
+            q2 = q[2];
+            if (mine) {
+                const ColumnTerms ct = column_terms(m.x, q0, q1, px);
+                dx = ct.dx;
+                e = eval_pair(ct, m.y, q2, a.opacities[g], py);
+                if (rec) {
+                    // each record was composited by the forward with these
+                    // same operations: only the T < 1 guard remains to test
+                    al = Tc < 1.0f ? e.alpha : 0.0f;
+                    t_before = t_rec;
+                    take = true;
+                } else if (e.s >= 0.0f && e.alpha >= a.alpha_cutoff && Tc < 1.0f) {
+                    al = e.alpha;
+                    t_before = Tc / (1.0f - e.alpha);
+                    take = true;
+                }
             }
-            float dx;
-            const PairEval e = eval_at(g, dx);
-            if (!(e.s >= 0.0f && e.alpha >= a.alpha_cutoff && Tc < 1.0f)) continue;
-            const float t_before = Tc / (1.0f - e.alpha);
-            pair(g, t_before, e, dx, e.alpha);
+        }
+        if (mine) {
+            if (rec) next_record();
+            else cur = cur - 1 >= tr.start ? cur - 1 : -1;
+        }
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (tm == 0u) continue;
+        const bool lone = (tm & (tm - 1u)) == 0u;
+        // one field's terms into the splat's gradient
+        auto add = [&](float* dst, float v) {
+            if (lone) {
+                if (take && v != 0.0f) atomicAdd(dst, v);
+            } else {
+                v = warp_sum(v);
+                if (lane == 0 && v != 0.0f) atomicAdd(dst, v);
+            }
+        };
+        const float* col = a.colors + (int64_t)g * nch;
+        const float vis = t_before * al;
+        float gcol = 0.0f;
+        for (int c = 0; c < nch; ++c) {
+            const float gc = take ? gp[c] : 0.0f;
+            add(&gr.grad_colors[(int64_t)g * nch + c], gc * vis);
+            gcol += gc * col[c];
+        }
+        const float g_alpha = t_before * (gcol - Q);
+        const float g_raw = take && al > 0.0f && e.raw < kAlphaClamp ? g_alpha : 0.0f;
+        const float g_s = -g_raw * e.raw;
+        const float gmx = g_s * (q0 * dx + q1 * e.dy);
+        const float gmy = g_s * (q2 * e.dy + q1 * dx);
+        add(&gr.grad_opacities[g], g_raw * e.resp);
+        add(&gr.grad_means2d[2 * (int64_t)g], gmx);
+        add(&gr.grad_means2d[2 * (int64_t)g + 1], gmy);
+        add(&gr.grad_conics[3 * (int64_t)g], g_s * (0.5f * dx * dx));
+        add(&gr.grad_conics[3 * (int64_t)g + 1], g_s * (dx * e.dy));
+        add(&gr.grad_conics[3 * (int64_t)g + 2], g_s * (0.5f * e.dy * e.dy));
+        if (ABS) {
+            add(&gr.grad_means2d_abs[2 * (int64_t)g], fabsf(gmx));
+            add(&gr.grad_means2d_abs[2 * (int64_t)g + 1], fabsf(gmy));
+        }
+        if (take) {
+            Q = al * gcol + (1.0f - al) * Q;
             Tc = t_before;
         }
     }
