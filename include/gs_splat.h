@@ -368,9 +368,10 @@ int gs_rasterize_bwd(const float* means2d, const float* conics,
  * revisited and T before each pair is read instead of recovered by a
  * division; a pixel whose step_count exceeds max_steps walks its tile's list
  * from its last id down instead, recovering T_before = T / (1 - alpha) as
- * gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel does.  Each pair
- * adds its terms with global atomics (an alternative to the mask-trace
- * backward, whose per-entry reduction is cheaper; both are measured).
+ * gsplat 1.0.0, raster_backward.c, gs_raster_backward_pixel does.  The
+ * pixels of a warp walk in step by list position, and each pair's terms are
+ * summed over the warp before one global atomic per field (an alternative
+ * to the mask-trace backward, which is cheaper; both are measured).
  * Limits: max_steps >= 1 and max_steps * C * H * W < 2^40; otherwise as the
  * forward and backward above.
  */
