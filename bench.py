@@ -457,7 +457,7 @@ def run_ours(args, rank, world, scene):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic (seeded workload 3 generator)",
+        "data": f"synthetic (seeded workload {args.workload} generator)",
         "config": workload_config(s, I, max_list, world),
         "msplat_isect_per_s": round(I / (isect_ms * 1e-3) / 1e6, 1),
         "msplat_per_s": round(s.C * s.N / (ms * 1e-3) / 1e6, 1),
